@@ -1,0 +1,261 @@
+"""Python binding of libddpbucket (the C ABI in include/ddp_bucket.h).
+
+Argument marshalling only: every step of the path -- bucket assignment, pack,
+ring-ordered reduction, unpack, scheduling -- runs in the library (host C++ and
+sm_103a kernels).  PyTorch supplies device memory and streams.  The library is
+loaded on first use; if it has not been built, every call raises.
+
+Functions keep the C names.  Device arguments accept a torch tensor (its
+data_ptr is passed), an integer address, or None (NULL).  A non-OK status
+raises DdpError carrying the status and the library's message.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import _build
+
+# status codes, dtypes, orders, modes, reducer flags (mirror the header)
+DDP_OK, DDP_E_INVAL, DDP_E_ALIGN, DDP_E_CUDA, DDP_E_STATE, DDP_E_INCOMPLETE, DDP_E_TIMEOUT, DDP_E_CAPACITY = range(8)
+DDP_F32, DDP_BF16, DDP_F16 = 0, 1, 2
+DDP_ORDER_REVERSE, DDP_ORDER_FWD_THEN_REVERSE, DDP_ORDER_MEGATRON = 0, 1, 2
+DDP_ALLREDUCE, DDP_REDUCE_SCATTER = 0, 1
+DDP_R_FUSED, DDP_R_COPY_BACK, DDP_R_TIMING, DDP_R_DRY_RUN = 1, 2, 4, 8
+
+
+class DdpError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+class BucketDesc(C.Structure):
+    """ddp_bucket_desc: host struct holding device table pointers."""
+    _fields_ = [("numel", C.c_int64), ("nseg", C.c_int32), ("dtype", C.c_int32),
+                ("seg_offset", C.c_void_p), ("seg_param", C.c_void_p)]
+
+
+_i64p = C.POINTER(C.c_int64)
+_i32p = C.POINTER(C.c_int32)
+_vp = C.c_void_p
+_LIB = None
+
+_SIGS = {
+    "ddp_assign_buckets": (C.c_int32, [_i64p, _i32p, C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
+                                       C.c_int32, _i32p, _i64p, _i32p, _i64p, _i64p, _i32p, _i32p, C.c_int32,
+                                       _i32p]),
+    "ddp_pack": (C.c_int32, [C.POINTER(BucketDesc), _vp, _vp, C.c_int32, C.c_int32, _vp, C.c_int64, C.c_int32, _vp]),
+    "ddp_bucket_allreduce": (C.c_int32, [_vp, C.c_int64, C.c_int64, C.c_int32, C.c_int32, _vp]),
+    "ddp_unpack": (C.c_int32, [C.POINTER(BucketDesc), _vp, C.c_int64, C.c_int32, C.c_int32, _vp, C.c_int32, _vp,
+                               _vp]),
+    "ddp_fused_bucket": (C.c_int32, [C.POINTER(BucketDesc), _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+                                     _vp, C.c_int64, _vp, _vp, _vp]),
+    "ddp_reducer_create": (C.c_int32, [C.c_int32, C.c_int32, _i32p, _i32p, C.POINTER(BucketDesc), _i64p, C.c_int32,
+                                       C.c_int32, C.c_int32, _vp, _vp, C.c_int32, _vp, C.c_int64, _vp, _vp, _vp,
+                                       C.POINTER(_vp)]),
+    "ddp_reducer_prepare": (C.c_int32, [_vp, C.c_int32]),
+    "ddp_reducer_mark_ready": (C.c_int32, [_vp, C.c_int32, _vp]),
+    "ddp_reducer_mark_ready_many": (C.c_int32, [_vp, _i32p, C.c_int32, _vp]),
+    "ddp_reducer_finalize": (C.c_int32, [_vp, _vp, C.c_int64]),
+    "ddp_reducer_issue_log": (C.c_int32, [_vp, _i32p, C.c_int32, _i32p]),
+    "ddp_reducer_bucket_ms": (C.c_int32, [_vp, C.POINTER(C.c_float), C.c_int32]),
+    "ddp_reducer_destroy": (None, [_vp]),
+    "ddp_status_str": (C.c_char_p, [C.c_int32]),
+    "ddp_last_error_message": (C.c_char_p, []),
+    "ddp_version": (C.c_int32, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libddpbucket; raises if it was never built (no fallback exists)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libddpbucket is not built ({path} missing): run __graft_entry__.build() "
+                               "or python -m allreduce_ddp_assign_gb300._build")
+        h = C.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = h
+    return _LIB
+
+
+def _status_name(s: int) -> str:
+    try:
+        return lib().ddp_status_str(s).decode()
+    except Exception:  # pragma: no cover - library missing
+        return f"status {s}"
+
+
+def _check(status: int) -> None:
+    if status != DDP_OK:
+        raise DdpError(status, lib().ddp_last_error_message().decode())
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() or None
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream or None
+        except Exception:
+            pass
+        return None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+def _a(x, dt):
+    return np.ascontiguousarray(x, dtype=dt)
+
+
+def _cp(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+# ---------------------------------------------------------------------------
+# step 1
+# ---------------------------------------------------------------------------
+def ddp_assign_buckets(numels, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=1 << 20, order=DDP_ORDER_REVERSE,
+                       pad_multiple=1, grad_reduce_in_fp32=1) -> dict:
+    numels = _a(numels, np.int64)
+    P = len(numels)
+    dtypes = np.zeros(P, np.int32) if dtypes is None else _a(dtypes, np.int32)
+    cap = P + 2
+    out = dict(bucket_of=np.zeros(P, np.int32), offset_of=np.zeros(P, np.int64), members=np.zeros(max(P, 1), np.int32),
+               bucket_numel=np.zeros(cap, np.int64), bucket_bytes=np.zeros(cap, np.int64),
+               bucket_dtype=np.zeros(cap, np.int32), bucket_order=np.zeros(cap, np.int32))
+    nb = C.c_int32(0)
+    _check(lib().ddp_assign_buckets(_cp(numels, _i64p), _cp(dtypes, _i32p), P, int(cap_bytes), int(first_cap_bytes),
+                                    int(order), int(pad_multiple), int(grad_reduce_in_fp32),
+                                    _cp(out["bucket_of"], _i32p), _cp(out["offset_of"], _i64p),
+                                    _cp(out["members"], _i32p), _cp(out["bucket_numel"], _i64p),
+                                    _cp(out["bucket_bytes"], _i64p), _cp(out["bucket_dtype"], _i32p),
+                                    _cp(out["bucket_order"], _i32p), cap, C.byref(nb)))
+    B = nb.value
+    for k in ("bucket_numel", "bucket_bytes", "bucket_dtype", "bucket_order"):
+        out[k] = out[k][:B].copy()
+    out["members"] = out["members"][:P].copy()
+    out["nbuckets"] = B
+    return out
+
+
+# ---------------------------------------------------------------------------
+# steps 2-4
+# ---------------------------------------------------------------------------
+def ddp_pack(desc: BucketDesc, grads, used, ld, W, main_grad, replica_stride, accumulate=0, stream=None) -> None:
+    _check(lib().ddp_pack(C.byref(desc), _ptr(grads), _ptr(used), int(ld), int(W), _ptr(main_grad),
+                          int(replica_stride), int(accumulate), _stream(stream)))
+
+
+def ddp_bucket_allreduce(replicas, replica_stride, numel, W, mode=DDP_ALLREDUCE, stream=None) -> None:
+    _check(lib().ddp_bucket_allreduce(_ptr(replicas), int(replica_stride), int(numel), int(W), int(mode),
+                                      _stream(stream)))
+
+
+def ddp_unpack(desc: BucketDesc, main_grad, replica_stride, W, mode, grads_out, ld, global_used=None,
+               stream=None) -> None:
+    _check(lib().ddp_unpack(C.byref(desc), _ptr(main_grad), int(replica_stride), int(W), int(mode),
+                            _ptr(grads_out), int(ld), _ptr(global_used), _stream(stream)))
+
+
+def ddp_fused_bucket(desc: BucketDesc, grads, used, ld, W, mode, accumulate, main_grad, replica_stride,
+                     grads_out=None, global_used=None, stream=None) -> None:
+    _check(lib().ddp_fused_bucket(C.byref(desc), _ptr(grads), _ptr(used), int(ld), int(W), int(mode),
+                                  int(accumulate), _ptr(main_grad), int(replica_stride), _ptr(grads_out),
+                                  _ptr(global_used), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# step 5
+# ---------------------------------------------------------------------------
+def ddp_reducer_create(nparams, bucket_of, bucket_order, descs, bucket_start, W, mode, flags, grads=None, used=None,
+                       ld=0, main_grad=None, replica_stride=0, grads_out=None, global_used=None, side_stream=None):
+    bucket_of = _a(bucket_of, np.int32)
+    bucket_order = _a(bucket_order, np.int32)
+    bucket_start = _a(bucket_start, np.int64)
+    B = len(bucket_order)
+    arr = (BucketDesc * max(B, 1))(*descs)
+    h = _vp()
+    side = None if flags & DDP_R_DRY_RUN else _stream(side_stream)
+    _check(lib().ddp_reducer_create(int(nparams), B, _cp(bucket_of, _i32p), _cp(bucket_order, _i32p), arr,
+                                    _cp(bucket_start, _i64p), int(W), int(mode), int(flags), _ptr(grads), _ptr(used),
+                                    int(ld), _ptr(main_grad), int(replica_stride), _ptr(grads_out), _ptr(global_used),
+                                    side, C.byref(h)))
+    return h.value
+
+
+def ddp_reducer_prepare(r, accumulate=0) -> None:
+    _check(lib().ddp_reducer_prepare(r, int(accumulate)))
+
+
+def ddp_reducer_mark_ready(r, param, producer_stream=None) -> None:
+    _check(lib().ddp_reducer_mark_ready(r, int(param), _stream(producer_stream)))
+
+
+def ddp_reducer_mark_ready_many(r, params, producer_stream=None) -> None:
+    params = _a(params, np.int32)
+    _check(lib().ddp_reducer_mark_ready_many(r, _cp(params, _i32p), len(params), _stream(producer_stream)))
+
+
+def ddp_reducer_finalize(r, consumer_stream=None, timeout_us=0) -> None:
+    _check(lib().ddp_reducer_finalize(r, _stream(consumer_stream), int(timeout_us)))
+
+
+def ddp_reducer_issue_log(r, cap=4096) -> list:
+    out = np.zeros(cap, np.int32)
+    n = C.c_int32(0)
+    _check(lib().ddp_reducer_issue_log(r, _cp(out, _i32p), cap, C.byref(n)))
+    return [int(v) for v in out[:n.value]]
+
+
+def ddp_reducer_bucket_ms(r, nbuckets) -> np.ndarray:
+    out = np.zeros(max(nbuckets, 1), np.float32)
+    _check(lib().ddp_reducer_bucket_ms(r, out.ctypes.data_as(C.POINTER(C.c_float)), len(out)))
+    return out[:nbuckets]
+
+
+def ddp_reducer_destroy(r) -> None:
+    if r:
+        lib().ddp_reducer_destroy(r)
+
+
+def ddp_status_str(s: int) -> str:
+    return lib().ddp_status_str(int(s)).decode()
+
+
+def ddp_last_error_message() -> str:
+    return lib().ddp_last_error_message().decode()
+
+
+def ddp_version() -> int:
+    return int(lib().ddp_version())
+
+
+from .plan import Plan  # noqa: E402  (plumbing over the calls above)
+
+__all__ = [n for n in _SIGS] + ["Plan", "BucketDesc", "DdpError", "lib", "library_path"]

@@ -1,0 +1,29 @@
+// Internal helpers shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cstdarg>
+#include <cstdint>
+
+#include "ddp_bucket.h"
+
+namespace ddp {
+
+// Record the calling thread's error message and return `code`.
+ddp_status fail(ddp_status code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+// Clear the calling thread's message and return DDP_OK.
+ddp_status ok();
+
+constexpr int32_t kMaxReplicas = 64;
+
+// Device data-path launchers (kernels.cu); arguments are already validated.
+ddp_status launch_pack(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
+                       int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream);
+ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream);
+ddp_status launch_unpack(const ddp_bucket_desc& b, const float* main_grad, int64_t stride, int32_t W,
+                         int32_t mode, void* const* grads_out, int32_t ld, const uint8_t* global_used,
+                         void* stream);
+ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
+                        int32_t W, int32_t mode, int32_t accumulate, float* main_grad, int64_t stride,
+                        void* const* grads_out, const uint8_t* global_used, void* stream);
+
+}  // namespace ddp

@@ -1,0 +1,586 @@
+// Steps 2-4 of the path on the GPU: pack, ring-ordered reduction with the 1/W
+// scale, unpack, and the three fused into one pass.
+//
+// Sources: "DDP: ring AllReduce and gradient buckets" sections 17.4 (ring
+// allreduce = reduce-scatter then all-gather, 1/N of the data per step), 17.9
+// (each contribution multiplied by 1/world_size), 17.12 (copy into the
+// bucket); "Megatron DDP: contiguous buffer and overlap" sections 1 (fp32
+// main_grad, bf16 gradients widened) and 3 (reduce_scatter leaves shard r on
+// rank r).
+//
+// Every kernel is one template, bucket_kernel<OP, WT, DT>: the grid splits
+// the bucket's elements into equal contiguous slices, one per CTA.  A CTA
+// walks its slice in "pieces", cut wherever a ring chunk or a parameter
+// segment ends, so that within a piece the chunk c (hence the ring order) and
+// the source tensors are fixed.  The W replicas' pointers of the piece are
+// staged in shared memory.  Aligned pieces stream 16-byte vectors
+// (ld/st.global.cs: each byte is touched once); the rest takes scalar,
+// still coalesced, accesses.  HBM-bound: no tensor cores (nothing is a
+// contraction).
+//
+// Bit-exactness: for an element of chunk c the W scaled values are summed in
+// ring order c+1, c+2, ..., c with __fmul_rn / __fadd_rn (no FMA
+// contraction), the first term taken as is -- the additions the ring's
+// reduce-scatter performs, in its order.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "common.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int64_t kMinElemsPerCta = 4096;
+
+enum Op { OP_RING = 0, OP_PACK = 1, OP_FUSED = 2, OP_UNPACK = 3 };
+
+struct Ctx {
+    int64_t n;          // bucket elements, padding included
+    int64_t chunk;      // ring chunk length (n when the op has no ring order)
+    int32_t nchunks;    // W for ring-ordered ops, 1 otherwise
+    int32_t W;
+    int32_t mode;
+    int32_t accumulate;
+    float inv_w;
+    int32_t nseg;       // 0 with seg_offset == nullptr: the whole bucket is one piece
+    const int64_t* seg_offset;
+    const int32_t* seg_param;
+    int32_t ld;
+    const void* const* grads;
+    const uint8_t* used;
+    void* const* grads_out;
+    const uint8_t* global_used;
+    float* mg;          // replica 0 of the bucket (main_grad), may be null for OP_FUSED
+    int64_t stride;     // elements between replicas of mg
+    int32_t mg_vec;     // every replica of mg is 16-byte aligned
+};
+
+struct PieceShared {
+    const void* src[ddp::kMaxReplicas];  // replica w's gradient of the piece's parameter, or null
+    float* dst[ddp::kMaxReplicas];       // replica w's output of that parameter, or null
+};
+
+// ---------------------------------------------------------------------------
+// element access
+// ---------------------------------------------------------------------------
+template <int VEC> struct Lane;
+
+template <> struct Lane<4> {
+    using T = float4;
+    __device__ __forceinline__ static T zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ static T ld(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+    __device__ __forceinline__ static void st(float* p, T v) { __stcs(reinterpret_cast<float4*>(p), v); }
+    __device__ __forceinline__ static T mul(T a, float s)
+    {
+        return make_float4(__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(a.z, s), __fmul_rn(a.w, s));
+    }
+    __device__ __forceinline__ static T add(T a, T b)
+    {
+        return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+    }
+    template <int DT> __device__ __forceinline__ static T ldg(const void* base, int64_t i);
+};
+
+template <> __device__ __forceinline__ float4 Lane<4>::ldg<DDP_F32>(const void* base, int64_t i)
+{
+    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+}
+template <> __device__ __forceinline__ float4 Lane<4>::ldg<DDP_BF16>(const void* base, int64_t i)
+{
+    // bf16 -> fp32 widening is exact: the bf16 bits become the upper half
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+template <> __device__ __forceinline__ float4 Lane<4>::ldg<DDP_F16>(const void* base, int64_t i)
+{
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i));
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+template <> struct Lane<1> {
+    using T = float;
+    __device__ __forceinline__ static T zero() { return 0.f; }
+    __device__ __forceinline__ static T ld(const float* p) { return __ldcs(p); }
+    __device__ __forceinline__ static void st(float* p, T v) { __stcs(p, v); }
+    __device__ __forceinline__ static T mul(T a, float s) { return __fmul_rn(a, s); }
+    __device__ __forceinline__ static T add(T a, T b) { return __fadd_rn(a, b); }
+    template <int DT> __device__ __forceinline__ static T ldg(const void* base, int64_t i);
+};
+
+template <> __device__ __forceinline__ float Lane<1>::ldg<DDP_F32>(const void* base, int64_t i)
+{
+    return __ldcs(static_cast<const float*>(base) + i);
+}
+template <> __device__ __forceinline__ float Lane<1>::ldg<DDP_BF16>(const void* base, int64_t i)
+{
+    return __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short*>(base) + i)) << 16);
+}
+template <> __device__ __forceinline__ float Lane<1>::ldg<DDP_F16>(const void* base, int64_t i)
+{
+    return __half2float(__ushort_as_half(__ldcs(static_cast<const unsigned short*>(base) + i)));
+}
+
+__host__ __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t lmax(int64_t a, int64_t b) { return a > b ? a : b; }
+
+template <int DT> __host__ __device__ constexpr int elem_bytes() { return DT == DDP_F32 ? 4 : 2; }
+
+// Loads per thread kept in flight: about 16 vectors whatever W is.
+template <int WT> __host__ __device__ constexpr int unroll_for()
+{
+    return WT == 2 ? 4 : (WT == 4 ? 2 : 1);
+}
+
+// ---------------------------------------------------------------------------
+// one piece: elements [a, b) of chunk c, inside one segment (or the padding)
+// ---------------------------------------------------------------------------
+// Processes elements e0 + VEC*v, v in [0, count).  `off` is the segment's
+// first bucket element (gradient index i = e - off).
+template <int OP, int WT, int DT, int VEC, int U>
+__device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, int c, int64_t e0, int64_t count,
+                                          int64_t off)
+{
+    using L = Lane<VEC>;
+    using T = typename L::T;
+    const int W = WT ? WT : cx.W;
+    const int64_t step = static_cast<int64_t>(kThreads) * U;
+    for (int64_t v0 = threadIdx.x; v0 < count; v0 += step) {
+        int64_t e[U];
+        bool live[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + static_cast<int64_t>(u) * kThreads;
+            live[u] = v < count;
+            e[u] = e0 + static_cast<int64_t>(VEC) * v;
+        }
+
+        if constexpr (OP == OP_RING || OP == OP_FUSED) {
+            T acc[U];
+            // value of replica r at element x (before scaling)
+            auto value = [&](int r, int64_t x) -> T {
+                if constexpr (OP == OP_RING) {
+                    return L::ld(cx.mg + r * cx.stride + x);
+                } else {
+                    const void* src = sh.src[r];
+                    if (cx.accumulate) {
+                        const T m = L::ld(cx.mg + r * cx.stride + x);
+                        return src ? L::add(m, L::template ldg<DT>(src, x - off)) : m;
+                    }
+                    return src ? L::template ldg<DT>(src, x - off) : L::zero();
+                }
+            };
+            auto term = [&](int k) {
+                int r = c + 1 + k;  // ring order: c+1, c+2, ..., c
+                if (r >= W) r -= W;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (!live[u]) continue;
+                    const T t = L::mul(value(r, e[u]), cx.inv_w);
+                    acc[u] = (k == 0) ? t : L::add(acc[u], t);
+                }
+            };
+            if constexpr (WT > 0) {
+#pragma unroll
+                for (int k = 0; k < WT; ++k) term(k);
+            } else {
+#pragma unroll 4
+                for (int k = 0; k < W; ++k) term(k);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (!live[u]) continue;
+                if (cx.mg) {
+                    if (cx.mode == DDP_ALLREDUCE) {
+                        for (int w = 0; w < W; ++w) L::st(cx.mg + w * cx.stride + e[u], acc[u]);
+                    } else {
+                        L::st(cx.mg + c * cx.stride + e[u], acc[u]);
+                    }
+                }
+                if constexpr (OP == OP_FUSED) {
+                    if (cx.mode == DDP_ALLREDUCE) {
+                        for (int w = 0; w < W; ++w)
+                            if (sh.dst[w]) L::st(sh.dst[w] + (e[u] - off), acc[u]);
+                    } else if (sh.dst[c]) {
+                        L::st(sh.dst[c] + (e[u] - off), acc[u]);
+                    }
+                }
+            }
+        } else if constexpr (OP == OP_PACK) {
+            for (int w = 0; w < W; ++w) {
+                const void* src = sh.src[w];
+                if (cx.accumulate && !src) continue;  // no gradient: the bucket keeps its sum
+                float* row = cx.mg + w * cx.stride;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (!live[u]) continue;
+                    T t = src ? L::template ldg<DT>(src, e[u] - off) : L::zero();
+                    if (cx.accumulate) t = L::add(L::ld(row + e[u]), t);
+                    L::st(row + e[u], t);
+                }
+            }
+        } else {  // OP_UNPACK
+            for (int w = 0; w < W; ++w) {
+                if (cx.mode == DDP_REDUCE_SCATTER && w != c) continue;
+                float* dst = sh.dst[w];
+                if (!dst) continue;
+                const float* row = cx.mg + w * cx.stride;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (live[u]) L::st(dst + (e[u] - off), L::ld(row + e[u]));
+            }
+        }
+    }
+}
+
+// Stage the piece's pointers; returns nonzero (on every thread) when all of
+// them allow 16-byte vectors.  Contains two block-wide barriers.
+template <int OP, int DT>
+__device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int s, int64_t off)
+{
+    __syncthreads();  // the previous piece is done reading sh
+    int ok = 1;
+    const int t = threadIdx.x;
+    if (t < cx.W) {
+        const void* src = nullptr;
+        float* dst = nullptr;
+        const int p = (cx.seg_offset && s < cx.nseg) ? cx.seg_param[s] : -1;
+        if (p >= 0 && p < cx.ld) {
+            const int64_t slot = static_cast<int64_t>(t) * cx.ld + p;
+            if constexpr (OP == OP_PACK || OP == OP_FUSED) {
+                if (!cx.used || cx.used[slot]) src = cx.grads[slot];
+            }
+            if constexpr (OP == OP_UNPACK || OP == OP_FUSED) {
+                if (cx.grads_out && (!cx.global_used || cx.global_used[p]))
+                    dst = static_cast<float*>(cx.grads_out[slot]);
+            }
+        }
+        sh.src[t] = src;
+        sh.dst[t] = dst;
+        // vectors at bucket elements e = 0 mod 4 read gradient index e - off
+        constexpr int64_t gb = elem_bytes<DT>();
+        if (src && ((reinterpret_cast<uintptr_t>(src) - static_cast<uintptr_t>(off * gb)) % (4 * gb)) != 0) ok = 0;
+        if (dst && ((reinterpret_cast<uintptr_t>(dst) - static_cast<uintptr_t>(off * 4)) % 16) != 0) ok = 0;
+    }
+    return __syncthreads_and(ok) && (cx.mg == nullptr || cx.mg_vec);
+}
+
+template <int OP, int WT, int DT>
+__device__ __forceinline__ void process_piece(const Ctx& cx, PieceShared& sh, int c, int s, int64_t off, int64_t a,
+                                              int64_t b)
+{
+    constexpr int U = unroll_for<WT>();
+    if (piece_setup<OP, DT>(cx, sh, s, off)) {
+        const int64_t va = lmin(b, (a + 3) & ~int64_t(3));
+        const int64_t vb = lmax(va, b & ~int64_t(3));
+        run_range<OP, WT, DT, 1, 1>(cx, sh, c, a, va - a, off);
+        run_range<OP, WT, DT, 4, U>(cx, sh, c, va, (vb - va) >> 2, off);
+        run_range<OP, WT, DT, 1, 1>(cx, sh, c, vb, b - vb, off);
+    } else {
+        run_range<OP, WT, DT, 1, 4>(cx, sh, c, a, b - a, off);
+    }
+}
+
+template <int OP, int WT, int DT>
+__global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
+{
+    __shared__ PieceShared sh;
+    const int64_t G = gridDim.x;
+    const int64_t blk = blockIdx.x;
+    // this CTA's slice of the bucket, boundaries on 16-element multiples
+    const int64_t lo = (blk * cx.n / G) & ~int64_t(15);
+    const int64_t hi = (blk + 1 == G) ? cx.n : (((blk + 1) * cx.n / G) & ~int64_t(15));
+    if (lo >= hi) return;  // whole CTA: no barrier is skipped by part of it
+
+    int c = static_cast<int>(lo / cx.chunk);
+    if (c >= cx.nchunks) c = cx.nchunks - 1;
+    int s = 0;
+    if (cx.seg_offset) {  // segment holding lo: last s with seg_offset[s] <= lo (s == nseg: padding)
+        int lo_i = 0, hi_i = cx.nseg + 1;
+        while (hi_i - lo_i > 1) {
+            const int mid = (lo_i + hi_i) >> 1;
+            if (cx.seg_offset[mid] <= lo) lo_i = mid; else hi_i = mid;
+        }
+        s = lo_i;
+    }
+    int64_t a = lo;
+    while (a < hi) {
+        const int64_t c_end = (c + 1 >= cx.nchunks) ? cx.n : lmin(static_cast<int64_t>(c + 1) * cx.chunk, cx.n);
+        int64_t s_off = 0, s_end = cx.n;
+        if (cx.seg_offset) {
+            s_off = cx.seg_offset[s];
+            s_end = (s < cx.nseg) ? cx.seg_offset[s + 1] : cx.n;
+        }
+        const int64_t b = lmin(hi, lmin(c_end, s_end));
+        if (b > a) process_piece<OP, WT, DT>(cx, sh, c, s, s_off, a, b);
+        a = lmax(a, b);
+        while (c + 1 < cx.nchunks && static_cast<int64_t>(c + 1) * cx.chunk <= a) ++c;
+        if (cx.seg_offset)
+            while (s < cx.nseg && cx.seg_offset[s + 1] <= a) ++s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 132;
+    }
+    return cached[dev];
+}
+
+template <int OP, int WT, int DT>
+ddp_status launch_instance(const Ctx& cx, void* stream)
+{
+    static int blocks_per_sm = 0;
+    auto kern = bucket_kernel<OP, WT, DT>;
+    if (!blocks_per_sm) {
+        int v = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, 0) != cudaSuccess || v < 1) v = 1;
+        blocks_per_sm = v;
+    }
+    const int64_t want = (cx.n + kMinElemsPerCta - 1) / kMinElemsPerCta;
+    const int64_t room = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min(want, room)));
+    kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(cx);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "kernel launch failed: %s", cudaGetErrorString(err));
+    return ddp::ok();
+}
+
+template <int OP, int DT>
+ddp_status dispatch_w(const Ctx& cx, void* stream)
+{
+    switch (cx.W) {
+    case 2: return launch_instance<OP, 2, DT>(cx, stream);
+    case 4: return launch_instance<OP, 4, DT>(cx, stream);
+    case 8: return launch_instance<OP, 8, DT>(cx, stream);
+    case 16: return launch_instance<OP, 16, DT>(cx, stream);
+    default: return launch_instance<OP, 0, DT>(cx, stream);
+    }
+}
+
+template <int OP>
+ddp_status dispatch(const Ctx& cx, int32_t dtype, void* stream)
+{
+    if constexpr (OP == OP_RING || OP == OP_UNPACK) {
+        return dispatch_w<OP, DDP_F32>(cx, stream);  // no gradient is read
+    } else {
+        switch (dtype) {
+        case DDP_BF16: return dispatch_w<OP, DDP_BF16>(cx, stream);
+        case DDP_F16: return dispatch_w<OP, DDP_F16>(cx, stream);
+        default: return dispatch_w<OP, DDP_F32>(cx, stream);
+        }
+    }
+}
+
+Ctx base_ctx(int64_t n, int32_t W, bool ring_order, int32_t mode)
+{
+    Ctx cx{};
+    cx.n = n;
+    cx.W = W;
+    cx.mode = mode;
+    cx.inv_w = 1.0f / static_cast<float>(W);
+    if (ring_order) {
+        cx.nchunks = W;
+        cx.chunk = std::max<int64_t>(1, (n + W - 1) / W);
+    } else {
+        cx.nchunks = 1;
+        cx.chunk = std::max<int64_t>(1, n);
+    }
+    return cx;
+}
+
+void set_segments(Ctx& cx, const ddp_bucket_desc& b)
+{
+    cx.nseg = b.nseg;
+    cx.seg_offset = b.nseg > 0 ? b.seg_offset : nullptr;
+    cx.seg_param = b.seg_param;
+}
+
+void set_mg(Ctx& cx, float* mg, int64_t stride)
+{
+    cx.mg = mg;
+    cx.stride = stride;
+    cx.mg_vec = mg && (reinterpret_cast<uintptr_t>(mg) % 16 == 0) && (stride % 4 == 0);
+}
+
+}  // namespace
+
+namespace ddp {
+
+ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream)
+{
+    if (n == 0 || W == 1) return ok();  // the mean of one replica is the replica (x * 1 is exact)
+    Ctx cx = base_ctx(n, W, true, mode);
+    set_mg(cx, replicas, stride);
+    return dispatch<OP_RING>(cx, DDP_F32, stream);
+}
+
+ddp_status launch_pack(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
+                       int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream)
+{
+    if (b.numel == 0) return ok();
+    Ctx cx = base_ctx(b.numel, W, false, DDP_ALLREDUCE);
+    set_segments(cx, b);
+    set_mg(cx, main_grad, stride);
+    cx.ld = ld;
+    cx.grads = grads;
+    cx.used = used;
+    cx.accumulate = accumulate != 0;
+    return dispatch<OP_PACK>(cx, b.dtype, stream);
+}
+
+ddp_status launch_unpack(const ddp_bucket_desc& b, const float* main_grad, int64_t stride, int32_t W,
+                         int32_t mode, void* const* grads_out, int32_t ld, const uint8_t* global_used,
+                         void* stream)
+{
+    if (b.numel == 0 || b.nseg == 0) return ok();
+    Ctx cx = base_ctx(b.numel, W, mode == DDP_REDUCE_SCATTER, mode);
+    set_segments(cx, b);
+    set_mg(cx, const_cast<float*>(main_grad), stride);
+    cx.ld = ld;
+    cx.grads_out = grads_out;
+    cx.global_used = global_used;
+    return dispatch<OP_UNPACK>(cx, DDP_F32, stream);
+}
+
+ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
+                        int32_t W, int32_t mode, int32_t accumulate, float* main_grad, int64_t stride,
+                        void* const* grads_out, const uint8_t* global_used, void* stream)
+{
+    if (b.numel == 0) return ok();
+    Ctx cx = base_ctx(b.numel, W, true, mode);
+    set_segments(cx, b);
+    set_mg(cx, main_grad, stride);
+    cx.ld = ld;
+    cx.grads = grads;
+    cx.used = used;
+    cx.grads_out = grads_out;
+    cx.global_used = global_used;
+    cx.accumulate = accumulate != 0;
+    return dispatch<OP_FUSED>(cx, b.dtype, stream);
+}
+
+}  // namespace ddp
+
+// ---------------------------------------------------------------------------
+// C ABI: validation, then launch
+// ---------------------------------------------------------------------------
+namespace {
+
+ddp_status check_w(const char* fn, int32_t W)
+{
+    if (W < 1 || W > ddp::kMaxReplicas)
+        return ddp::fail(DDP_E_INVAL, "%s: W = %d outside [1, %d]", fn, W, ddp::kMaxReplicas);
+    return DDP_OK;
+}
+
+ddp_status check_mode(const char* fn, int32_t mode, int64_t n, int32_t W)
+{
+    if (mode != DDP_ALLREDUCE && mode != DDP_REDUCE_SCATTER)
+        return ddp::fail(DDP_E_INVAL, "%s: unknown mode %d", fn, mode);
+    if (mode == DDP_REDUCE_SCATTER && n % W != 0)
+        return ddp::fail(DDP_E_INVAL, "%s: reduce_scatter needs numel %% W == 0 (numel %lld, W %d)", fn,
+                         static_cast<long long>(n), W);
+    return DDP_OK;
+}
+
+ddp_status check_desc(const char* fn, const ddp_bucket_desc* b, int32_t ld, bool need_tables)
+{
+    if (!b) return ddp::fail(DDP_E_INVAL, "%s: bucket descriptor is NULL", fn);
+    if (b->numel < 0 || b->nseg < 0)
+        return ddp::fail(DDP_E_INVAL, "%s: negative size (numel %lld, nseg %d)", fn,
+                         static_cast<long long>(b->numel), b->nseg);
+    if (b->dtype != DDP_F32 && b->dtype != DDP_BF16 && b->dtype != DDP_F16)
+        return ddp::fail(DDP_E_INVAL, "%s: unknown dtype %d", fn, b->dtype);
+    if (b->nseg > 0 && (!b->seg_offset || !b->seg_param))
+        return ddp::fail(DDP_E_INVAL, "%s: segment tables are NULL with nseg = %d", fn, b->nseg);
+    if (need_tables && b->nseg > 0 && ld < 1) return ddp::fail(DDP_E_INVAL, "%s: ld = %d < 1", fn, ld);
+    return DDP_OK;
+}
+
+ddp_status check_mg(const char* fn, const float* mg, int64_t stride, int64_t n, int32_t W)
+{
+    if (!mg && n > 0) return ddp::fail(DDP_E_INVAL, "%s: main_grad is NULL", fn);
+    if (W > 1 && stride < n)
+        return ddp::fail(DDP_E_INVAL, "%s: replica_stride %lld < numel %lld", fn, static_cast<long long>(stride),
+                         static_cast<long long>(n));
+    return DDP_OK;
+}
+
+#define DDP_TRY(x)                          \
+    do {                                    \
+        const ddp_status st_ = (x);         \
+        if (st_ != DDP_OK) return st_;      \
+    } while (0)
+
+}  // namespace
+
+extern "C" ddp_status ddp_bucket_allreduce(float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
+                                           int32_t mode, void* stream)
+{
+    const char* fn = "ddp_bucket_allreduce";
+    DDP_TRY(check_w(fn, W));
+    if (numel < 0) return ddp::fail(DDP_E_INVAL, "%s: numel < 0", fn);
+    DDP_TRY(check_mode(fn, mode, numel, W));
+    DDP_TRY(check_mg(fn, replicas, replica_stride, numel, W));
+    return ddp::launch_allreduce(replicas, replica_stride, numel, W, mode, stream);
+}
+
+extern "C" ddp_status ddp_pack(const ddp_bucket_desc* bucket, const void* const* grads, const uint8_t* used,
+                               int32_t ld, int32_t W, float* main_grad, int64_t replica_stride, int32_t accumulate,
+                               void* stream)
+{
+    const char* fn = "ddp_pack";
+    DDP_TRY(check_w(fn, W));
+    DDP_TRY(check_desc(fn, bucket, ld, true));
+    if (bucket->nseg > 0 && !grads) return ddp::fail(DDP_E_INVAL, "%s: grads table is NULL", fn);
+    DDP_TRY(check_mg(fn, main_grad, replica_stride, bucket->numel, W));
+    return ddp::launch_pack(*bucket, grads, used, ld, W, main_grad, replica_stride, accumulate, stream);
+}
+
+extern "C" ddp_status ddp_unpack(const ddp_bucket_desc* bucket, const float* main_grad, int64_t replica_stride,
+                                 int32_t W, int32_t mode, void* const* grads_out, int32_t ld,
+                                 const uint8_t* global_used, void* stream)
+{
+    const char* fn = "ddp_unpack";
+    DDP_TRY(check_w(fn, W));
+    DDP_TRY(check_desc(fn, bucket, ld, true));
+    DDP_TRY(check_mode(fn, mode, bucket->numel, W));
+    if (bucket->nseg > 0 && !grads_out) return ddp::fail(DDP_E_INVAL, "%s: grads_out table is NULL", fn);
+    DDP_TRY(check_mg(fn, main_grad, replica_stride, bucket->numel, W));
+    return ddp::launch_unpack(*bucket, main_grad, replica_stride, W, mode, grads_out, ld, global_used, stream);
+}
+
+extern "C" ddp_status ddp_fused_bucket(const ddp_bucket_desc* bucket, const void* const* grads,
+                                       const uint8_t* used, int32_t ld, int32_t W, int32_t mode,
+                                       int32_t accumulate, float* main_grad, int64_t replica_stride,
+                                       void* const* grads_out, const uint8_t* global_used, void* stream)
+{
+    const char* fn = "ddp_fused_bucket";
+    DDP_TRY(check_w(fn, W));
+    DDP_TRY(check_desc(fn, bucket, ld, true));
+    DDP_TRY(check_mode(fn, mode, bucket->numel, W));
+    if (bucket->nseg > 0 && !grads) return ddp::fail(DDP_E_INVAL, "%s: grads table is NULL", fn);
+    if (!main_grad && !grads_out && bucket->numel > 0)
+        return ddp::fail(DDP_E_INVAL, "%s: main_grad and grads_out are both NULL", fn);
+    if (accumulate && !main_grad && bucket->numel > 0)
+        return ddp::fail(DDP_E_INVAL, "%s: accumulate needs main_grad", fn);
+    if (main_grad) DDP_TRY(check_mg(fn, main_grad, replica_stride, bucket->numel, W));
+    return ddp::launch_fused(*bucket, grads, used, ld, W, mode, accumulate, main_grad, replica_stride, grads_out,
+                             global_used, stream);
+}

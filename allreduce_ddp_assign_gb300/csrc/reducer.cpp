@@ -1,0 +1,389 @@
+// Step 5 of the path: the reducer -- per-bucket pending counts, strictly
+// in-order issue on a side stream, and the end-of-backward wait.
+//
+// "DDP: ring AllReduce and gradient buckets" sections 17.2 (pending count per
+// bucket), 17.12 (mark_variable_ready; mark_bucket_ready issues buckets in
+// index order from next_bucket_), 17.16 (prepare_for_backward resets the
+// counts; marking a variable twice is an error), 17.41 (finalize_backward waits
+// on every bucket; on CUDA the wait is a stream wait); "Lecture 15: PyTorch
+// DDP" section 2.3 (bucket i+1 waits for bucket i even if it filled first; all
+// ranks must issue in the same order); "Megatron DDP: contiguous buffer and
+// overlap" sections 2-3 (grad-ready hook, start_grad_sync / finish_grad_sync on
+// a separate stream).
+//
+// GPU side: when a bucket's count reaches zero, an event is recorded on every
+// stream that produced one of its gradients; when the bucket's turn comes the
+// side stream waits for those events and the bucket's kernels are launched on
+// it.  Finalize records one event on the side stream and makes the consumer
+// wait for it; with a timeout it also polls that event on the host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "common.h"
+
+namespace {
+
+enum class Phase { Idle, Backward, Finalized };
+
+bool cuda_ok(cudaError_t e, const char* what, ddp_status* st)
+{
+    if (e == cudaSuccess) return true;
+    *st = ddp::fail(DDP_E_CUDA, "%s failed: %s", what, cudaGetErrorString(e));
+    return false;
+}
+
+}  // namespace
+
+struct ddp_reducer {
+    int32_t nparams = 0, nbuckets = 0, W = 1, mode = DDP_ALLREDUCE, flags = 0;
+    std::vector<int32_t> bucket_of, order, bucket_params;
+    std::vector<ddp_bucket_desc> buckets;
+    std::vector<int64_t> start;
+    const void* const* grads = nullptr;
+    const uint8_t* used = nullptr;
+    int32_t ld = 0;
+    float* mg = nullptr;
+    int64_t stride = 0;
+    void* const* grads_out = nullptr;
+    const uint8_t* global_used = nullptr;
+    cudaStream_t side = nullptr;
+
+    // one iteration
+    Phase phase = Phase::Idle;
+    int32_t accumulate = 0;
+    std::vector<int32_t> pending;
+    std::vector<uint8_t> marked;
+    int32_t next = 0;
+    std::vector<std::vector<cudaStream_t>> producers;
+    std::vector<int32_t> log;
+
+    // CUDA events (none in dry-run mode)
+    std::vector<std::vector<cudaEvent_t>> ready;
+    std::vector<cudaEvent_t> t_begin, t_end;
+    cudaEvent_t done = nullptr;
+    bool timing_valid = false;
+
+    bool dry() const { return flags & DDP_R_DRY_RUN; }
+
+    std::string unmarked_list() const
+    {
+        std::string s;
+        int shown = 0;
+        for (int32_t p = 0; p < nparams; ++p) {
+            if (marked[p]) continue;
+            if (shown == 64) {
+                s += " ...";
+                break;
+            }
+            s += " " + std::to_string(p);
+            ++shown;
+        }
+        return s;
+    }
+
+    ddp_status launch_bucket(int32_t b)
+    {
+        const ddp_bucket_desc& d = buckets[b];
+        float* mgb = mg ? mg + start[b] : nullptr;
+        void* st = static_cast<void*>(side);
+        const bool copy_back = flags & DDP_R_COPY_BACK;
+        if (flags & DDP_R_FUSED)
+            return ddp::launch_fused(d, grads, used, ld, W, mode, accumulate, mgb, stride,
+                                     copy_back ? grads_out : nullptr, global_used, st);
+        ddp_status s = ddp::launch_pack(d, grads, used, ld, W, mgb, stride, accumulate, st);
+        if (s == DDP_OK) s = ddp::launch_allreduce(mgb, stride, d.numel, W, mode, st);
+        if (s == DDP_OK && copy_back)
+            s = ddp::launch_unpack(d, mgb, stride, W, mode, grads_out, ld, global_used, st);
+        return s;
+    }
+
+    ddp_status issue(int32_t b)
+    {
+        log.push_back(b);
+        if (dry()) return DDP_OK;
+        ddp_status st = DDP_OK;
+        for (size_t i = 0; i < producers[b].size(); ++i)
+            if (!cuda_ok(cudaStreamWaitEvent(side, ready[b][i], 0), "cudaStreamWaitEvent", &st)) return st;
+        if (flags & DDP_R_TIMING)
+            if (!cuda_ok(cudaEventRecord(t_begin[b], side), "cudaEventRecord", &st)) return st;
+        st = launch_bucket(b);
+        if (st != DDP_OK) return st;
+        if (flags & DDP_R_TIMING)
+            if (!cuda_ok(cudaEventRecord(t_end[b], side), "cudaEventRecord", &st)) return st;
+        return DDP_OK;
+    }
+
+    ddp_status bucket_ready(int32_t b)
+    {
+        if (!dry()) {
+            ddp_status st = DDP_OK;
+            auto& evs = ready[b];
+            while (evs.size() < producers[b].size()) {
+                cudaEvent_t e = nullptr;
+                if (!cuda_ok(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate", &st)) return st;
+                evs.push_back(e);
+            }
+            for (size_t i = 0; i < producers[b].size(); ++i)
+                if (!cuda_ok(cudaEventRecord(evs[i], producers[b][i]), "cudaEventRecord", &st)) return st;
+        }
+        while (next < nbuckets && pending[order[next]] == 0) {
+            const ddp_status st = issue(order[next]);
+            ++next;
+            if (st != DDP_OK) return st;
+        }
+        return DDP_OK;
+    }
+
+    void destroy_events()
+    {
+        if (dry()) return;
+        for (auto& v : ready)
+            for (cudaEvent_t e : v) cudaEventDestroy(e);
+        for (cudaEvent_t e : t_begin) cudaEventDestroy(e);
+        for (cudaEvent_t e : t_end) cudaEventDestroy(e);
+        if (done) cudaEventDestroy(done);
+    }
+};
+
+extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, const int32_t* bucket_of,
+                                         const int32_t* bucket_order, const ddp_bucket_desc* buckets,
+                                         const int64_t* bucket_start, int32_t W, int32_t mode, int32_t flags,
+                                         const void* const* grads, const uint8_t* used, int32_t ld,
+                                         float* main_grad, int64_t replica_stride, void* const* grads_out,
+                                         const uint8_t* global_used, void* side_stream, ddp_reducer** out)
+{
+    using ddp::fail;
+    const char* fn = "ddp_reducer_create";
+    if (!out) return fail(DDP_E_INVAL, "%s: out is NULL", fn);
+    *out = nullptr;
+    if (nparams < 0 || nbuckets < 0) return fail(DDP_E_INVAL, "%s: negative size", fn);
+    if (nparams > 0 && !bucket_of) return fail(DDP_E_INVAL, "%s: bucket_of is NULL", fn);
+    if (nbuckets > 0 && (!bucket_order || !buckets || !bucket_start))
+        return fail(DDP_E_INVAL, "%s: a per-bucket array is NULL", fn);
+    if (W < 1 || W > ddp::kMaxReplicas) return fail(DDP_E_INVAL, "%s: W = %d outside [1, %d]", fn, W, ddp::kMaxReplicas);
+    if (mode != DDP_ALLREDUCE && mode != DDP_REDUCE_SCATTER) return fail(DDP_E_INVAL, "%s: unknown mode %d", fn, mode);
+    if (flags & ~(DDP_R_FUSED | DDP_R_COPY_BACK | DDP_R_TIMING | DDP_R_DRY_RUN))
+        return fail(DDP_E_INVAL, "%s: unknown flag bits 0x%x", fn, flags);
+    const bool dry = flags & DDP_R_DRY_RUN;
+
+    auto r = new ddp_reducer();
+    r->nparams = nparams;
+    r->nbuckets = nbuckets;
+    r->W = W;
+    r->mode = mode;
+    r->flags = flags;
+    r->bucket_of.assign(bucket_of, bucket_of + nparams);
+    r->order.assign(bucket_order, bucket_order + nbuckets);
+    r->buckets.assign(buckets, buckets + nbuckets);
+    r->start.assign(bucket_start, bucket_start + nbuckets);
+    r->bucket_params.assign(nbuckets, 0);
+    auto reject = [&](ddp_status s) {
+        delete r;
+        return s;
+    };
+    for (int32_t p = 0; p < nparams; ++p) {
+        if (bucket_of[p] < 0 || bucket_of[p] >= nbuckets)
+            return reject(fail(DDP_E_INVAL, "%s: parameter %d maps to bucket %d of %d", fn, p, bucket_of[p], nbuckets));
+        ++r->bucket_params[bucket_of[p]];
+    }
+    std::vector<uint8_t> seen(nbuckets, 0);
+    for (int32_t k = 0; k < nbuckets; ++k) {
+        const int32_t b = bucket_order[k];
+        if (b < 0 || b >= nbuckets || seen[b])
+            return reject(fail(DDP_E_INVAL, "%s: bucket_order is not a permutation (position %d)", fn, k));
+        seen[b] = 1;
+        if (r->bucket_params[b] == 0)
+            return reject(fail(DDP_E_INVAL, "%s: bucket %d has no parameter", fn, b));
+        const ddp_bucket_desc& d = buckets[b];
+        if (d.numel < 0 || d.nseg < 0 || (d.nseg > 0 && (!d.seg_offset || !d.seg_param)))
+            return reject(fail(DDP_E_INVAL, "%s: bad descriptor for bucket %d", fn, b));
+        if (mode == DDP_REDUCE_SCATTER && d.numel % W != 0)
+            return reject(fail(DDP_E_INVAL, "%s: bucket %d numel %lld not a multiple of W = %d", fn, b,
+                               static_cast<long long>(d.numel), W));
+        if (bucket_start[b] < 0 || (W > 1 && bucket_start[b] + d.numel > replica_stride))
+            return reject(fail(DDP_E_INVAL, "%s: bucket %d [%lld, +%lld) exceeds replica_stride %lld", fn, b,
+                               static_cast<long long>(bucket_start[b]), static_cast<long long>(d.numel),
+                               static_cast<long long>(replica_stride)));
+    }
+    if (!dry) {
+        if (nparams > 0 && (!grads || ld < 1)) return reject(fail(DDP_E_INVAL, "%s: grads table is NULL or ld < 1", fn));
+        if (!(flags & DDP_R_FUSED) && !main_grad)
+            return reject(fail(DDP_E_INVAL, "%s: staged issue (no DDP_R_FUSED) needs main_grad", fn));
+        if (!main_grad && !(flags & DDP_R_COPY_BACK))
+            return reject(fail(DDP_E_INVAL, "%s: without main_grad the results need DDP_R_COPY_BACK", fn));
+        if ((flags & DDP_R_COPY_BACK) && !grads_out)
+            return reject(fail(DDP_E_INVAL, "%s: DDP_R_COPY_BACK needs grads_out", fn));
+    }
+    r->grads = grads;
+    r->used = used;
+    r->ld = ld;
+    r->mg = main_grad;
+    r->stride = replica_stride;
+    r->grads_out = grads_out;
+    r->global_used = global_used;
+    r->side = static_cast<cudaStream_t>(side_stream);
+    r->pending.assign(nbuckets, 0);
+    r->marked.assign(nparams, 0);
+    r->producers.resize(nbuckets);
+    r->ready.resize(nbuckets);
+
+    if (!dry) {
+        ddp_status st = DDP_OK;
+        auto mk = [&](cudaEvent_t* e, unsigned fl) {
+            return cuda_ok(cudaEventCreateWithFlags(e, fl), "cudaEventCreate", &st);
+        };
+        if (!mk(&r->done, cudaEventDisableTiming)) return reject(st);
+        for (int32_t b = 0; b < nbuckets; ++b) {
+            cudaEvent_t e = nullptr;
+            if (!mk(&e, cudaEventDisableTiming)) return reject(st);
+            r->ready[b].push_back(e);
+        }
+        if (flags & DDP_R_TIMING) {
+            r->t_begin.assign(nbuckets, nullptr);
+            r->t_end.assign(nbuckets, nullptr);
+            for (int32_t b = 0; b < nbuckets; ++b)
+                if (!mk(&r->t_begin[b], cudaEventDefault) || !mk(&r->t_end[b], cudaEventDefault)) return reject(st);
+        }
+    }
+    *out = r;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate)
+{
+    if (!r) return ddp::fail(DDP_E_INVAL, "ddp_reducer_prepare: reducer is NULL");
+    if (accumulate && !r->mg && !r->dry())
+        return ddp::fail(DDP_E_INVAL, "ddp_reducer_prepare: accumulate needs main_grad");
+    ddp_status st = DDP_OK;
+    if (r->phase == Phase::Backward && r->next < r->nbuckets) {
+        bool any = false;
+        for (uint8_t m : r->marked) any = any || m;
+        if (any)
+            st = ddp::fail(DDP_E_INCOMPLETE,
+                           "ddp_reducer_prepare: the previous iteration did not finish reducing its buckets "
+                           "(%d of %d issued); parameters never marked ready:%s",
+                           r->next, r->nbuckets, r->unmarked_list().c_str());
+    }
+    for (int32_t b = 0; b < r->nbuckets; ++b) {
+        r->pending[b] = r->bucket_params[b];
+        r->producers[b].clear();
+    }
+    std::fill(r->marked.begin(), r->marked.end(), 0);
+    r->next = 0;
+    r->log.clear();
+    r->accumulate = accumulate != 0;
+    r->phase = Phase::Backward;
+    return st == DDP_OK ? ddp::ok() : st;
+}
+
+extern "C" ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* producer_stream)
+{
+    if (!r) return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready: reducer is NULL");
+    if (param < 0 || param >= r->nparams)
+        return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready: parameter %d outside [0, %d)", param, r->nparams);
+    if (r->phase != Phase::Backward)
+        return ddp::fail(DDP_E_STATE, "ddp_reducer_mark_ready: parameter %d marked outside an iteration "
+                                      "(call ddp_reducer_prepare first)", param);
+    if (r->marked[param])
+        return ddp::fail(DDP_E_STATE, "ddp_reducer_mark_ready: parameter %d was marked ready twice in one iteration",
+                         param);
+    r->marked[param] = 1;
+    const int32_t b = r->bucket_of[param];
+    if (!r->dry()) {
+        auto& ps = r->producers[b];
+        const cudaStream_t s = static_cast<cudaStream_t>(producer_stream);
+        bool have = false;
+        for (cudaStream_t x : ps) have = have || x == s;
+        if (!have) ps.push_back(s);
+    }
+    if (--r->pending[b] == 0) {
+        const ddp_status st = r->bucket_ready(b);
+        if (st != DDP_OK) return st;
+    }
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t* params, int32_t n,
+                                                  void* producer_stream)
+{
+    if (n < 0 || (n > 0 && !params)) return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready_many: bad list");
+    for (int32_t i = 0; i < n; ++i) {
+        const ddp_status st = ddp_reducer_mark_ready(r, params[i], producer_stream);
+        if (st != DDP_OK) return st;
+    }
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream, int64_t timeout_us)
+{
+    const char* fn = "ddp_reducer_finalize";
+    if (!r) return ddp::fail(DDP_E_INVAL, "%s: reducer is NULL", fn);
+    if (r->phase == Phase::Idle) return ddp::fail(DDP_E_STATE, "%s: no iteration in progress", fn);
+    if (r->phase == Phase::Backward) {
+        if (r->next < r->nbuckets)
+            return ddp::fail(DDP_E_INCOMPLETE, "%s: %d of %d buckets issued; parameters never marked ready:%s", fn,
+                             r->next, r->nbuckets, r->unmarked_list().c_str());
+        if (!r->dry()) {
+            ddp_status st = DDP_OK;
+            if (!cuda_ok(cudaEventRecord(r->done, r->side), "cudaEventRecord", &st)) return st;
+            if (consumer_stream &&
+                !cuda_ok(cudaStreamWaitEvent(static_cast<cudaStream_t>(consumer_stream), r->done, 0),
+                         "cudaStreamWaitEvent", &st))
+                return st;
+        }
+        r->phase = Phase::Finalized;
+        r->timing_valid = (r->flags & DDP_R_TIMING) != 0;
+    }
+    if (timeout_us > 0 && !r->dry()) {
+        const auto deadline = std::chrono::steady_clock::now() + std::chrono::microseconds(timeout_us);
+        for (;;) {
+            const cudaError_t q = cudaEventQuery(r->done);
+            if (q == cudaSuccess) break;
+            if (q != cudaErrorNotReady) return ddp::fail(DDP_E_CUDA, "%s: %s", fn, cudaGetErrorString(q));
+            if (std::chrono::steady_clock::now() >= deadline)
+                return ddp::fail(DDP_E_TIMEOUT, "%s: reductions still running after %lld us", fn,
+                                 static_cast<long long>(timeout_us));
+            std::this_thread::sleep_for(std::chrono::microseconds(20));
+        }
+    }
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n)
+{
+    if (!r || !n) return ddp::fail(DDP_E_INVAL, "ddp_reducer_issue_log: NULL argument");
+    *n = static_cast<int32_t>(r->log.size());
+    if (cap < *n || (!out && *n > 0))
+        return ddp::fail(DDP_E_CAPACITY, "ddp_reducer_issue_log: %d entries, room for %d", *n, cap);
+    for (int32_t i = 0; i < *n; ++i) out[i] = r->log[i];
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_bucket_ms(ddp_reducer* r, float* out, int32_t cap)
+{
+    const char* fn = "ddp_reducer_bucket_ms";
+    if (!r || !out) return ddp::fail(DDP_E_INVAL, "%s: NULL argument", fn);
+    if (!(r->flags & DDP_R_TIMING) || r->dry()) return ddp::fail(DDP_E_STATE, "%s: reducer built without timing", fn);
+    if (!r->timing_valid) return ddp::fail(DDP_E_STATE, "%s: no finalized iteration", fn);
+    if (cap < r->nbuckets) return ddp::fail(DDP_E_CAPACITY, "%s: %d buckets, room for %d", fn, r->nbuckets, cap);
+    ddp_status st = DDP_OK;
+    for (int32_t b = 0; b < r->nbuckets; ++b) {
+        if (!cuda_ok(cudaEventSynchronize(r->t_end[b]), "cudaEventSynchronize", &st)) return st;
+        float ms = 0.f;
+        if (!cuda_ok(cudaEventElapsedTime(&ms, r->t_begin[b], r->t_end[b]), "cudaEventElapsedTime", &st)) return st;
+        out[b] = ms;
+    }
+    return ddp::ok();
+}
+
+extern "C" void ddp_reducer_destroy(ddp_reducer* r)
+{
+    if (!r) return;
+    r->destroy_events();
+    delete r;
+}

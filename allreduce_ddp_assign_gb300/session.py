@@ -1,0 +1,135 @@
+"""User-level API: one object that owns a bucket plan, the replicas' buffers'
+pointer tables and a reducer, and runs DDP's synchronised backward over them.
+
+Plumbing over the C ABI: the assignment, every kernel and the schedule run in
+libddpbucket.  Gradients are marked ready in reverse parameter order, the order
+backward produces them ("DDP: ring AllReduce and gradient buckets", 17.3.1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import (DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, Plan, ddp_pack, ddp_reducer_bucket_ms, ddp_reducer_create,
+               ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
+               ddp_reducer_mark_ready_many, ddp_reducer_prepare)
+
+
+class BucketReducer:
+    """W data-parallel replicas of one model's gradients on this GPU.
+
+    grads[w][p]   replica w's gradient tensor of parameter p (fp32/bf16/fp16,
+                  contiguous, on the device), or None if never produced.
+    used[w][p]    optional 0/1 array: replica w produced p this iteration.
+    grads_out     optional [w][p] fp32 tensors receiving the reduced gradients
+                  (copy-back); otherwise read them through ``view``.
+    """
+
+    def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads, used=None,
+                 grads_out=None, fused=True, timing=False, side_stream=None, main_grad=True, grad_reduce_in_fp32=1):
+        import torch
+
+        self.W, self.mode = int(W), int(mode)
+        self.plan = Plan(numels, dtypes, cap_bytes, first_cap_bytes, order, pad_multiple, grad_reduce_in_fp32)
+        P = self.plan.nparams
+        self.side = side_stream if side_stream is not None else torch.cuda.Stream()
+        self.main_grad = self.plan.alloc_main_grad(self.W) if main_grad else None
+        self._tensors = (grads, grads_out)   # the pointer tables below point into these
+        self.grads_tab = self.plan.pointer_table(grads)
+        self.used_np = None if used is None else np.ascontiguousarray(used, dtype=np.uint8).reshape(self.W, P)
+        self.used_tab = None if used is None else self.plan.flag_table(self.used_np)
+        gu = None if used is None else self.used_np.max(axis=0)
+        self.global_used_tab = None if gu is None else self.plan.flag_table(gu)
+        self.out_tab = None if grads_out is None else self.plan.pointer_table(grads_out)
+        flags = (DDP_R_FUSED if fused else 0) | (DDP_R_COPY_BACK if grads_out is not None else 0) | \
+                (DDP_R_TIMING if timing else 0)
+        self.handle = ddp_reducer_create(P, self.plan.bucket_of, self.plan.bucket_order, self.plan.descs,
+                                         self.plan.bucket_start, self.W, self.mode, flags, self.grads_tab,
+                                         self.used_tab, P, self.main_grad, self.plan.replica_stride, self.out_tab,
+                                         self.global_used_tab, self.side)
+        self.ready_order = np.arange(P - 1, -1, -1, dtype=np.int32)
+
+    # -- one iteration ----------------------------------------------------
+    def accumulate_local(self, grads_tab, first: bool, stream=None):
+        """A no_sync micro-step: add (or, for the first, copy) this micro-step's
+        gradients into main_grad without reducing (ddp_pack).  The tensors behind
+        grads_tab must stay alive until the stream has run the kernels."""
+        for b in range(self.plan.nbuckets):
+            ddp_pack(self.plan.descs[b], grads_tab, self.used_tab, self.plan.nparams, self.W,
+                     self.plan.main_grad_at(self.main_grad, b), self.plan.replica_stride, 0 if first else 1, stream)
+
+    def backward(self, producer_stream=None, accumulate=False, order=None, one_by_one=False):
+        """Mark every parameter ready in gradient-ready order; buckets go out on
+        the side stream as they complete, in issue order."""
+        ddp_reducer_prepare(self.handle, int(accumulate))
+        order = self.ready_order if order is None else order
+        if one_by_one:
+            for p in order:
+                ddp_reducer_mark_ready(self.handle, int(p), producer_stream)
+        else:
+            ddp_reducer_mark_ready_many(self.handle, order, producer_stream)
+
+    def finalize(self, consumer_stream=None, timeout_us=0):
+        ddp_reducer_finalize(self.handle, consumer_stream, timeout_us)
+
+    def step(self, producer_stream=None, consumer_stream=None, accumulate=False):
+        self.backward(producer_stream, accumulate)
+        self.finalize(consumer_stream)
+
+    # -- results ------------------------------------------------------------
+    def view(self, p: int, w: int = 0):
+        return self.plan.view(self.main_grad, p, w)
+
+    def issue_log(self):
+        return ddp_reducer_issue_log(self.handle)
+
+    def bucket_ms(self):
+        return ddp_reducer_bucket_ms(self.handle, self.plan.nbuckets)
+
+    def close(self):
+        if self.handle:
+            ddp_reducer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class HostBucketReducer:
+    """Host-buffer front end of BucketReducer.  Each step copies every replica's
+    gradients from pinned host memory to the device, runs the synchronised
+    backward's bucket reduction, and copies the reduced main_grad back.
+
+    host_in   pinned [W, total] tensor (gradient dtype): replica w's gradients of
+              all parameters back to back in parameter order.
+    host_out  pinned [W * replica_stride] fp32 tensor.
+    """
+
+    def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, torch_dtype,
+                 used=None, fused=True, timing=False):
+        import torch
+
+        numels = [int(v) for v in numels]
+        offs = np.concatenate([[0], np.cumsum(numels)]).astype(np.int64)
+        self.dev_in = torch.empty((W, int(offs[-1])), dtype=torch_dtype, device="cuda")
+        grads = [[self.dev_in[w, offs[p]:offs[p + 1]] for p in range(len(numels))] for w in range(W)]
+        self.reducer = BucketReducer(numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads,
+                                     used=used, fused=fused, timing=timing)
+
+    @property
+    def replica_stride(self) -> int:
+        return self.reducer.plan.replica_stride
+
+    def step(self, host_in, host_out, stream=None):
+        import torch
+
+        stream = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(stream):
+            self.dev_in.copy_(host_in, non_blocking=True)
+            self.reducer.step(stream, stream)
+            host_out.copy_(self.reducer.main_grad, non_blocking=True)
+
+    def close(self):
+        self.reducer.close()

@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Benchmark of the gradient-bucket path: bucket-allreduce HBM GB/s.
+
+One step = one synchronised backward's bucket reduction over the whole
+workload: the reducer is prepared, every parameter is marked ready in
+gradient-ready order (reverse parameter order) on the compute stream, each
+bucket is issued in order on a side stream as soon as it and every bucket
+before it are complete (fused pack + ring-ordered reduce + 1/W kernel), and
+finalize makes the compute stream wait.  Inputs are resident in HBM when the
+timed region starts.  GB/s counts the path's algorithmic bytes: every gradient
+byte read once (plus main_grad when accumulating) and every result byte
+written once.
+
+Default workload: W = 8 replicas of ResNet-50's 161 gradient tensors (25.6M
+fp32 parameters), reverse-order buckets capped at 25 MiB with a 1 MiB first
+bucket (5 buckets), allreduce mean.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Under torchrun (N > 1) every rank runs the whole workload on its own GPU
+(replicas only, no collective on the data path); the barrier and the maximum
+over ranks of the elapsed time give the whole-job number.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = "bucket-allreduce HBM GB/s (and % of 8 TB/s roofline) per bucket size and W"
+NOMINAL_HBM_GBS = 8000.0
+WORKLOADS = {
+    "mlp3_w4_allreduce": WL.c1_mlp,
+    "resnet50_w8_allreduce": WL.c2_resnet50,
+    "gpt2_small_w8_reduce_scatter": WL.c3_gpt2,
+    "bert_large_w4_nosync4_allreduce": WL.c4_bert_large,
+}
+DEFAULT = "resnet50_w8_allreduce"
+ELEM = {WL.F32: 4, WL.BF16: 2}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+def bucket_bytes(wl, numel: int, param_elems: int, used_elems: int, kind: str) -> int:
+    """Bytes one launch must move for one bucket.
+    fused:  every used gradient read, main_grad read when accumulating, result written
+            (allreduce: W replicas; reduce_scatter: one shard per replica = one bucket);
+    pack0:  gradients read, bucket written (copy); packN: gradients + bucket read, bucket written
+            (only used segments are touched when accumulating)."""
+    W, b_in = wl.W, ELEM[wl.dtype]
+    if kind == "fused":
+        rd = W * used_elems * b_in
+        wr = W * numel * 4 if wl.mode == WL.ALLREDUCE else numel * 4
+        return rd + wr
+    if kind == "fused_acc":
+        rd = W * used_elems * b_in + W * numel * 4
+        wr = W * numel * 4 if wl.mode == WL.ALLREDUCE else numel * 4
+        return rd + wr
+    if kind == "pack0":
+        return W * used_elems * b_in + W * numel * 4
+    if kind == "packN":
+        return W * used_elems * (b_in + 8)
+    raise ValueError(kind)
+
+
+def step_launches(wl, plan):
+    """[(kind, bucket, bytes)] of one step, in launch order."""
+    used = set(range(wl.nparams)) - set(wl.unused)
+    out = []
+    per_bucket = []
+    for b in range(plan.nbuckets):
+        mem = plan.members[b]
+        pe = sum(wl.numels[p] for p in mem)
+        ue = sum(wl.numels[p] for p in mem if p in used)
+        per_bucket.append((int(plan.bucket_numel[b]), pe, ue))
+    for m in range(wl.micro_steps - 1):
+        for b in range(plan.nbuckets):
+            out.append(("pack0" if m == 0 else "packN", b, bucket_bytes(wl, *per_bucket[b], "pack0" if m == 0 else "packN")))
+    kind = "fused_acc" if wl.micro_steps > 1 else "fused"
+    for b in plan.bucket_order:
+        out.append((kind, int(b), bucket_bytes(wl, *per_bucket[int(b)], kind)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+        self.gpu = vis[local_rank].strip() if len(vis) > local_rank and vis[local_rank].strip() else str(local_rank)
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            return False
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + float("0." + f[0].split(".")[1])
+                self.rows.append((ts, float(f[2]), float(f[3]), f[5], f[6], f[7], f[8], f[9]))
+            except (ValueError, IndexError):
+                continue
+        return False
+
+    def summary(self):
+        if self.proc is None or not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for r in self.rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside or sorted(self.rows, key=lambda r: abs(r[0] - (self.t0 or 0)))[:3]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in use for n, v in zip(names, r[4:]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle: CPU baseline and reference arm
+# ---------------------------------------------------------------------------
+_SAMPLE_CACHE: dict = {}
+
+
+def oracle_sample(wl, seconds: float, min_reps: int = 1):
+    """Time the oracle (as it is: single-threaded C, pack then ring) on bucket 0 of
+    the workload's plan, repeated for about `seconds`.  Returns (GB/s, description,
+    reps, seconds).  Inputs are generated once and kept."""
+    import oracle
+
+    orc = oracle.load()
+    if wl.name not in _SAMPLE_CACHE:
+        plan = orc.assign(wl.numels, [wl.dtype] * wl.nparams, wl.cap_bytes, wl.first_cap_bytes, wl.order,
+                          wl.pad_multiple, wl.grad_reduce_in_fp32)
+        mem = plan["members"][0]
+        grads = [[[WL.grad_raw_np(wl, p, w, m) for p in mem] for w in range(wl.W)] for m in range(wl.micro_steps)]
+        _SAMPLE_CACHE[wl.name] = (plan, grads)
+    plan, grads = _SAMPLE_CACHE[wl.name]
+    mem = plan["members"][0]
+    offs = [int(plan["offset_of"][p]) for p in mem]
+    numel = int(plan["bucket_numel"][0])
+    used = np.ones((wl.W, len(mem)), np.uint8)
+    for j, p in enumerate(mem):
+        if p in wl.unused:
+            used[:, j] = 0
+    ue = sum(wl.numels[p] for p in mem if p not in wl.unused)
+    pe = sum(wl.numels[p] for p in mem)
+    nbytes = 0
+    for m in range(wl.micro_steps - 1):
+        nbytes += bucket_bytes(wl, numel, pe, ue, "pack0" if m == 0 else "packN")
+    nbytes += bucket_bytes(wl, numel, pe, ue, "fused_acc" if wl.micro_steps > 1 else "fused")
+    reps, t_total = 0, 0.0
+    while reps < min_reps or t_total < seconds:
+        t = time.perf_counter()
+        buf = None
+        for m in range(wl.micro_steps):
+            buf = orc.pack(grads[m], offs, numel, [wl.dtype] * len(mem), used, accumulate=m > 0, out=buf)
+        orc.ring(buf, wl.mode)
+        t_total += time.perf_counter() - t
+        reps += 1
+    desc = (f"bucket 0 of {plan['nbuckets']} ({len(mem)} tensors, {numel} elements x W={wl.W}), "
+            f"pack{'+accumulate' if wl.micro_steps > 1 else ''} + ring, {reps} reps, inputs pre-generated")
+    return nbytes * reps / t_total / 1e9, desc, reps, t_total
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0)
+    vals, times = [], []
+    total_bytes_time = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, desc, reps, t = oracle_sample(wl, 0.0)
+        vals.append(v)
+        total_bytes_time.append((v * t, t))
+    elapsed = time.perf_counter() - t0
+    gb = sum(x for x, _ in total_bytes_time)
+    tt = sum(t for _, t in total_bytes_time)
+    value = gb / tt
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * tt / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded splitmix64)",
+            "impl": "reference",
+            "config": {"workload": wl.name, "W": wl.W, "mode": "allreduce" if wl.mode == 0 else "reduce_scatter",
+                       "sample": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(elapsed, 2)}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def profile_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
+    if it was captured on the current kernel source."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(kernel_tag)
+        src = open(os.path.join(ROOT, "allreduce_ddp_assign_gb300", "csrc", "kernels.cu"), "rb").read()
+        if rec and rec.get("kernels_cu_sha256") == hashlib.sha256(src).hexdigest():
+            return rec.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+    return None
+
+
+def run_ours(args, wl):
+    import torch
+
+    import allreduce_ddp_assign_gb300 as D
+    from allreduce_ddp_assign_gb300.session import BucketReducer, HostBucketReducer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    D.lib()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    # inputs resident in HBM
+    used = None
+    if wl.unused:
+        used = np.ones((wl.W, wl.nparams), np.uint8)
+        used[:, wl.unused] = 0
+    micro = [[[None if p in wl.unused else WL.grad_torch(wl, p, w, m, dev) for p in range(wl.nparams)]
+              for w in range(wl.W)] for m in range(wl.micro_steps)]
+    sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                         wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True, timing=True)
+    tabs = [sess.plan.pointer_table(micro[m]) for m in range(wl.micro_steps - 1)]
+    compute = torch.cuda.current_stream()
+    launches = step_launches(wl, sess.plan)
+    step_bytes = sum(x[2] for x in launches)
+
+    def step():
+        for m in range(wl.micro_steps - 1):   # no_sync micro-steps: local accumulation on the compute stream
+            sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
+        sess.backward(compute, accumulate=wl.micro_steps > 1)
+        sess.finalize(compute)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    side_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks.mark("t0")
+        ev0.record(compute)
+        for k in range(K):
+            side_ev[k][0].record(sess.side)
+            step()
+            side_ev[k][1].record(sess.side)
+        ev1.record(compute)
+        torch.cuda.synchronize()
+        clocks.mark("t1")
+        if dist:
+            dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    side_ms = sum(a.elapsed_time(b) for a, b in side_ev)
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
+    per_bucket_ms = sess.bucket_ms()
+    value = job_value(world, step_bytes, K, elapsed_ms)
+
+    # the dominant kernel: the per-bucket fused launch on the side stream (the
+    # no_sync packs of an accumulating workload run on the compute stream)
+    fused = [x for x in launches if x[0].startswith("fused")]
+    fused_bytes = sum(x[2] for x in fused)
+    if wl.micro_steps > 1:
+        kern_ms = float(sum(per_bucket_ms))  # last step's fused launches (the packs are not on the side stream)
+        achieved = fused_bytes / (kern_ms * 1e-3) / 1e9
+        timing_src = "reducer events around each fused launch, last timed step"
+    else:
+        kern_ms = side_ms / K
+        achieved = fused_bytes / (kern_ms * 1e-3) / 1e9
+        timing_src = "CUDA events on the side stream around each step's launches, timed region"
+    tag = f"fused_{wl.name}"
+    traffic = profile_traffic(tag)
+
+    # end to end: pinned host buffers in, reduced main_grad out, through the public API
+    e2e = None
+    if not args.no_e2e and wl.micro_steps == 1:
+        tdt = torch.float32 if wl.dtype == WL.F32 else torch.bfloat16
+        host = HostBucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                                 wl.first_cap_bytes, wl.pad_multiple, tdt, used=used)
+        total = sum(wl.numels)
+        h_in = torch.empty((wl.W, total), dtype=tdt, pin_memory=True)
+        for w in range(wl.W):
+            h_in[w] = torch.cat([micro[-1][w][p].reshape(-1) if micro[-1][w][p] is not None else
+                                 torch.zeros(wl.numels[p], dtype=tdt, device=dev)
+                                 for p in range(wl.nparams)]).cpu()
+        h_out = torch.empty((wl.W * host.replica_stride,), dtype=torch.float32, pin_memory=True)
+        for _ in range(max(args.warmup, 3)):
+            host.step(h_in, h_out)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        Ke = max(3, min(K, 50))
+        a.record()
+        for _ in range(Ke):
+            host.step(h_in, h_out)
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+        e2e = {"value": round(job_value(world, step_bytes, Ke, e_ms), 3), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h_in.numel() * h_in.element_size()),
+               "d2h_bytes_per_step": int(h_out.numel() * 4), "steps": Ke}
+        host.close()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, desc, reps, t = oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "cpu_model": _cpu_model(), "host_cores": len(os.sched_getaffinity(0))}
+
+    clk = clocks.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(elapsed_ms / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.dtype == WL.F32 else "bf16->f32",
+            "data": "synthetic (seeded splitmix64 gradients of the model's parameter shapes)",
+            "config": {"workload": wl.name, "W": wl.W, "mode": "allreduce" if wl.mode == 0 else "reduce_scatter",
+                       "buckets": sess.plan.nbuckets, "params": wl.nparams, "elements": sum(wl.numels),
+                       "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": f"replicas x{world}", "pct_of_nominal_8TBs": round(100 * value / NOMINAL_HBM_GBS, 2),
+                       "buckets_per_s": round(world * K * sess.plan.nbuckets / (elapsed_ms * 1e-3), 1)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
+                         "kernel": tag, "timing": timing_src,
+                         "per_bucket_gbs": [round(x[2] / (per_bucket_ms[x[1]] * 1e-3) / 1e9, 1) if per_bucket_ms[x[1]] > 0
+                                            else None for x in fused]},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": len(launches) * K,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    sess.close()
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """Maximum of x over the ranks of the default process group (x itself alone)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, bytes_per_step: int, steps: int, max_elapsed_ms: float) -> float:
+    """Whole-job GB/s: every rank moved bytes_per_step per step; the slowest rank sets the time."""
+    return world * bytes_per_step * steps / (max_elapsed_ms * 1e-3) / 1e9
+
+
+def _cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    wl = WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

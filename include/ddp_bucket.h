@@ -1,0 +1,397 @@
+/*
+ * ddp_bucket.h -- C ABI of libddpbucket, the gradient-bucket reduction of
+ * data-parallel training on one GB300 (sm_103a).
+ *
+ * The path has five steps, each an entry point below:
+ *   assign    parameters -> size-capped buckets          (host)
+ *   pack      per-parameter gradients -> fp32 bucket      (device kernel)
+ *   reduce    W replicas of a bucket, ring order, 1/W     (device kernel)
+ *   unpack    reduced bucket -> per-parameter gradients   (device kernel)
+ *   schedule  in-order bucket issue gated by events       (host + device)
+ * plus ddp_fused_bucket, which does pack + reduce + unpack in one pass.
+ *
+ * The W data-parallel ranks are W replica buffers in this GPU's memory; the
+ * ring's summation order is reproduced element by element inside the kernels.
+ *
+ * Sources (page title, section):
+ *   "DDP: ring AllReduce and gradient buckets" (PyTorch internals book, ch. 17)
+ *     -- the DDP chapter below;
+ *   "Lecture 15: PyTorch DDP" (CMU 11-868 notes) -- the lecture;
+ *   "Megatron DDP: contiguous buffer and overlap" -- the Megatron page.
+ *
+ * Conventions for every call:
+ *   - Status: every call returns a ddp_status (int32_t).  Nothing is thrown
+ *     across the ABI.  On failure ddp_last_error_message() (per thread) says
+ *     why, naming the parameter or bucket involved.  Arguments are validated on
+ *     the host before anything is launched; a failed call launches nothing.
+ *   - Memory: the caller owns all host and device memory.  The library
+ *     allocates no device memory.  A reducer owns host bookkeeping and the
+ *     CUDA events it creates, released by ddp_reducer_destroy.
+ *   - Streams: `stream` arguments are cudaStream_t handles passed as void*
+ *     (NULL = the legacy default stream).  Data-path calls are asynchronous on
+ *     that stream; only ddp_reducer_finalize with a timeout waits on the host.
+ *   - Pointers marked DEVICE must be device (or managed) memory of the current
+ *     device; HOST pointers are ordinary host memory read during the call.
+ *   - Element types: DDP_F32, DDP_BF16, DDP_F16 gradients; buckets
+ *     (main_grad) are always fp32 (the Megatron page, section 1: main_grad in
+ *     fp32, grad_reduce_in_fp32).
+ *   - Sizes are element counts unless a name ends in _bytes.
+ *   - Alignment: no alignment is required.  16-byte-aligned buffers whose
+ *     offsets keep that alignment take the vector path; the rest is done with
+ *     scalar accesses on the GPU (there is no CPU fallback).
+ */
+#ifndef DDP_BUCKET_H
+#define DDP_BUCKET_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ddp_status;
+enum {
+    DDP_OK = 0,
+    DDP_E_INVAL = 1,      /* bad argument (null pointer, size, range, mode) */
+    DDP_E_ALIGN = 2,      /* reserved: a layout no kernel path accepts */
+    DDP_E_CUDA = 3,       /* a CUDA runtime call failed (message has the CUDA error) */
+    DDP_E_STATE = 4,      /* call out of order, e.g. a parameter marked ready twice */
+    DDP_E_INCOMPLETE = 5, /* buckets not all reduced: some parameters never marked ready */
+    DDP_E_TIMEOUT = 6,    /* ddp_reducer_finalize's deadline passed before the GPU finished */
+    DDP_E_CAPACITY = 7    /* an output array is too small */
+};
+
+enum { DDP_F32 = 0, DDP_BF16 = 1, DDP_F16 = 2 };
+
+/* Bucket assignment orders. */
+enum {
+    /* Rebuilt DDP buckets: parameters in reverse model.parameters() order
+     * (approximately the order backward produces gradients); bucket 0 gets
+     * first_cap_bytes, the rest cap_bytes; issued 0, 1, 2, ...
+     * (DDP chapter, sections 17.2 and 17.13; lecture, section 2.2). */
+    DDP_ORDER_REVERSE = 0,
+    /* Initial DDP buckets (also find_unused_parameters=True): computed over
+     * forward order with caps [first, cap, cap, ...], then the bucket list is
+     * reversed, so the first-cap bucket comes last (DDP chapter, 17.13). */
+    DDP_ORDER_FWD_THEN_REVERSE = 1,
+    /* Megatron contiguous buffer: forward layout, bucket 0 holds p0, every
+     * bucket capped at cap_bytes (first_cap_bytes ignored), numel padded to a
+     * multiple of pad_multiple; issued from the last bucket to the first,
+     * the order backward fills them (Megatron page, sections 1-2). */
+    DDP_ORDER_MEGATRON = 2
+};
+
+/* Reduction modes (Megatron page, section 3, start_grad_sync). */
+enum {
+    DDP_ALLREDUCE = 0,      /* every replica ends with the mean of the bucket */
+    DDP_REDUCE_SCATTER = 1  /* replica r ends with the mean of shard r only */
+};
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: bucket assignment (host)                                          */
+/* ------------------------------------------------------------------------ */
+/*
+ * ddp_assign_buckets -- map parameters to size-capped buckets.
+ *
+ * Defined by: DDP chapter 17.2 (a bucket is closed once its bytes reach the
+ * cap, so it may overshoot; default cap 25 MiB; the rebuilt first bucket uses
+ * 1 MiB) and 17.13 (reversed order, the rebuilt and the initial assignment);
+ * lecture 2.2 (fill in reverse parameter order, close at the cap) and exercise
+ * 3; lecture answer 9 and the Megatron page 1 (one dtype per bucket buffer;
+ * max(40 MB, 1 MB x DP) buckets over a contiguous fp32 buffer).
+ *
+ * Rule: walk the parameters in the order's iteration order; append each to the
+ * open bucket of its dtype; after appending, if that bucket's bytes >= its cap,
+ * close it.  Each dtype group keeps its own cap sequence (first cap for its
+ * first bucket, except DDP_ORDER_MEGATRON).  At the end the still-open buckets
+ * are closed in order of their dtype's first appearance.  Offsets are tight
+ * (no gaps) in append order; bucket_numel is rounded up to pad_multiple.
+ * Bucket bytes count 4 bytes per element when grad_reduce_in_fp32 != 0 (the
+ * bucket is fp32 main_grad), else the dtype's own size.
+ *
+ * HOST in:  numels[nparams] (>= 0), dtypes[nparams] (DDP_F32/BF16/F16),
+ *           cap_bytes > 0, first_cap_bytes > 0, order (DDP_ORDER_*),
+ *           pad_multiple >= 1.
+ * HOST out (caller-allocated): bucket_of[nparams], offset_of[nparams]
+ *           (elements from the bucket's start), members[nparams] (bucket 0's
+ *           parameters in layout order, then bucket 1's, ...), and per bucket
+ *           (max_buckets entries): bucket_numel (padded), bucket_bytes
+ *           (unpadded), bucket_dtype, bucket_order (bucket_order[k] = bucket
+ *           issued k-th); *nbuckets.
+ * Errors: DDP_E_INVAL (null pointer, bad value, nparams < 0);
+ *         DDP_E_CAPACITY if more than max_buckets buckets are needed
+ *         (*nbuckets then holds the count needed).  nparams + 2 always suffices.
+ */
+ddp_status ddp_assign_buckets(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
+                              int64_t cap_bytes, int64_t first_cap_bytes, int32_t order,
+                              int32_t pad_multiple, int32_t grad_reduce_in_fp32,
+                              int32_t* bucket_of, int64_t* offset_of, int32_t* members,
+                              int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
+                              int32_t* bucket_order, int32_t max_buckets, int32_t* nbuckets);
+
+/* ------------------------------------------------------------------------ */
+/* Bucket descriptor used by the device steps                                */
+/* ------------------------------------------------------------------------ */
+/*
+ * One bucket as the kernels see it (DDP chapter 17.2: a bucket has an index,
+ * a flat buffer and a parameter list; lecture 2.2, GradBucket).  The struct is
+ * HOST memory passed by pointer; its two tables are DEVICE arrays that the
+ * caller fills once from ddp_assign_buckets's output and keeps alive while
+ * kernels that use them run.
+ *
+ *   numel       elements of the bucket, padding included (bucket_numel[b]).
+ *   nseg        parameters in the bucket (>= 0).
+ *   dtype       gradient dtype of every segment (bucket_dtype[b]).
+ *   seg_offset  DEVICE int64[nseg + 1], ascending: segment s covers bucket
+ *               elements [seg_offset[s], seg_offset[s+1]); seg_offset[0] == 0;
+ *               [seg_offset[nseg], numel) is padding.
+ *   seg_param   DEVICE int32[nseg]: the parameter (column of the pointer
+ *               tables below) of segment s.
+ *
+ * Pointer tables (DEVICE arrays of device pointers, replica-major, leading
+ * dimension ld >= 1 + the largest seg_param):
+ *   grads[w * ld + p]      replica w's gradient of parameter p (dtype, numel
+ *                          elements); may be NULL where used[] says unused.
+ *   grads_out[w * ld + p]  fp32 destination of the reduced gradient.
+ *   used[w * ld + p]       uint8, nonzero if replica w produced a gradient
+ *                          for p this iteration (NULL: all used).
+ *   global_used[p]         uint8, nonzero if any replica used p (NULL: all).
+ *
+ * Replicated buckets: main_grad points at replica 0's copy of the bucket;
+ * replica w's copy starts replica_stride elements after replica w-1's
+ * (replica_stride >= numel).
+ */
+typedef struct ddp_bucket_desc {
+    int64_t numel;
+    int32_t nseg;
+    int32_t dtype;
+    const int64_t* seg_offset;
+    const int32_t* seg_param;
+} ddp_bucket_desc;
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: pack (device)                                                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * ddp_pack -- copy (or accumulate) per-parameter gradients into the bucket.
+ *
+ * Defined by: DDP chapter 17.12 (mark_variable_ready copies the gradient into
+ * the bucket's flat buffer) and 17.5; Megatron page 1 (fp32 main_grad, bf16
+ * gradients widened); lecture 4.1 and the summary of Li et al. 2020 section
+ * 2.2.4 (no_sync: gradients accumulate locally and the next synchronised
+ * backward reduces the sum); DDP chapter 17.33 (an unused parameter's segment
+ * is zero).
+ *
+ * For every replica w and bucket element e in segment s (parameter p, index
+ * i = e - seg_offset[s]):
+ *   accumulate == 0:  main_grad[w][e] = used ? (float)grads[w][p][i] : 0
+ *   accumulate != 0:  main_grad[w][e] = main_grad[w][e] + (float)grads[w][p][i]
+ *                     (unchanged where unused)
+ * Padding elements are set to 0 when accumulate == 0 and left alone otherwise.
+ * No 1/W scaling here: the scale is fused into the reduction.
+ *
+ * Errors: DDP_E_INVAL (W outside [1, 64], null desc/tables/main_grad,
+ * replica_stride < numel, ld < 1, negative sizes); DDP_E_CUDA (launch failure).
+ */
+ddp_status ddp_pack(const ddp_bucket_desc* bucket, const void* const* grads, const uint8_t* used,
+                    int32_t ld, int32_t W, float* main_grad, int64_t replica_stride,
+                    int32_t accumulate, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step 3: reduce (device)                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * ddp_bucket_allreduce -- average W replicas of one fp32 bucket in place, in
+ * the ring allreduce's summation order.
+ *
+ * Defined by: DDP chapter 17.4 (ring: reduce-scatter in N-1 steps, each rank
+ * sending 1/N to the next and adding what arrives, then all-gather in N-1
+ * steps) and 17.1, 17.9 (every rank ends with the average; each contribution is
+ * multiplied by 1/world_size); Megatron page 3 (reduce_scatter leaves shard r
+ * on rank r; scaling by 1/DP before the collective).
+ *
+ * With chunk length L = ceil(n / W), chunk c = [c*L, min((c+1)*L, n)).  For an
+ * element e of chunk c, with x_w = replicas[w*replica_stride + e] * fp32(1/W)
+ * (each product rounded to fp32):
+ *   s = x_{(c+1)%W}; then s = s + x_{(c+k)%W} for k = 2..W (fp32, in order)
+ * i.e. the order in which the ring's reduce-scatter visits ranks, ending on
+ * rank c.  No fused multiply-add is used.
+ *   DDP_ALLREDUCE:       s is written to element e of every replica.
+ *   DDP_REDUCE_SCATTER:  s is written to element e of replica c only (shard c
+ *                        of replica c); every other element is left as is.
+ *                        Requires n % W == 0.
+ * W == 1 leaves the bucket unchanged; n == 0 does nothing.
+ *
+ * replicas: DEVICE fp32, W copies, replica_stride >= n apart.
+ * Errors: DDP_E_INVAL (W outside [1, 64], null pointer with n > 0, stride < n,
+ * bad mode, reduce-scatter with n % W != 0); DDP_E_CUDA.
+ */
+ddp_status ddp_bucket_allreduce(float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
+                                int32_t mode, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step 4: unpack (device)                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * ddp_unpack -- copy the reduced bucket back into per-parameter gradients.
+ *
+ * Defined by: DDP chapter 17.5 and 17.12 (without gradient_as_bucket_view the
+ * reduced bucket is copied back to each .grad; with it .grad is a view of the
+ * bucket and nothing moves -- use offset_of/bucket_numel as views instead of
+ * calling this); DDP chapter 17.33 and lecture 4.2 (a parameter no rank used
+ * keeps its .grad untouched); Megatron page 3 (after reduce_scatter a rank only
+ * holds its own shard).
+ *
+ *   grads_out[w][p][i] = main_grad[w][seg_offset[s] + i]
+ * for every segment whose global_used[p] is nonzero (all if NULL).  In
+ * DDP_REDUCE_SCATTER mode replica w writes only the elements inside shard w
+ * (bucket elements [w*numel/W, (w+1)*numel/W)).
+ *
+ * Errors: as ddp_pack, plus bad mode / reduce-scatter with numel % W != 0.
+ */
+ddp_status ddp_unpack(const ddp_bucket_desc* bucket, const float* main_grad, int64_t replica_stride,
+                      int32_t W, int32_t mode, void* const* grads_out, int32_t ld,
+                      const uint8_t* global_used, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Steps 2-4 fused (device)                                                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * ddp_fused_bucket -- pack, reduce and unpack one bucket in a single pass: the
+ * gradients are read once, summed in ring order with the 1/W scale, and the
+ * result is written where the staged calls would put it.
+ *
+ * Results are bit-identical to ddp_pack (same accumulate, used) followed by
+ * ddp_bucket_allreduce (same mode) and, when grads_out != NULL, ddp_unpack,
+ * with one difference in reduce-scatter mode: main_grad is written only inside
+ * shard w of replica w (the staged ddp_pack would also have written the packed
+ * local gradients elsewhere).
+ *
+ *   main_grad     DEVICE fp32 bucket replicas; may be NULL when accumulate == 0
+ *                 and grads_out != NULL (the bucket then never materialises).
+ *   grads_out     DEVICE pointer table or NULL (gradient_as_bucket_view: the
+ *                 caller reads main_grad through views).  May alias grads
+ *                 when the gradients are fp32 (reduce in place).
+ *
+ * Errors: DDP_E_INVAL as the staged calls, and if both main_grad and grads_out
+ * are NULL, or accumulate != 0 with main_grad NULL; DDP_E_CUDA.
+ */
+ddp_status ddp_fused_bucket(const ddp_bucket_desc* bucket, const void* const* grads,
+                            const uint8_t* used, int32_t ld, int32_t W, int32_t mode,
+                            int32_t accumulate, float* main_grad, int64_t replica_stride,
+                            void* const* grads_out, const uint8_t* global_used, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step 5: the reducer -- in-order bucket issue on a side stream             */
+/* ------------------------------------------------------------------------ */
+/*
+ * Models DDP's Reducer (DDP chapter 17.2, 17.12, 17.16, 17.41; lecture 2.3;
+ * the summary of Li et al. section 2.2.3; Megatron page 2): each bucket has a
+ * pending count; marking a parameter ready decrements it; a bucket whose count
+ * reaches 0 is ready, and buckets are issued strictly in issue order starting
+ * from the next unissued one (bucket k+1 waits for bucket k even if it filled
+ * first).  Each issue makes the side stream wait for the streams that produced
+ * the bucket's gradients (CUDA events) and launches that bucket's reduction on
+ * the side stream; finalize makes the consumer stream wait for all of them.
+ */
+typedef struct ddp_reducer ddp_reducer;
+
+enum {
+    DDP_R_FUSED = 1,     /* issue ddp_fused_bucket per bucket (else pack + allreduce [+ unpack]) */
+    DDP_R_COPY_BACK = 2, /* write reduced gradients to grads_out (else main_grad views only) */
+    DDP_R_TIMING = 4,    /* record CUDA events around each bucket's kernels (ddp_reducer_bucket_ms) */
+    DDP_R_DRY_RUN = 8    /* schedule only: no CUDA call at all; issues are logged, not launched */
+};
+
+/*
+ * ddp_reducer_create
+ *   nparams, nbuckets     sizes of the plan from ddp_assign_buckets.
+ *   bucket_of             HOST int32[nparams].
+ *   bucket_order          HOST int32[nbuckets] (issue order).
+ *   buckets               HOST ddp_bucket_desc[nbuckets] (device tables inside),
+ *                         copied into the reducer.
+ *   bucket_start          HOST int64[nbuckets]: element offset of bucket b inside
+ *                         each main_grad replica (main_grad + w*replica_stride +
+ *                         bucket_start[b] is replica w's copy of bucket b).
+ *   W, mode, flags        replicas (1..64), DDP_ALLREDUCE/DDP_REDUCE_SCATTER, DDP_R_*.
+ *   grads, used, ld       DEVICE pointer table / flags as for ddp_pack.
+ *   main_grad, replica_stride   DEVICE fp32 buffer holding every bucket per replica.
+ *   grads_out, global_used      as for ddp_unpack (used with DDP_R_COPY_BACK).
+ *   side_stream           the stream the reductions run on.
+ * The pointers are kept and used by later calls; they must stay valid until
+ * ddp_reducer_destroy.  With DDP_R_DRY_RUN the device pointers may be NULL.
+ * Errors: DDP_E_INVAL; DDP_E_CUDA (event creation).
+ */
+ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, const int32_t* bucket_of,
+                              const int32_t* bucket_order, const ddp_bucket_desc* buckets,
+                              const int64_t* bucket_start, int32_t W, int32_t mode, int32_t flags,
+                              const void* const* grads, const uint8_t* used, int32_t ld,
+                              float* main_grad, int64_t replica_stride, void* const* grads_out,
+                              const uint8_t* global_used, void* side_stream, ddp_reducer** out);
+
+/*
+ * ddp_reducer_prepare -- start an iteration (prepare_for_backward, DDP chapter
+ * 17.16): reset every pending count, the ready marks and the issue position.
+ * accumulate != 0 means main_grad already holds gradients accumulated locally
+ * during no_sync micro-steps and this backward adds to them (lecture 4.1).
+ * Errors: DDP_E_INCOMPLETE if the previous iteration marked some parameters
+ * but never finished (the DDP chapter 17.6 error "Expected to have finished
+ * reduction in the prior iteration"); the message lists the parameter indices
+ * that did not receive a gradient.  The reducer is reset anyway.
+ */
+ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate);
+
+/*
+ * ddp_reducer_mark_ready -- the autograd hook of parameter `param` fired: its
+ * gradient has been (or is being) produced on `producer_stream`
+ * (mark_variable_ready, DDP chapter 17.12; lecture 2.3).
+ * Errors: DDP_E_INVAL (param out of range); DDP_E_STATE if param was already
+ * marked in this iteration (DDP chapter 17.16: "Expected to mark a variable
+ * ready only once") or prepare was not called; DDP_E_CUDA (event/launch).
+ */
+ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* producer_stream);
+
+/*
+ * ddp_reducer_mark_ready_many -- ddp_reducer_mark_ready for params[0..n-1], in
+ * that order, all produced on producer_stream (one backward layer's weight and
+ * bias, or a whole backward pass, in one call).  HOST params[n].  Stops at the
+ * first failing parameter and returns its status; the earlier ones stay marked.
+ */
+ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t* params, int32_t n, void* producer_stream);
+
+/*
+ * ddp_reducer_finalize -- end of backward (finalize_backward, DDP chapter
+ * 17.41; Megatron finish_grad_sync): makes consumer_stream (may be NULL: none)
+ * wait for every issued reduction.  With timeout_us > 0 it also waits on the
+ * host, polling, until the reductions finish or the deadline passes.
+ * Errors: DDP_E_INCOMPLETE if some bucket was never issued (message lists the
+ * unmarked parameters); DDP_E_TIMEOUT if the deadline passed (the work stays
+ * queued; call again or synchronise); DDP_E_CUDA.
+ */
+ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream, int64_t timeout_us);
+
+/* Buckets issued in this iteration, in issue order (HOST out[cap]); *n = count. */
+ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n);
+
+/*
+ * Per-bucket GPU time in milliseconds of the last finalized iteration (needs
+ * DDP_R_TIMING; waits for those events).  HOST out[cap], indexed by bucket id.
+ */
+ddp_status ddp_reducer_bucket_ms(ddp_reducer* r, float* out, int32_t cap);
+
+void ddp_reducer_destroy(ddp_reducer* r);
+
+/* ------------------------------------------------------------------------ */
+/* Errors and version                                                        */
+/* ------------------------------------------------------------------------ */
+const char* ddp_status_str(ddp_status s);
+/* Message of the calling thread's last failed call ("" if none). */
+const char* ddp_last_error_message(void);
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t ddp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDP_BUCKET_H */

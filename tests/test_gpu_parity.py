@@ -1,0 +1,445 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Bit-exact comparisons throughout: the kernels reproduce the ring's summation
+order, the fp32 1/W pre-scale and the exact bf16/fp16 widening, so every result
+must match the oracle's bits (the 1e-6 relative bound is never needed).
+"""
+import numpy as np
+import pytest
+
+import allreduce_ddp_assign_gb300 as D
+import oracle as O
+import workloads as WL
+from gpu_util import GUARD, SENTINEL, assert_bits_equal, bits, chunk_of, oracle_at, packed_at
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+DEV = torch.device("cuda:0")
+
+
+def guarded(n_elems: int, offset: int = 0):
+    """A device fp32 buffer of n_elems (+offset) elements with sentinel guard bands."""
+    buf = torch.full((GUARD + offset + n_elems + GUARD,), float(SENTINEL), dtype=torch.float32, device=DEV)
+    return buf, GUARD + offset
+
+
+def check_guards(buf, start, n_elems):
+    h = buf.cpu().numpy()
+    assert np.all(bits(h[:start]) == bits(np.array([SENTINEL]))), "write before the buffer"
+    assert np.all(bits(h[start + n_elems:]) == bits(np.array([SENTINEL]))), "write after the buffer"
+
+
+# ---------------------------------------------------------------------------
+# step 3 alone: ddp_bucket_allreduce
+# ---------------------------------------------------------------------------
+ALLREDUCE_CASES = [(W, n) for W in (1, 2, 3, 4, 5, 8, 16, 64) for n in (0, 1, 3, 4, 7, 64, 1000, 4099, 65549)]
+
+
+@pytest.mark.parametrize("layout", ["tight", "stride_pad", "misaligned"])
+@pytest.mark.parametrize("W,n", ALLREDUCE_CASES)
+def test_allreduce_vs_oracle(orc, W, n, layout):
+    rng = np.random.default_rng(1000 * W + n)
+    for mode in (D.DDP_ALLREDUCE, D.DDP_REDUCE_SCATTER):
+        nn = n - n % W if mode == D.DDP_REDUCE_SCATTER else n
+        stride = nn + (5 if layout == "stride_pad" else 0)
+        stride = max(stride, 1)
+        off = 1 if layout == "misaligned" else 0
+        x = rng.standard_normal((W, nn)).astype(np.float32)
+        buf, start = guarded(W * stride, off)
+        view = buf[start:start + W * stride].view(W, stride)
+        view[:, :nn] = torch.from_numpy(x).to(DEV)
+        D.ddp_bucket_allreduce(buf.data_ptr() + 4 * start, stride, nn, W, mode)
+        torch.cuda.synchronize()
+        want, sent = orc.ring(x.copy(), mode)
+        got = view.cpu().numpy()
+        assert_bits_equal(got[:, :nn], want, f"W={W} n={nn} {layout} mode={mode}")
+        if stride > nn:
+            assert np.all(bits(got[:, nn:]) == bits(np.array([SENTINEL])))
+        check_guards(buf, start, W * stride)
+
+
+def test_allreduce_nonfinite_propagates(orc):
+    """An inf in one replica reaches every replica; +inf and -inf give NaN
+    (DDP chapter, 17.18: one rank's overflow is seen by all)."""
+    W, n = 4, 4096
+    x = np.ones((W, n), np.float32)
+    x[2, 10] = np.inf
+    x[1, 20], x[3, 20] = np.inf, -np.inf
+    t = torch.from_numpy(x).to(DEV)
+    D.ddp_bucket_allreduce(t, n, n, W, D.DDP_ALLREDUCE)
+    got = t.cpu().numpy()
+    want, _ = orc.ring(x.copy())
+    assert np.all(np.isposinf(got[:, 10])) and np.all(np.isnan(got[:, 20]))
+    mask = np.ones(n, bool)
+    mask[20] = False
+    assert_bits_equal(got[:, mask], want[:, mask])
+
+
+# ---------------------------------------------------------------------------
+# steps 2-4: pack, unpack, fused over random segment lists
+# ---------------------------------------------------------------------------
+def random_bucket(rng, W, dtype, nseg, misalign):
+    sizes = [int(s) for s in rng.choice([0, 1, 2, 3, 5, 17, 64, 255, 1024, 4097, 20000], size=nseg)]
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    pad = int(rng.integers(0, 8))
+    numel = int(offs[-1]) + pad
+    grads_np = []
+    for w in range(W):
+        row = []
+        for s in range(nseg):
+            v = rng.standard_normal(sizes[s]).astype(np.float32)
+            if dtype == D.DDP_BF16:
+                v = WL.f32_to_bf16_bits_np(v)
+            elif dtype == D.DDP_F16:
+                v = v.astype(np.float16).view(np.uint16)
+            row.append(v)
+        grads_np.append(row)
+    used = (rng.random((W, nseg)) > 0.2).astype(np.uint8) if nseg else np.zeros((W, 0), np.uint8)
+    # device copies: each replica's segments carved out of one flat allocation at
+    # offsets that are odd when `misalign` (exercising the scalar path)
+    tdt = {D.DDP_F32: torch.float32, D.DDP_BF16: torch.int16, D.DDP_F16: torch.int16}[dtype]
+    keep, ptrs = [], np.zeros(W * max(nseg, 1), np.int64)
+    for w in range(W):
+        total = sum(sizes) + 3 * nseg + 8
+        flat = torch.zeros(total, dtype=tdt, device=DEV)
+        keep.append(flat)
+        pos = 1 if misalign else 0
+        for s in range(nseg):
+            a = grads_np[w][s]
+            t = torch.from_numpy(a.view(np.int16) if dtype != D.DDP_F32 else a)
+            flat[pos:pos + sizes[s]] = t.to(DEV)
+            ptrs[w * nseg + s] = flat.data_ptr() + pos * flat.element_size()
+            pos += sizes[s] + (int(rng.integers(0, 3)) if misalign else (-sizes[s]) % 4)
+    seg_off = torch.from_numpy(offs).to(DEV)
+    seg_par = torch.arange(max(nseg, 1), dtype=torch.int32, device=DEV)
+    desc = D.BucketDesc(numel, nseg, dtype, seg_off.data_ptr(), seg_par.data_ptr())
+    tab = torch.from_numpy(ptrs).to(DEV)
+    return dict(sizes=sizes, offs=offs, numel=numel, grads_np=grads_np, used=used, desc=desc, tab=tab,
+                keep=keep + [seg_off, seg_par], nseg=nseg)
+
+
+def oracle_pack(orc, bk, W, dtype, accumulate, init):
+    segs = [[bk["grads_np"][w][s] if bk["used"][w, s] else None for s in range(bk["nseg"])] for w in range(W)]
+    out = init.copy()
+    return orc.pack(segs, bk["offs"][:-1], bk["numel"], [dtype] * bk["nseg"], used=bk["used"],
+                    accumulate=accumulate, out=out)
+
+
+def alloc_outs(bk, W, fill):
+    outs = [[torch.full((max(s, 1),), fill, dtype=torch.float32, device=DEV) for s in bk["sizes"]] for _ in range(W)]
+    ptrs = np.array([outs[w][s].data_ptr() for w in range(W) for s in range(bk["nseg"])] or [0], np.int64)
+    return outs, torch.from_numpy(ptrs).to(DEV)
+
+
+SEG_CASES = [(W, dt, mis) for W in (1, 2, 3, 4, 8, 16) for dt in (D.DDP_F32, D.DDP_BF16, D.DDP_F16)
+             for mis in (False, True)]
+
+
+@pytest.mark.parametrize("W,dtype,misalign", SEG_CASES)
+def test_staged_pack_reduce_unpack(orc, W, dtype, misalign):
+    rng = np.random.default_rng(W * 31 + dtype * 7 + misalign)
+    for trial in range(3):
+        bk = random_bucket(rng, W, dtype, int(rng.integers(0, 9)), misalign)
+        n, nseg = bk["numel"], bk["nseg"]
+        mode = D.DDP_REDUCE_SCATTER if (trial == 2 and n % W == 0) else D.DDP_ALLREDUCE
+        stride = n + 3
+        init = rng.standard_normal((W, n)).astype(np.float32)
+        buf, start = guarded(W * stride)
+        mg = buf[start:start + W * stride].view(W, stride)
+        mg[:, :n] = torch.from_numpy(init).to(DEV)
+        used_t = torch.from_numpy(bk["used"].reshape(-1).copy()).to(DEV) if nseg else None
+        mgp = buf.data_ptr() + 4 * start
+        for accumulate in (0, 1):
+            D.ddp_pack(bk["desc"], bk["tab"], used_t, max(nseg, 1), W, mgp, stride, accumulate)
+            init = oracle_pack(orc, bk, W, dtype, accumulate, init)
+            assert_bits_equal(mg[:, :n].cpu().numpy(), init, f"pack acc={accumulate}")
+        D.ddp_bucket_allreduce(mgp, stride, n, W, mode)
+        want, _ = orc.ring(init.copy(), mode)
+        assert_bits_equal(mg[:, :n].cpu().numpy(), want, "reduce")
+        gu = bk["used"].max(axis=0) if nseg else np.zeros(0, np.uint8)
+        outs, out_tab = alloc_outs(bk, W, -3.0)
+        gu_t = torch.from_numpy(gu.copy()).to(DEV) if nseg else None
+        D.ddp_unpack(bk["desc"], mgp, stride, W, mode, out_tab, max(nseg, 1), gu_t)
+        exp = orc.unpack(want.copy(), bk["offs"][:-1], bk["sizes"], mode, gu,
+                         outs=[[np.full(s, -3.0, np.float32) for s in bk["sizes"]] for _ in range(W)])
+        for w in range(W):
+            for s in range(nseg):
+                assert_bits_equal(outs[w][s][:bk["sizes"][s]].cpu().numpy(), exp[w][s], f"unpack w={w} s={s}")
+        check_guards(buf, start, W * stride)
+
+
+@pytest.mark.parametrize("W,dtype,misalign", SEG_CASES)
+def test_fused_matches_staged_oracle(orc, W, dtype, misalign):
+    rng = np.random.default_rng(W * 131 + dtype * 17 + misalign)
+    for trial in range(4):
+        bk = random_bucket(rng, W, dtype, int(rng.integers(0, 9)), misalign)
+        n, nseg = bk["numel"], bk["nseg"]
+        mode = D.DDP_REDUCE_SCATTER if (trial % 2 and n % W == 0) else D.DDP_ALLREDUCE
+        accumulate = trial >= 2
+        copy_back = trial in (1, 2)
+        stride = n + (0 if misalign else 4)
+        init = rng.standard_normal((W, n)).astype(np.float32)
+        buf, start = guarded(W * stride)
+        mg = buf[start:start + W * stride].view(W, stride)
+        mg[:, :n] = torch.from_numpy(init).to(DEV)
+        used_t = torch.from_numpy(bk["used"].reshape(-1).copy()).to(DEV) if nseg else None
+        gu = bk["used"].max(axis=0) if nseg else np.zeros(0, np.uint8)
+        gu_t = torch.from_numpy(gu.copy()).to(DEV) if nseg else None
+        outs, out_tab = alloc_outs(bk, W, 5.0) if copy_back else (None, None)
+        D.ddp_fused_bucket(bk["desc"], bk["tab"], used_t, max(nseg, 1), W, mode, int(accumulate),
+                           buf.data_ptr() + 4 * start, stride, out_tab, gu_t)
+        packed = oracle_pack(orc, bk, W, dtype, accumulate, init)
+        want, _ = orc.ring(packed.copy(), mode)
+        got = mg[:, :n].cpu().numpy()
+        if mode == D.DDP_ALLREDUCE:
+            assert_bits_equal(got, want, "fused main_grad")
+        else:
+            k = n // W
+            for w in range(W):  # shard w of replica w reduced; the rest untouched
+                assert_bits_equal(got[w, w * k:(w + 1) * k], want[w, w * k:(w + 1) * k], f"shard {w}")
+                rest = np.ones(n, bool)
+                rest[w * k:(w + 1) * k] = False
+                assert_bits_equal(got[w, rest], init[w, rest], f"outside shard {w}")
+        if copy_back:
+            exp = orc.unpack(want.copy(), bk["offs"][:-1], bk["sizes"], mode, gu,
+                             outs=[[np.full(s, 5.0, np.float32) for s in bk["sizes"]] for _ in range(W)])
+            for w in range(W):
+                for s in range(nseg):
+                    assert_bits_equal(outs[w][s][:bk["sizes"][s]].cpu().numpy(), exp[w][s], f"copy-back {w},{s}")
+        check_guards(buf, start, W * stride)
+
+
+def test_fused_in_place_without_main_grad(orc):
+    """grads_out aliasing fp32 grads, no bucket buffer: DDP without
+    gradient_as_bucket_view, reduced straight back into .grad."""
+    rng = np.random.default_rng(5)
+    W = 8
+    bk = random_bucket(rng, W, D.DDP_F32, 7, False)
+    D.ddp_fused_bucket(bk["desc"], bk["tab"], None, bk["nseg"], W, D.DDP_ALLREDUCE, 0, None, 0, bk["tab"], None)
+    bk["used"][:] = 1
+    packed = oracle_pack(orc, bk, W, D.DDP_F32, False, np.zeros((W, bk["numel"]), np.float32))
+    want, _ = orc.ring(packed, D.DDP_ALLREDUCE)
+    flat = bk["keep"]
+    for w in range(W):
+        pos = 0
+        for s, sz in enumerate(bk["sizes"]):
+            got = flat[w][pos:pos + sz].cpu().numpy()
+            assert_bits_equal(got, want[w, bk["offs"][s]:bk["offs"][s] + sz], f"in place w={w} s={s}")
+            pos += sz + (-sz) % 4
+
+
+# ---------------------------------------------------------------------------
+# the workloads, through the same reducer path the benchmark times
+# ---------------------------------------------------------------------------
+def device_grads(wl, m=0, skip_unused=True):
+    return [[None if (skip_unused and p in wl.unused) else WL.grad_torch(wl, p, w, m, DEV)
+             for p in range(wl.nparams)] for w in range(wl.W)]
+
+
+def used_flags(wl):
+    u = np.ones((wl.W, wl.nparams), np.uint8)
+    u[:, wl.unused] = 0
+    return u
+
+
+def make_session(wl, grads, fused=True, grads_out=None, timing=False):
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    return BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                         wl.first_cap_bytes, wl.pad_multiple, grads, used=used_flags(wl) if wl.unused else None,
+                         grads_out=grads_out, fused=fused, timing=timing)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_workload_full_vs_oracle(orc, name, fused):
+    wl = WL.ALL[name]()
+    sess = make_session(wl, device_grads(wl), fused=fused)
+    sess.step()
+    torch.cuda.synchronize()
+    ref = O.run_workload(wl, orc, copy_back=False)
+    assert sess.plan.nbuckets == ref["plan"]["nbuckets"]
+    for b in range(sess.plan.nbuckets):
+        got = sess.plan.bucket_view(sess.main_grad, b).cpu().numpy()
+        assert_bits_equal(got, ref["bucket"][b], f"{name} bucket {b}")
+    if name == "c1":  # dyadic inputs: the mean is exact
+        x = [[WL.grad_np(wl, p, w) for p in range(wl.nparams)] for w in range(wl.W)]
+        for p in range(wl.nparams):
+            mean = sum(x[w][p].astype(np.float64) for w in range(wl.W)) / wl.W
+            assert np.array_equal(sess.view(p, 3).cpu().numpy().astype(np.float64), mean)
+    sess.close()
+
+
+def test_mlp_copy_back_partial_use(orc):
+    """C1 with copy-back, parameter 2 unused on replica 1 only and parameter 4 on no
+    replica: partial use averages in a zero, global non-use leaves .grad alone."""
+    wl = WL.c1_mlp()
+    grads = device_grads(wl)
+    used = np.ones((wl.W, wl.nparams), np.uint8)
+    used[1, 2] = 0
+    used[:, 4] = 0
+    outs = [[torch.full((n,), 9.0, device=DEV) for n in wl.numels] for _ in range(wl.W)]
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    for fused in (True, False):
+        for w in range(wl.W):
+            for p in range(wl.nparams):
+                outs[w][p].fill_(9.0)
+        sess = BucketReducer(wl.numels, None, wl.W, wl.mode, wl.order, wl.cap_bytes, wl.first_cap_bytes, 1, grads,
+                             used=used, grads_out=outs, fused=fused)
+        sess.step()
+        torch.cuda.synchronize()
+        raw = [[[None if not used[w, p] else WL.grad_raw_np(wl, p, w) for p in range(wl.nparams)]
+                for w in range(wl.W)]]
+        plan = orc.assign(wl.numels, None, wl.cap_bytes, wl.first_cap_bytes, wl.order)
+        mem = plan["members"][0]
+        offs = [int(plan["offset_of"][p]) for p in mem]
+        buf = orc.pack([[raw[0][w][p] for p in mem] for w in range(wl.W)], offs, int(plan["bucket_numel"][0]),
+                       used=used[:, mem])
+        buf, _ = orc.ring(buf)
+        exp = orc.unpack(buf, offs, [wl.numels[p] for p in mem], 0, used.max(axis=0)[mem],
+                         outs=[[np.full(wl.numels[p], 9.0, np.float32) for p in mem] for _ in range(wl.W)])
+        for w in range(wl.W):
+            for j, p in enumerate(mem):
+                assert_bits_equal(outs[w][p].cpu().numpy(), exp[w][j], f"fused={fused} w={w} p={p}")
+        assert np.all(outs[0][4].cpu().numpy() == 9.0)
+        sess.close()
+
+
+def _sample(rng, n, k=1500):
+    return np.unique(np.concatenate([rng.integers(0, n, k), [0, n - 1]]))
+
+
+@pytest.mark.slow
+def test_gpt2_reduce_scatter_full_size_sampled(orc):
+    """GPT-2 small, bf16 -> fp32, Megatron buckets, W = 8 reduce_scatter: sampled
+    elements of every shard against the oracle; nothing outside the shards written."""
+    wl = WL.c3_gpt2()
+    sess = make_session(wl, device_grads(wl))
+    sess.main_grad.fill_(float(SENTINEL))
+    sess.step()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(33)
+    plan = sess.plan
+    for b in range(plan.nbuckets):
+        n = int(plan.bucket_numel[b])
+        got = plan.bucket_view(sess.main_grad, b).cpu().numpy()
+        k = n // wl.W
+        for w in range(wl.W):  # outside shard w, replica w keeps the sentinel
+            assert np.all(bits(got[w, :w * k]) == bits(np.array([SENTINEL])))
+            assert np.all(bits(got[w, (w + 1) * k:]) == bits(np.array([SENTINEL])))
+        e = _sample(rng, n)
+        owner = chunk_of(e, n, wl.W)
+        t = np.zeros((wl.W, len(e)), np.float32)
+        for p in plan.members[b]:
+            lo, hi = int(plan.offset_of[p]), int(plan.offset_of[p]) + wl.numels[p]
+            sel = np.nonzero((e >= lo) & (e < hi))[0]
+            if len(sel):
+                t[:, sel] = packed_at(orc, wl, p, e[sel] - lo, 1)
+        want = oracle_at(orc, t, owner)
+        assert_bits_equal(got[owner, e], want, f"bucket {b}")
+    sess.close()
+
+
+@pytest.mark.slow
+def test_bert_nosync_full_size_sampled(orc):
+    """BERT-large, W = 4: three no_sync micro-steps accumulated locally, the fourth
+    reduced with the accumulated sum; one encoder layer unused (zero)."""
+    wl = WL.c4_bert_large()
+    sess = make_session(wl, device_grads(wl, 3))
+    for m in range(3):
+        g = device_grads(wl, m)
+        tab = sess.plan.pointer_table(g)
+        sess.accumulate_local(tab, first=m == 0)
+        torch.cuda.synchronize()
+        del tab, g
+    sess.step(accumulate=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(44)
+    plan = sess.plan
+    used = used_flags(wl)
+    for b in range(plan.nbuckets):
+        n = int(plan.bucket_numel[b])
+        got = plan.bucket_view(sess.main_grad, b).cpu().numpy()
+        for w in range(1, wl.W):
+            assert np.array_equal(bits(got[0]), bits(got[w]))
+        e = _sample(rng, n, 500)
+        t = np.zeros((wl.W, len(e)), np.float32)
+        for p in plan.members[b]:
+            lo, hi = int(plan.offset_of[p]), int(plan.offset_of[p]) + wl.numels[p]
+            sel = np.nonzero((e >= lo) & (e < hi))[0]
+            if len(sel):
+                t[:, sel] = packed_at(orc, wl, p, e[sel] - lo, 4, used[:, p])
+        want = oracle_at(orc, t, chunk_of(e, n, wl.W))
+        assert_bits_equal(got[0, e], want, f"bucket {b}")
+    for p in wl.unused:
+        assert not torch.any(sess.view(p, 2))
+    sess.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("nbytes,W", [(1 << 30, 16), (1 << 28, 2), ((1 << 20) + 4 * 13, 8)])
+def test_sweep_bucket_sampled(orc, nbytes, W):
+    n = nbytes // 4
+    x = WL.bucket_torch(nbytes, W, DEV)
+    D.ddp_bucket_allreduce(x, n, n, W, D.DDP_ALLREDUCE)
+    torch.cuda.synchronize()
+    for w in range(1, W):
+        assert torch.equal(x[0], x[w])
+    rng = np.random.default_rng(55)
+    e = _sample(rng, n, 4000)
+    t = np.stack([WL.values_np(WL.bits_at_np(WL.stream_key(1005, WL.stream_id(0, w)), e), "uniform")
+                  for w in range(W)])
+    want = oracle_at(orc, t, chunk_of(e, n, W))
+    assert_bits_equal(x[W - 1, torch.from_numpy(e).to(DEV)].cpu().numpy(), want)
+
+
+# ---------------------------------------------------------------------------
+# the reducer on real streams
+# ---------------------------------------------------------------------------
+def test_reducer_waits_for_producer_stream(orc):
+    """Gradients are written on a delayed producer stream just before each
+    mark_ready; the side stream must see them (event-gated issue)."""
+    wl = WL.Workload("linear12", WL.linear12(), 4, 0, 0, 25 << 20, 1 << 20, 1, 0, "dyadic12", 1.0, 77)
+    final = device_grads(wl)
+    grads = [[torch.zeros_like(final[w][p]) for p in range(wl.nparams)] for w in range(wl.W)]
+    sess = make_session(wl, grads, timing=True)
+    prod = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    D.ddp_reducer_prepare(sess.handle, 0)
+    with torch.cuda.stream(prod):
+        for p in sess.ready_order:
+            torch.cuda._sleep(200_000)
+            for w in range(wl.W):
+                grads[w][p].copy_(final[w][p])
+            D.ddp_reducer_mark_ready(sess.handle, p, prod)
+    sess.finalize(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert sess.issue_log() == [0, 1, 2]
+    ref = O.run_workload(wl, orc, copy_back=False)
+    for b in range(3):
+        assert_bits_equal(sess.plan.bucket_view(sess.main_grad, b).cpu().numpy(), ref["bucket"][b], f"bucket {b}")
+    ms = sess.bucket_ms()
+    assert np.all(ms > 0)
+    sess.close()
+
+
+def test_reducer_finalize_timeout_then_recovers(orc):
+    wl = WL.c1_mlp()
+    sess = make_session(wl, device_grads(wl))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(sess.side):
+        torch.cuda._sleep(400_000_000)   # ~0.2 s of spinning on the side stream (bounded)
+    sess.backward()
+    with pytest.raises(D.DdpError) as e:
+        sess.finalize(None, timeout_us=2000)
+    assert e.value.status == D.DDP_E_TIMEOUT
+    sess.finalize(None, timeout_us=30_000_000)    # same iteration: now it completes
+    torch.cuda.synchronize()
+    ref = O.run_workload(wl, orc, copy_back=False)
+    assert_bits_equal(sess.plan.bucket_view(sess.main_grad, 0).cpu().numpy(), ref["bucket"][0])
+    sess.close()

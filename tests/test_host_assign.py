@@ -1,0 +1,45 @@
+"""The library's bucket assignment equals the oracle's, bit for bit (CPU only)."""
+import numpy as np
+import pytest
+
+import allreduce_ddp_assign_gb300 as D
+import workloads as WL
+
+KEYS = ("bucket_of", "offset_of", "bucket_numel", "bucket_bytes", "bucket_dtype", "bucket_order")
+
+
+def same(a, r):
+    assert a["nbuckets"] == r["nbuckets"]
+    for k in KEYS:
+        assert np.array_equal(a[k], r[k]), k
+    assert [int(p) for p in a["members"]] == [p for m in r["members"] for p in m]
+
+
+@pytest.mark.parametrize("name", sorted(WL.ALL))
+def test_configs(orc, name):
+    wl = WL.ALL[name]()
+    args = (wl.numels, [wl.dtype] * wl.nparams, wl.cap_bytes, wl.first_cap_bytes, wl.order, wl.pad_multiple, 1)
+    same(D.ddp_assign_buckets(*args), orc.assign(*args))
+
+
+@pytest.mark.parametrize("order", [0, 1, 2])
+def test_page_examples(orc, order):
+    for n, cap, first in ((WL.numels(WL.linear12()), 25 << 20, 1 << 20),
+                          ([2_500_000, 500_000, 2_000_000, 5_000_000, 1_000_000], 12_000_000, 12_000_000),
+                          (WL.numels(WL.resnet50()), 25_000_000, 25_000_000),
+                          (WL.numels(WL.bert_large()), 25_000_000, 25_000_000)):
+        same(D.ddp_assign_buckets(n, None, cap, first, order), orc.assign(n, None, cap, first, order))
+
+
+def test_random(orc):
+    rng = np.random.default_rng(3)
+    for trial in range(400):
+        P = int(rng.integers(0, 30))
+        n = rng.integers(0, 5000, size=P)
+        dt = rng.integers(0, 3, size=P) if trial % 3 else np.zeros(P, np.int64)
+        cap = int(rng.integers(1, 20000))
+        first = int(rng.integers(1, 20000))
+        order = int(rng.integers(0, 3))
+        pad = int(rng.integers(1, 9))
+        fp32 = int(rng.integers(0, 2))
+        same(D.ddp_assign_buckets(n, dt, cap, first, order, pad, fp32), orc.assign(n, dt, cap, first, order, pad, fp32))

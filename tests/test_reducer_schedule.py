@@ -1,0 +1,124 @@
+"""The reducer's schedule (pending counts, in-order issue, errors) on the host,
+in dry-run mode: no CUDA call is made (CPU only)."""
+import pytest
+
+import allreduce_ddp_assign_gb300 as D
+
+
+def make(bucket_of, order=None, nb=None):
+    nb = nb if nb is not None else max(bucket_of) + 1
+    order = list(range(nb)) if order is None else order
+    descs = [D.BucketDesc(8, 0, 0, None, None) for _ in range(nb)]
+    return D.ddp_reducer_create(len(bucket_of), bucket_of, order, descs, [0] * nb, 2, D.DDP_ALLREDUCE,
+                                D.DDP_R_DRY_RUN | D.DDP_R_FUSED, replica_stride=8)
+
+
+def test_in_order_issue_when_ready_out_of_order():
+    # params 0,1 -> bucket 0; 2 -> bucket 1; 3,4 -> bucket 2 (lecture, section 2.3)
+    r = make([0, 0, 1, 2, 2])
+    D.ddp_reducer_prepare(r)
+    for p in (3, 4):             # bucket 2 fills first: nothing may be issued
+        D.ddp_reducer_mark_ready(r, p)
+    assert D.ddp_reducer_issue_log(r) == []
+    D.ddp_reducer_mark_ready(r, 2)        # bucket 1 ready, bucket 0 still pending
+    assert D.ddp_reducer_issue_log(r) == []
+    D.ddp_reducer_mark_ready(r, 0)
+    assert D.ddp_reducer_issue_log(r) == []
+    D.ddp_reducer_mark_ready(r, 1)        # bucket 0 completes: 0, 1, 2 go out in order
+    assert D.ddp_reducer_issue_log(r) == [0, 1, 2]
+    D.ddp_reducer_finalize(r)
+    D.ddp_reducer_destroy(r)
+
+
+def test_issue_as_soon_as_prefix_ready():
+    r = make([0, 1, 2])
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready(r, 0)
+    assert D.ddp_reducer_issue_log(r) == [0]
+    D.ddp_reducer_mark_ready(r, 1)
+    assert D.ddp_reducer_issue_log(r) == [0, 1]
+    D.ddp_reducer_mark_ready(r, 2)
+    D.ddp_reducer_finalize(r)
+    D.ddp_reducer_destroy(r)
+
+
+def test_megatron_issue_order_is_last_to_first():
+    plan = D.ddp_assign_buckets([10] * 6, None, 80, 80, D.DDP_ORDER_MEGATRON)
+    assert plan["nbuckets"] == 3
+    r = make(plan["bucket_of"], list(plan["bucket_order"]))
+    D.ddp_reducer_prepare(r)
+    for p in range(5, -1, -1):  # backward produces the last parameters first
+        D.ddp_reducer_mark_ready(r, p)
+    assert D.ddp_reducer_issue_log(r) == [2, 1, 0]
+    D.ddp_reducer_finalize(r)
+    D.ddp_reducer_destroy(r)
+
+
+def test_double_mark_is_a_state_error():
+    r = make([0, 0])
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready(r, 1)
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_mark_ready(r, 1)
+    assert e.value.status == D.DDP_E_STATE and "parameter 1" in str(e.value)
+    D.ddp_reducer_destroy(r)
+
+
+def test_missing_mark_reported_at_finalize_and_next_prepare():
+    r = make([0, 0, 1, 1])
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready(r, 0)
+    D.ddp_reducer_mark_ready(r, 1)
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_finalize(r)
+    assert e.value.status == D.DDP_E_INCOMPLETE and e.value.args[0].endswith(": 2 3")
+    with pytest.raises(D.DdpError) as e:            # next iteration starts: same complaint
+        D.ddp_reducer_prepare(r)
+    assert e.value.status == D.DDP_E_INCOMPLETE and "2 3" in str(e.value)
+    # the reducer was reset anyway: a full iteration now works
+    for p in range(4):
+        D.ddp_reducer_mark_ready(r, p)
+    D.ddp_reducer_finalize(r)
+    assert D.ddp_reducer_issue_log(r) == [0, 1]
+    D.ddp_reducer_destroy(r)
+
+
+def test_mark_outside_iteration_and_bad_index():
+    r = make([0])
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_mark_ready(r, 0)
+    assert e.value.status == D.DDP_E_STATE
+    D.ddp_reducer_prepare(r)
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_mark_ready(r, 7)
+    assert e.value.status == D.DDP_E_INVAL
+    D.ddp_reducer_destroy(r)
+
+
+def test_create_validation():
+    descs = [D.BucketDesc(8, 0, 0, None, None)]
+    with pytest.raises(D.DdpError):    # bucket_of points past the buckets
+        D.ddp_reducer_create(2, [0, 1], [0], descs, [0], 2, 0, D.DDP_R_DRY_RUN, replica_stride=8)
+    with pytest.raises(D.DdpError):    # order not a permutation
+        D.ddp_reducer_create(2, [0, 1], [1, 1], descs * 2, [0, 0], 2, 0, D.DDP_R_DRY_RUN, replica_stride=8)
+    with pytest.raises(D.DdpError):    # a bucket without parameters
+        D.ddp_reducer_create(2, [0, 0], [0, 1], descs * 2, [0, 0], 2, 0, D.DDP_R_DRY_RUN, replica_stride=8)
+    with pytest.raises(D.DdpError):    # reduce_scatter needs numel % W == 0
+        D.ddp_reducer_create(1, [0], [0], [D.BucketDesc(7, 0, 0, None, None)], [0], 2, 1, D.DDP_R_DRY_RUN,
+                             replica_stride=8)
+    with pytest.raises(D.DdpError):    # bucket past the replica stride
+        D.ddp_reducer_create(1, [0], [0], descs, [4], 2, 0, D.DDP_R_DRY_RUN, replica_stride=8)
+
+
+def test_repeated_iterations_and_timing_refused_in_dry_run():
+    r = make([0, 1, 1])
+    for _ in range(3):
+        D.ddp_reducer_prepare(r)
+        for p in (2, 1, 0):
+            D.ddp_reducer_mark_ready(r, p)
+        D.ddp_reducer_finalize(r)
+        assert D.ddp_reducer_issue_log(r) == [0, 1]
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_bucket_ms(r, 2)
+    assert e.value.status == D.DDP_E_STATE
+    D.ddp_reducer_destroy(r)
