@@ -23,7 +23,8 @@ DDP_OK, DDP_E_INVAL, DDP_E_ALIGN, DDP_E_CUDA, DDP_E_STATE, DDP_E_INCOMPLETE, DDP
 DDP_F32, DDP_BF16, DDP_F16 = 0, 1, 2
 DDP_ORDER_REVERSE, DDP_ORDER_FWD_THEN_REVERSE, DDP_ORDER_MEGATRON = 0, 1, 2
 DDP_ALLREDUCE, DDP_REDUCE_SCATTER = 0, 1
-DDP_R_FUSED, DDP_R_COPY_BACK, DDP_R_TIMING, DDP_R_DRY_RUN = 1, 2, 4, 8
+DDP_R_FUSED, DDP_R_COPY_BACK, DDP_R_TIMING, DDP_R_DRY_RUN, DDP_R_COALESCE = 1, 2, 4, 8, 16
+DDP_KERNEL_AUTO, DDP_KERNEL_PLAIN = 0, 1
 
 
 class DdpError(RuntimeError):
@@ -53,6 +54,8 @@ _SIGS = {
                                _vp]),
     "ddp_fused_bucket": (C.c_int32, [C.POINTER(BucketDesc), _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                      _vp, C.c_int64, _vp, _vp, _vp]),
+    "ddp_fused_bucket_group": (C.c_int32, [C.POINTER(BucketDesc), _i64p, C.c_int32, _vp, _vp, C.c_int32, C.c_int32,
+                                           C.c_int32, C.c_int32, _vp, C.c_int64, _vp, _vp, _vp]),
     "ddp_reducer_create": (C.c_int32, [C.c_int32, C.c_int32, _i32p, _i32p, C.POINTER(BucketDesc), _i64p, C.c_int32,
                                        C.c_int32, C.c_int32, _vp, _vp, C.c_int32, _vp, C.c_int64, _vp, _vp, _vp,
                                        C.POINTER(_vp)]),
@@ -63,6 +66,8 @@ _SIGS = {
     "ddp_reducer_issue_log": (C.c_int32, [_vp, _i32p, C.c_int32, _i32p]),
     "ddp_reducer_bucket_ms": (C.c_int32, [_vp, C.POINTER(C.c_float), C.c_int32]),
     "ddp_reducer_destroy": (None, [_vp]),
+    "ddp_set_kernel_variant": (C.c_int32, [C.c_int32]),
+    "ddp_device_status": (C.c_int32, [_vp, _i32p, C.c_int32]),
     "ddp_status_str": (C.c_char_p, [C.c_int32]),
     "ddp_last_error_message": (C.c_char_p, []),
     "ddp_version": (C.c_int32, []),
@@ -190,6 +195,16 @@ def ddp_fused_bucket(desc: BucketDesc, grads, used, ld, W, mode, accumulate, mai
                                   _ptr(global_used), _stream(stream)))
 
 
+def ddp_fused_bucket_group(descs, bucket_start, grads, used, ld, W, mode, accumulate, main_grad, replica_stride,
+                           grads_out=None, global_used=None, stream=None) -> None:
+    B = len(descs)
+    arr = (BucketDesc * max(B, 1))(*descs)
+    starts = _a(bucket_start, np.int64)
+    _check(lib().ddp_fused_bucket_group(arr, _cp(starts, _i64p), B, _ptr(grads), _ptr(used), int(ld), int(W),
+                                        int(mode), int(accumulate), _ptr(main_grad), int(replica_stride),
+                                        _ptr(grads_out), _ptr(global_used), _stream(stream)))
+
+
 # ---------------------------------------------------------------------------
 # step 5
 # ---------------------------------------------------------------------------
@@ -242,6 +257,16 @@ def ddp_reducer_bucket_ms(r, nbuckets) -> np.ndarray:
 def ddp_reducer_destroy(r) -> None:
     if r:
         lib().ddp_reducer_destroy(r)
+
+
+def ddp_set_kernel_variant(variant: int) -> None:
+    _check(lib().ddp_set_kernel_variant(int(variant)))
+
+
+def ddp_device_status(stream=None, reset=False) -> int:
+    v = C.c_int32(0)
+    _check(lib().ddp_device_status(_stream(stream), C.byref(v), int(bool(reset))))
+    return v.value
 
 
 def ddp_status_str(s: int) -> str:

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUTDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUTDIR, "libddpbucket.so")
-SOURCES = ["kernels.cu", "reducer.cpp", "assign.cpp", "status.cpp"]
+SOURCES = ["kernels.cu", "stream.cu", "reducer.cpp", "assign.cpp", "status.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,6 +31,7 @@ def nvcc() -> str:
 
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "common.h"),
+                                                        os.path.join(CSRC, "device_common.cuh"),
                                                         os.path.join(INCLUDE, "ddp_bucket.h")]
     return files
 
@@ -42,15 +43,19 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
-    if not force and not extra and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra: tuple = (), out: str | None = None) -> str:
+    """Compile and link; `extra` adds nvcc flags (e.g. -D tunables) and `out` names
+    another library path (the objects then go beside it)."""
+    lib = out or LIB
+    if not force and not extra and out is None and up_to_date():
         return LIB
-    os.makedirs(OUTDIR, exist_ok=True)
+    outdir = os.path.dirname(lib)
+    os.makedirs(outdir, exist_ok=True)
     cc = nvcc()
     common = ["-std=c++17", "-O3", "-I", INCLUDE, "-Xcompiler", "-fPIC", "--cudart", "shared", *extra]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUTDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(outdir, os.path.basename(src) + ".o")
         cmd = [cc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cu"):
             cmd[1:1] = [*ARCH, "-lineinfo"]
@@ -63,13 +68,13 @@ def build(force: bool = False, verbose: bool = False, extra: tuple = ()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, "-shared", *ARCH, "--cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -25,5 +25,9 @@ ddp_status launch_unpack(const ddp_bucket_desc& b, const float* main_grad, int64
 ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
                         int32_t W, int32_t mode, int32_t accumulate, float* main_grad, int64_t stride,
                         void* const* grads_out, const uint8_t* global_used, void* stream);
+// Several buckets (bs[i] with main_grad copy mgs[i], may be null) in as few launches as possible.
+ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
+                              const uint8_t* used, int32_t ld, int32_t W, int32_t mode, int32_t accumulate,
+                              int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream);
 
 }  // namespace ddp

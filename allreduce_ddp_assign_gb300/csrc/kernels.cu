@@ -28,115 +28,12 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <vector>
 
 #include "common.h"
+#include "device_common.cuh"
 
-namespace {
-
-constexpr int kThreads = 256;
-constexpr int64_t kMinElemsPerCta = 4096;
-
-enum Op { OP_RING = 0, OP_PACK = 1, OP_FUSED = 2, OP_UNPACK = 3 };
-
-struct Ctx {
-    int64_t n;          // bucket elements, padding included
-    int64_t chunk;      // ring chunk length (n when the op has no ring order)
-    int32_t nchunks;    // W for ring-ordered ops, 1 otherwise
-    int32_t W;
-    int32_t mode;
-    int32_t accumulate;
-    float inv_w;
-    int32_t nseg;       // 0 with seg_offset == nullptr: the whole bucket is one piece
-    const int64_t* seg_offset;
-    const int32_t* seg_param;
-    int32_t ld;
-    const void* const* grads;
-    const uint8_t* used;
-    void* const* grads_out;
-    const uint8_t* global_used;
-    float* mg;          // replica 0 of the bucket (main_grad), may be null for OP_FUSED
-    int64_t stride;     // elements between replicas of mg
-    int32_t mg_vec;     // every replica of mg is 16-byte aligned
-};
-
-struct PieceShared {
-    const void* src[ddp::kMaxReplicas];  // replica w's gradient of the piece's parameter, or null
-    float* dst[ddp::kMaxReplicas];       // replica w's output of that parameter, or null
-};
-
-// ---------------------------------------------------------------------------
-// element access
-// ---------------------------------------------------------------------------
-template <int VEC> struct Lane;
-
-template <> struct Lane<4> {
-    using T = float4;
-    __device__ __forceinline__ static T zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
-    __device__ __forceinline__ static T ld(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-    __device__ __forceinline__ static void st(float* p, T v) { __stcs(reinterpret_cast<float4*>(p), v); }
-    __device__ __forceinline__ static T mul(T a, float s)
-    {
-        return make_float4(__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(a.z, s), __fmul_rn(a.w, s));
-    }
-    __device__ __forceinline__ static T add(T a, T b)
-    {
-        return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
-    }
-    template <int DT> __device__ __forceinline__ static T ldg(const void* base, int64_t i);
-};
-
-template <> __device__ __forceinline__ float4 Lane<4>::ldg<DDP_F32>(const void* base, int64_t i)
-{
-    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
-}
-template <> __device__ __forceinline__ float4 Lane<4>::ldg<DDP_BF16>(const void* base, int64_t i)
-{
-    // bf16 -> fp32 widening is exact: the bf16 bits become the upper half
-    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i));
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
-template <> __device__ __forceinline__ float4 Lane<4>::ldg<DDP_F16>(const void* base, int64_t i)
-{
-    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i));
-    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
-
-template <> struct Lane<1> {
-    using T = float;
-    __device__ __forceinline__ static T zero() { return 0.f; }
-    __device__ __forceinline__ static T ld(const float* p) { return __ldcs(p); }
-    __device__ __forceinline__ static void st(float* p, T v) { __stcs(p, v); }
-    __device__ __forceinline__ static T mul(T a, float s) { return __fmul_rn(a, s); }
-    __device__ __forceinline__ static T add(T a, T b) { return __fadd_rn(a, b); }
-    template <int DT> __device__ __forceinline__ static T ldg(const void* base, int64_t i);
-};
-
-template <> __device__ __forceinline__ float Lane<1>::ldg<DDP_F32>(const void* base, int64_t i)
-{
-    return __ldcs(static_cast<const float*>(base) + i);
-}
-template <> __device__ __forceinline__ float Lane<1>::ldg<DDP_BF16>(const void* base, int64_t i)
-{
-    return __uint_as_float(static_cast<uint32_t>(__ldcs(static_cast<const unsigned short*>(base) + i)) << 16);
-}
-template <> __device__ __forceinline__ float Lane<1>::ldg<DDP_F16>(const void* base, int64_t i)
-{
-    return __half2float(__ushort_as_half(__ldcs(static_cast<const unsigned short*>(base) + i)));
-}
-
-__host__ __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
-__host__ __device__ __forceinline__ int64_t lmax(int64_t a, int64_t b) { return a > b ? a : b; }
-
-template <int DT> __host__ __device__ constexpr int elem_bytes() { return DT == DDP_F32 ? 4 : 2; }
-
-// Loads per thread kept in flight: about 16 vectors whatever W is.
-template <int WT> __host__ __device__ constexpr int unroll_for()
-{
-    return WT == 2 ? 4 : (WT == 4 ? 2 : 1);
-}
+namespace ddpk {
 
 // ---------------------------------------------------------------------------
 // one piece: elements [a, b) of chunk c, inside one segment (or the padding)
@@ -418,15 +315,39 @@ void set_mg(Ctx& cx, float* mg, int64_t stride)
     cx.mg_vec = mg && (reinterpret_cast<uintptr_t>(mg) % 16 == 0) && (stride % 4 == 0);
 }
 
-}  // namespace
+int g_variant = DDP_KERNEL_AUTO;
+int kernel_variant() { return g_variant; }
+
+}  // namespace ddpk
+
+extern "C" ddp_status ddp_set_kernel_variant(int32_t variant)
+{
+    if (variant != DDP_KERNEL_AUTO && variant != DDP_KERNEL_PLAIN)
+        return ddp::fail(DDP_E_INVAL, "ddp_set_kernel_variant: unknown variant %d", variant);
+    ddpk::g_variant = variant;
+    return ddp::ok();
+}
 
 namespace ddp {
+
+using namespace ddpk;
 
 ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream)
 {
     if (n == 0 || W == 1) return ok();  // the mean of one replica is the replica (x * 1 is exact)
     Ctx cx = base_ctx(n, W, true, mode);
     set_mg(cx, replicas, stride);
+    if (kernel_variant() == DDP_KERNEL_AUTO && cx.mg_vec && stream_supported(OP_RING, W, DDP_F32, false, mode)) {
+        StreamArgs a{};
+        a.total = n;
+        a.stride = stride;
+        a.inv_w = cx.inv_w;
+        a.W = W;
+        a.mode = mode;
+        a.nb = 1;
+        a.span[0] = StreamSpan{n, 0, replicas, nullptr, nullptr, 0, 1};
+        return launch_stream(OP_RING, a, DDP_F32, stream);
+    }
     return dispatch<OP_RING>(cx, DDP_F32, stream);
 }
 
@@ -472,7 +393,59 @@ ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, cons
     cx.grads_out = grads_out;
     cx.global_used = global_used;
     cx.accumulate = accumulate != 0;
+    if (kernel_variant() == DDP_KERNEL_AUTO && stream_supported(OP_FUSED, W, b.dtype, cx.accumulate, mode)) {
+        float* mgs[1] = {main_grad};
+        return launch_fused_group(&b, mgs, 1, grads, used, ld, W, mode, accumulate, stride, grads_out, global_used,
+                                  stream);
+    }
     return dispatch<OP_FUSED>(cx, b.dtype, stream);
+}
+
+ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
+                              const uint8_t* used, int32_t ld, int32_t W, int32_t mode, int32_t accumulate,
+                              int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream)
+{
+    const bool acc = accumulate != 0;
+    int32_t i = 0;
+    while (i < nb) {
+        // one streaming launch per run of same-dtype buckets (at most kMaxBatch)
+        const int32_t dt = bs[i].dtype;
+        if (kernel_variant() != DDP_KERNEL_AUTO || !stream_supported(OP_FUSED, W, dt, acc, mode)) {
+            const ddp_status st = launch_fused(bs[i], grads, used, ld, W, mode, accumulate, mgs[i], stride, grads_out,
+                                               global_used, stream);
+            if (st != DDP_OK) return st;
+            ++i;
+            continue;
+        }
+        StreamArgs a{};
+        a.stride = stride;
+        a.grads = grads;
+        a.used = used;
+        a.grads_out = grads_out;
+        a.global_used = global_used;
+        a.inv_w = 1.0f / static_cast<float>(W);
+        a.W = W;
+        a.mode = mode;
+        a.accumulate = acc;
+        a.ld = ld;
+        int64_t total = 0;
+        int32_t n = 0;
+        while (i < nb && n < kMaxBatch && bs[i].dtype == dt) {
+            const ddp_bucket_desc& d = bs[i];
+            float* mg = mgs[i];
+            const int32_t vec = mg && (reinterpret_cast<uintptr_t>(mg) % 16 == 0) && (stride % 4 == 0);
+            a.span[n] = StreamSpan{d.numel, total, mg, d.nseg > 0 ? d.seg_offset : nullptr, d.seg_param, d.nseg, vec};
+            total += d.numel;
+            ++n;
+            ++i;
+        }
+        a.nb = n;
+        a.total = total;
+        if (total == 0) continue;
+        const ddp_status st = launch_stream(OP_FUSED, a, dt, stream);
+        if (st != DDP_OK) return st;
+    }
+    return ok();
 }
 
 }  // namespace ddp
@@ -564,6 +537,37 @@ extern "C" ddp_status ddp_unpack(const ddp_bucket_desc* bucket, const float* mai
     if (bucket->nseg > 0 && !grads_out) return ddp::fail(DDP_E_INVAL, "%s: grads_out table is NULL", fn);
     DDP_TRY(check_mg(fn, main_grad, replica_stride, bucket->numel, W));
     return ddp::launch_unpack(*bucket, main_grad, replica_stride, W, mode, grads_out, ld, global_used, stream);
+}
+
+extern "C" ddp_status ddp_fused_bucket_group(const ddp_bucket_desc* buckets, const int64_t* bucket_start,
+                                             int32_t nbuckets, const void* const* grads, const uint8_t* used,
+                                             int32_t ld, int32_t W, int32_t mode, int32_t accumulate, float* main_grad,
+                                             int64_t replica_stride, void* const* grads_out,
+                                             const uint8_t* global_used, void* stream)
+{
+    const char* fn = "ddp_fused_bucket_group";
+    DDP_TRY(check_w(fn, W));
+    if (nbuckets < 0 || (nbuckets > 0 && (!buckets || (main_grad && !bucket_start))))
+        return ddp::fail(DDP_E_INVAL, "%s: bad bucket list", fn);
+    std::vector<float*> mgs(static_cast<size_t>(nbuckets), nullptr);
+    for (int32_t b = 0; b < nbuckets; ++b) {
+        DDP_TRY(check_desc(fn, &buckets[b], ld, true));
+        DDP_TRY(check_mode(fn, mode, buckets[b].numel, W));
+        if (buckets[b].nseg > 0 && !grads) return ddp::fail(DDP_E_INVAL, "%s: grads table is NULL", fn);
+        if (!main_grad && !grads_out && buckets[b].numel > 0)
+            return ddp::fail(DDP_E_INVAL, "%s: main_grad and grads_out are both NULL", fn);
+        if (accumulate && !main_grad && buckets[b].numel > 0)
+            return ddp::fail(DDP_E_INVAL, "%s: accumulate needs main_grad", fn);
+        if (main_grad) {
+            if (bucket_start[b] < 0 || (W > 1 && bucket_start[b] + buckets[b].numel > replica_stride))
+                return ddp::fail(DDP_E_INVAL, "%s: bucket %d [%lld, +%lld) exceeds replica_stride %lld", fn, b,
+                                 static_cast<long long>(bucket_start[b]), static_cast<long long>(buckets[b].numel),
+                                 static_cast<long long>(replica_stride));
+            mgs[b] = main_grad + bucket_start[b];
+        }
+    }
+    return ddp::launch_fused_group(buckets, mgs.data(), nbuckets, grads, used, ld, W, mode, accumulate,
+                                   replica_stride, grads_out, global_used, stream);
 }
 
 extern "C" ddp_status ddp_fused_bucket(const ddp_bucket_desc* bucket, const void* const* grads,

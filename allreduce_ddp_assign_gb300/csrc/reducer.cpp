@@ -67,6 +67,8 @@ struct ddp_reducer {
     std::vector<cudaEvent_t> t_begin, t_end;
     cudaEvent_t done = nullptr;
     bool timing_valid = false;
+    std::vector<ddp_bucket_desc> group_descs;  // scratch for coalesced issue
+    std::vector<float*> group_mgs;
 
     bool dry() const { return flags & DDP_R_DRY_RUN; }
 
@@ -102,22 +104,50 @@ struct ddp_reducer {
         return s;
     }
 
-    ddp_status issue(int32_t b)
+    // Issue the buckets order[pos .. pos+count-1] (all ready) on the side stream:
+    // wait for their producers, then one launch per bucket, or one coalesced launch.
+    ddp_status issue(int32_t pos, int32_t count)
     {
-        log.push_back(b);
+        for (int32_t i = 0; i < count; ++i) log.push_back(order[pos + i]);
         if (dry()) return DDP_OK;
         ddp_status st = DDP_OK;
-        for (size_t i = 0; i < producers[b].size(); ++i)
-            if (!cuda_ok(cudaStreamWaitEvent(side, ready[b][i], 0), "cudaStreamWaitEvent", &st)) return st;
-        if (flags & DDP_R_TIMING)
+        for (int32_t i = 0; i < count; ++i) {
+            const int32_t b = order[pos + i];
+            for (size_t j = 0; j < producers[b].size(); ++j)
+                if (!cuda_ok(cudaStreamWaitEvent(side, ready[b][j], 0), "cudaStreamWaitEvent", &st)) return st;
+        }
+        const bool timing = flags & DDP_R_TIMING;
+        if (count > 1) {
+            if (timing)
+                for (int32_t i = 0; i < count; ++i)
+                    if (!cuda_ok(cudaEventRecord(t_begin[order[pos + i]], side), "cudaEventRecord", &st)) return st;
+            group_descs.clear();
+            group_mgs.clear();
+            for (int32_t i = 0; i < count; ++i) {
+                const int32_t b = order[pos + i];
+                group_descs.push_back(buckets[b]);
+                group_mgs.push_back(mg ? mg + start[b] : nullptr);
+            }
+            st = ddp::launch_fused_group(group_descs.data(), group_mgs.data(), count, grads, used, ld, W, mode,
+                                         accumulate, stride, (flags & DDP_R_COPY_BACK) ? grads_out : nullptr,
+                                         global_used, static_cast<void*>(side));
+            if (st != DDP_OK) return st;
+            if (timing)
+                for (int32_t i = 0; i < count; ++i)
+                    if (!cuda_ok(cudaEventRecord(t_end[order[pos + i]], side), "cudaEventRecord", &st)) return st;
+            return DDP_OK;
+        }
+        const int32_t b = order[pos];
+        if (timing)
             if (!cuda_ok(cudaEventRecord(t_begin[b], side), "cudaEventRecord", &st)) return st;
         st = launch_bucket(b);
         if (st != DDP_OK) return st;
-        if (flags & DDP_R_TIMING)
+        if (timing)
             if (!cuda_ok(cudaEventRecord(t_end[b], side), "cudaEventRecord", &st)) return st;
         return DDP_OK;
     }
 
+    // Record the events that gate bucket b (its gradients' producers).
     ddp_status bucket_ready(int32_t b)
     {
         if (!dry()) {
@@ -131,9 +161,20 @@ struct ddp_reducer {
             for (size_t i = 0; i < producers[b].size(); ++i)
                 if (!cuda_ok(cudaEventRecord(evs[i], producers[b][i]), "cudaEventRecord", &st)) return st;
         }
+        return DDP_OK;
+    }
+
+    // Issue, in order, every bucket from `next` on whose count has reached zero.
+    ddp_status issue_ready()
+    {
+        if (phase != Phase::Backward) return DDP_OK;  // counts are only meaningful inside an iteration
+        const bool coalesce = flags & DDP_R_COALESCE;
         while (next < nbuckets && pending[order[next]] == 0) {
-            const ddp_status st = issue(order[next]);
-            ++next;
+            int32_t count = 1;
+            if (coalesce)
+                while (next + count < nbuckets && pending[order[next + count]] == 0) ++count;
+            const ddp_status st = issue(next, count);
+            next += count;
             if (st != DDP_OK) return st;
         }
         return DDP_OK;
@@ -167,8 +208,10 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
         return fail(DDP_E_INVAL, "%s: a per-bucket array is NULL", fn);
     if (W < 1 || W > ddp::kMaxReplicas) return fail(DDP_E_INVAL, "%s: W = %d outside [1, %d]", fn, W, ddp::kMaxReplicas);
     if (mode != DDP_ALLREDUCE && mode != DDP_REDUCE_SCATTER) return fail(DDP_E_INVAL, "%s: unknown mode %d", fn, mode);
-    if (flags & ~(DDP_R_FUSED | DDP_R_COPY_BACK | DDP_R_TIMING | DDP_R_DRY_RUN))
+    if (flags & ~(DDP_R_FUSED | DDP_R_COPY_BACK | DDP_R_TIMING | DDP_R_DRY_RUN | DDP_R_COALESCE))
         return fail(DDP_E_INVAL, "%s: unknown flag bits 0x%x", fn, flags);
+    if ((flags & DDP_R_COALESCE) && !(flags & DDP_R_FUSED))
+        return fail(DDP_E_INVAL, "%s: DDP_R_COALESCE needs DDP_R_FUSED", fn);
     const bool dry = flags & DDP_R_DRY_RUN;
 
     auto r = new ddp_reducer();
@@ -281,7 +324,10 @@ extern "C" ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate)
     return st == DDP_OK ? ddp::ok() : st;
 }
 
-extern "C" ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* producer_stream)
+namespace {
+
+// Mark one parameter; with defer the issue pass is left to the caller.
+ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool defer)
 {
     if (!r) return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready: reducer is NULL");
     if (param < 0 || param >= r->nparams)
@@ -302,21 +348,31 @@ extern "C" ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void
         if (!have) ps.push_back(s);
     }
     if (--r->pending[b] == 0) {
-        const ddp_status st = r->bucket_ready(b);
+        ddp_status st = r->bucket_ready(b);
+        if (st == DDP_OK && !defer) st = r->issue_ready();
         if (st != DDP_OK) return st;
     }
     return ddp::ok();
+}
+
+}  // namespace
+
+extern "C" ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* producer_stream)
+{
+    return mark_one(r, param, producer_stream, false);
 }
 
 extern "C" ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t* params, int32_t n,
                                                   void* producer_stream)
 {
     if (n < 0 || (n > 0 && !params)) return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready_many: bad list");
-    for (int32_t i = 0; i < n; ++i) {
-        const ddp_status st = ddp_reducer_mark_ready(r, params[i], producer_stream);
-        if (st != DDP_OK) return st;
-    }
-    return ddp::ok();
+    ddp_status st = DDP_OK;
+    for (int32_t i = 0; i < n && st == DDP_OK; ++i) st = mark_one(r, params[i], producer_stream, true);
+    // one issue pass for everything the list completed (coalesced when enabled),
+    // also after a failure so that the parameters already marked are not stranded
+    const ddp_status st2 = r ? r->issue_ready() : DDP_OK;
+    if (st != DDP_OK) return st;
+    return st2 == DDP_OK ? ddp::ok() : st2;
 }
 
 extern "C" ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream, int64_t timeout_us)
@@ -331,8 +387,7 @@ extern "C" ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream
         if (!r->dry()) {
             ddp_status st = DDP_OK;
             if (!cuda_ok(cudaEventRecord(r->done, r->side), "cudaEventRecord", &st)) return st;
-            if (consumer_stream &&
-                !cuda_ok(cudaStreamWaitEvent(static_cast<cudaStream_t>(consumer_stream), r->done, 0),
+            if (!cuda_ok(cudaStreamWaitEvent(static_cast<cudaStream_t>(consumer_stream), r->done, 0),
                          "cudaStreamWaitEvent", &st))
                 return st;
         }

@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, Plan, ddp_pack, ddp_reducer_bucket_ms, ddp_reducer_create,
+from . import (DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, Plan, ddp_pack, ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
                ddp_reducer_mark_ready_many, ddp_reducer_prepare)
 
@@ -25,7 +25,8 @@ class BucketReducer:
     """
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads, used=None,
-                 grads_out=None, fused=True, timing=False, side_stream=None, main_grad=True, grad_reduce_in_fp32=1):
+                 grads_out=None, fused=True, timing=False, side_stream=None, main_grad=True, grad_reduce_in_fp32=1,
+                 coalesce=False):
         import torch
 
         self.W, self.mode = int(W), int(mode)
@@ -41,7 +42,7 @@ class BucketReducer:
         self.global_used_tab = None if gu is None else self.plan.flag_table(gu)
         self.out_tab = None if grads_out is None else self.plan.pointer_table(grads_out)
         flags = (DDP_R_FUSED if fused else 0) | (DDP_R_COPY_BACK if grads_out is not None else 0) | \
-                (DDP_R_TIMING if timing else 0)
+                (DDP_R_TIMING if timing else 0) | (DDP_R_COALESCE if coalesce and fused else 0)
         self.handle = ddp_reducer_create(P, self.plan.bucket_of, self.plan.bucket_order, self.plan.descs,
                                          self.plan.bucket_start, self.W, self.mode, flags, self.grads_tab,
                                          self.used_tab, P, self.main_grad, self.plan.replica_stride, self.out_tab,
@@ -108,7 +109,7 @@ class HostBucketReducer:
     """
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, torch_dtype,
-                 used=None, fused=True, timing=False):
+                 used=None, fused=True, timing=False, coalesce=False):
         import torch
 
         numels = [int(v) for v in numels]
@@ -116,7 +117,7 @@ class HostBucketReducer:
         self.dev_in = torch.empty((W, int(offs[-1])), dtype=torch_dtype, device="cuda")
         grads = [[self.dev_in[w, offs[p]:offs[p + 1]] for p in range(len(numels))] for w in range(W)]
         self.reducer = BucketReducer(numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads,
-                                     used=used, fused=fused, timing=timing)
+                                     used=used, fused=fused, timing=timing, coalesce=coalesce)
 
     @property
     def replica_stride(self) -> int:

@@ -280,8 +280,10 @@ def run_ours(args, wl):
         used[:, wl.unused] = 0
     micro = [[[None if p in wl.unused else WL.grad_torch(wl, p, w, m, dev) for p in range(wl.nparams)]
               for w in range(wl.W)] for m in range(wl.micro_steps)]
+    coalesce = not args.no_coalesce
     sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
-                         wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True, timing=True)
+                         wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True, timing=True,
+                         coalesce=coalesce)
     tabs = [sess.plan.pointer_table(micro[m]) for m in range(wl.micro_steps - 1)]
     compute = torch.cuda.current_stream()
     launches = step_launches(wl, sess.plan)
@@ -318,21 +320,41 @@ def run_ours(args, wl):
     elapsed_ms = ev0.elapsed_time(ev1)
     side_ms = sum(a.elapsed_time(b) for a, b in side_ev)
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
-    per_bucket_ms = sess.bucket_ms()
     value = job_value(world, step_bytes, K, elapsed_ms)
 
-    # the dominant kernel: the per-bucket fused launch on the side stream (the
+    # the same step with one launch per bucket (no coalescing): per-bucket figures
+    pb_sess = sess
+    if coalesce:
+        pb_sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                                wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True, timing=True,
+                                main_grad=True)
+    def pb_step():
+        for m in range(wl.micro_steps - 1):
+            pb_sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
+        pb_sess.backward(compute, accumulate=wl.micro_steps > 1)
+        pb_sess.finalize(compute)
+    for _ in range(3):
+        pb_step()
+    torch.cuda.synchronize()
+    Kp = max(3, min(K, 50))
+    pa, pb_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pa.record(compute)
+    for _ in range(Kp):
+        pb_step()
+    pb_ev.record(compute)
+    torch.cuda.synchronize()
+    pb_value = job_value(1, step_bytes, Kp, pa.elapsed_time(pb_ev))
+    per_bucket_ms = [float(x) for x in pb_sess.bucket_ms()]
+    if pb_sess is not sess:
+        pb_sess.close()
+
+    # the dominant kernel: the fused pack+reduce launch(es) on the side stream (the
     # no_sync packs of an accumulating workload run on the compute stream)
     fused = [x for x in launches if x[0].startswith("fused")]
     fused_bytes = sum(x[2] for x in fused)
-    if wl.micro_steps > 1:
-        kern_ms = float(sum(per_bucket_ms))  # last step's fused launches (the packs are not on the side stream)
-        achieved = fused_bytes / (kern_ms * 1e-3) / 1e9
-        timing_src = "reducer events around each fused launch, last timed step"
-    else:
-        kern_ms = side_ms / K
-        achieved = fused_bytes / (kern_ms * 1e-3) / 1e9
-        timing_src = "CUDA events on the side stream around each step's launches, timed region"
+    kern_ms = side_ms / K
+    achieved = fused_bytes / (kern_ms * 1e-3) / 1e9
+    timing_src = "CUDA events on the side stream around each timed step's fused launches"
     tag = f"fused_{wl.name}"
     traffic = profile_traffic(tag)
 
@@ -341,7 +363,7 @@ def run_ours(args, wl):
     if not args.no_e2e and wl.micro_steps == 1:
         tdt = torch.float32 if wl.dtype == WL.F32 else torch.bfloat16
         host = HostBucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
-                                 wl.first_cap_bytes, wl.pad_multiple, tdt, used=used)
+                                 wl.first_cap_bytes, wl.pad_multiple, tdt, used=used, coalesce=coalesce)
         total = sum(wl.numels)
         h_in = torch.empty((wl.W, total), dtype=tdt, pin_memory=True)
         for w in range(wl.W):
@@ -384,15 +406,18 @@ def run_ours(args, wl):
                        "buckets": sess.plan.nbuckets, "params": wl.nparams, "elements": sum(wl.numels),
                        "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (no flush)",
                        "parallelism": f"replicas x{world}", "pct_of_nominal_8TBs": round(100 * value / NOMINAL_HBM_GBS, 2),
-                       "buckets_per_s": round(world * K * sess.plan.nbuckets / (elapsed_ms * 1e-3), 1)},
+                       "buckets_per_s": round(world * K * sess.plan.nbuckets / (elapsed_ms * 1e-3), 1),
+                       "issue": "coalesced (ready buckets in one launch)" if coalesce else "one launch per bucket",
+                       "per_bucket_issue": {"value": round(pb_value, 1), "unit": "GB/s", "steps": Kp,
+                                            "per_bucket_gbs": [round(x[2] / (per_bucket_ms[x[1]] * 1e-3) / 1e9, 1)
+                                                               if per_bucket_ms[x[1]] > 0 else None for x in fused],
+                                            "bucket_bytes": [int(x[2]) for x in fused]}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                         "kernel": tag, "timing": timing_src,
-                         "per_bucket_gbs": [round(x[2] / (per_bucket_ms[x[1]] * 1e-3) / 1e9, 1) if per_bucket_ms[x[1]] > 0
-                                            else None for x in fused]},
+                         "kernel": tag, "timing": timing_src},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": len(launches) * K,
+            "gpu_launches": (len(launches) - len(fused) + (-(-len(fused) // 32) if coalesce else len(fused))) * K,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -430,6 +455,51 @@ def _cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+def run_sweep(args):
+    """Bandwidth sweep (one fp32 bucket, S = 1 KiB * 4^k up to 1 GiB, W in {2, 4, 8, 16},
+    allreduce mean): ddp_bucket_allreduce timed alone with CUDA events, L2 flushed
+    before every rep by writing a buffer twice the L2 size; median of the reps.
+    Prints one JSON line per point."""
+    import torch
+
+    import allreduce_ddp_assign_gb300 as D
+
+    dev = torch.device("cuda", 0)
+    D.lib()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+    points = WL.c5_sweep_points()
+    if args.sweep_max_bytes:
+        points = [(b, w) for b, w in points if b <= args.sweep_max_bytes]
+    for nbytes, W in points:
+        n = nbytes // 4
+        x = WL.bucket_torch(nbytes, W, dev)
+        reps = 20 if nbytes * W < (256 << 20) else 5
+        times = []
+        for r in range(reps + 3):
+            flush.fill_(float(r))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            D.ddp_bucket_allreduce(x, n, n, W, D.DDP_ALLREDUCE)
+            b.record()
+            b.synchronize()
+            if r >= 3:
+                times.append(a.elapsed_time(b))
+        ms = float(np.median(times))
+        moved = 2 * W * nbytes
+        gbs = moved / (ms * 1e-3) / 1e9
+        print(json.dumps({"sweep": True, "bucket_bytes": nbytes, "W": W, "us": round(ms * 1e3, 2),
+                          "GBps": round(gbs, 1), "frac_measured": round(gbs / peak, 4),
+                          "pct_of_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                          "buckets_per_s": round(1e3 / ms, 1), "bytes_moved": moved,
+                          "l2_resident": moved < l2, "reps": reps}), flush=True)
+        del x
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,8 +509,13 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-coalesce", action="store_true", help="one launch per bucket in the timed steps")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true", help="bandwidth sweep of ddp_bucket_allreduce (JSON per point)")
+    ap.add_argument("--sweep-max-bytes", type=int, default=0)
     args = ap.parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, wl)

@@ -281,6 +281,26 @@ ddp_status ddp_fused_bucket(const ddp_bucket_desc* bucket, const void* const* gr
                             int32_t accumulate, float* main_grad, int64_t replica_stride,
                             void* const* grads_out, const uint8_t* global_used, void* stream);
 
+/*
+ * ddp_fused_bucket_group -- ddp_fused_bucket over several buckets in as few
+ * kernel launches as possible (one per run of up to 32 buckets of one dtype):
+ * the collectives of a bucket group coalesced into one call (Megatron page,
+ * section 3, _coalescing_manager).  Results are those of calling
+ * ddp_fused_bucket on each bucket in turn.
+ *
+ *   buckets[nbuckets]       HOST descriptors.
+ *   bucket_start[nbuckets]  HOST: bucket b occupies main_grad + bucket_start[b]
+ *                           in every replica (ignored when main_grad is NULL).
+ *   other arguments         as ddp_fused_bucket; main_grad is the start of the
+ *                           per-replica buffer holding all the buckets.
+ * Errors: as ddp_fused_bucket, for any bucket; DDP_E_INVAL if a bucket does
+ * not fit in replica_stride.  Nothing is launched when a bucket is rejected.
+ */
+ddp_status ddp_fused_bucket_group(const ddp_bucket_desc* buckets, const int64_t* bucket_start, int32_t nbuckets,
+                                  const void* const* grads, const uint8_t* used, int32_t ld, int32_t W,
+                                  int32_t mode, int32_t accumulate, float* main_grad, int64_t replica_stride,
+                                  void* const* grads_out, const uint8_t* global_used, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Step 5: the reducer -- in-order bucket issue on a side stream             */
 /* ------------------------------------------------------------------------ */
@@ -300,7 +320,9 @@ enum {
     DDP_R_FUSED = 1,     /* issue ddp_fused_bucket per bucket (else pack + allreduce [+ unpack]) */
     DDP_R_COPY_BACK = 2, /* write reduced gradients to grads_out (else main_grad views only) */
     DDP_R_TIMING = 4,    /* record CUDA events around each bucket's kernels (ddp_reducer_bucket_ms) */
-    DDP_R_DRY_RUN = 8    /* schedule only: no CUDA call at all; issues are logged, not launched */
+    DDP_R_DRY_RUN = 8,   /* schedule only: no CUDA call at all; issues are logged, not launched */
+    DDP_R_COALESCE = 16  /* buckets that become issuable together go out in one launch
+                            (ddp_fused_bucket_group); needs DDP_R_FUSED */
 };
 
 /*
@@ -354,15 +376,18 @@ ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* producer_
 /*
  * ddp_reducer_mark_ready_many -- ddp_reducer_mark_ready for params[0..n-1], in
  * that order, all produced on producer_stream (one backward layer's weight and
- * bias, or a whole backward pass, in one call).  HOST params[n].  Stops at the
- * first failing parameter and returns its status; the earlier ones stay marked.
+ * bias, or a whole backward pass, in one call).  HOST params[n].  The buckets
+ * the list completes are issued after the whole list is marked, in issue order
+ * (with DDP_R_COALESCE, consecutive ones in one launch).  Stops marking at the
+ * first failing parameter and returns its status; the earlier ones stay marked
+ * and their complete buckets are still issued.
  */
 ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t* params, int32_t n, void* producer_stream);
 
 /*
  * ddp_reducer_finalize -- end of backward (finalize_backward, DDP chapter
- * 17.41; Megatron finish_grad_sync): makes consumer_stream (may be NULL: none)
- * wait for every issued reduction.  With timeout_us > 0 it also waits on the
+ * 17.41; Megatron finish_grad_sync): makes consumer_stream (NULL: the legacy
+ * default stream) wait for every issued reduction.  With timeout_us > 0 it also waits on the
  * host, polling, until the reductions finish or the deadline passes.
  * Errors: DDP_E_INCOMPLETE if some bucket was never issued (message lists the
  * unmarked parameters); DDP_E_TIMEOUT if the deadline passed (the work stays
@@ -376,10 +401,37 @@ ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, int32_t cap
 /*
  * Per-bucket GPU time in milliseconds of the last finalized iteration (needs
  * DDP_R_TIMING; waits for those events).  HOST out[cap], indexed by bucket id.
+ * Buckets issued together in one coalesced launch each report that launch's time.
  */
 ddp_status ddp_reducer_bucket_ms(ddp_reducer* r, float* out, int32_t cap);
 
 void ddp_reducer_destroy(ddp_reducer* r);
+
+/* ------------------------------------------------------------------------ */
+/* Kernel variants and device status                                         */
+/* ------------------------------------------------------------------------ */
+/*
+ * Two implementations compute every data-path call with identical results:
+ *   DDP_KERNEL_AUTO   (default) ddp_bucket_allreduce and ddp_fused_bucket use
+ *                     the TMA-pipelined streaming kernel where its shared-memory
+ *                     stage ring fits (2 <= W <= 16, vector-aligned main_grad
+ *                     for the allreduce); everything else uses the plain kernel.
+ *   DDP_KERNEL_PLAIN  every call uses the plain kernel (16-byte loads straight
+ *                     into registers).
+ * The choice is process-wide and applies to calls made after it.
+ * Errors: DDP_E_INVAL for an unknown variant.
+ */
+enum { DDP_KERNEL_AUTO = 0, DDP_KERNEL_PLAIN = 1 };
+ddp_status ddp_set_kernel_variant(int32_t variant);
+
+/*
+ * ddp_device_status -- the library's device status word: 0 normally; bit 0
+ * set if a streaming kernel gave up on an mbarrier wait (about 2 s), recorded
+ * the failure and returned early, leaving its outputs incomplete.  Reads the
+ * word on `stream` (synchronising that stream); reset != 0 clears it.
+ * HOST out: *status.  Errors: DDP_E_INVAL (NULL status); DDP_E_CUDA.
+ */
+ddp_status ddp_device_status(void* stream, int32_t* status, int32_t reset);
 
 /* ------------------------------------------------------------------------ */
 /* Errors and version                                                        */

@@ -21,6 +21,16 @@ if not torch.cuda.is_available():  # pragma: no cover
 DEV = torch.device("cuda:0")
 
 
+@pytest.fixture(params=[D.DDP_KERNEL_AUTO, D.DDP_KERNEL_PLAIN], ids=["auto", "plain"])
+def variant(request):
+    """Both implementations (the TMA-pipelined streaming kernel where it applies,
+    and the plain 16-byte-load kernel) must match the oracle."""
+    D.ddp_set_kernel_variant(request.param)
+    yield request.param
+    D.ddp_set_kernel_variant(D.DDP_KERNEL_AUTO)
+    assert D.ddp_device_status(reset=True) == 0
+
+
 def guarded(n_elems: int, offset: int = 0):
     """A device fp32 buffer of n_elems (+offset) elements with sentinel guard bands."""
     buf = torch.full((GUARD + offset + n_elems + GUARD,), float(SENTINEL), dtype=torch.float32, device=DEV)
@@ -41,7 +51,7 @@ ALLREDUCE_CASES = [(W, n) for W in (1, 2, 3, 4, 5, 8, 16, 64) for n in (0, 1, 3,
 
 @pytest.mark.parametrize("layout", ["tight", "stride_pad", "misaligned"])
 @pytest.mark.parametrize("W,n", ALLREDUCE_CASES)
-def test_allreduce_vs_oracle(orc, W, n, layout):
+def test_allreduce_vs_oracle(orc, W, n, layout, variant):
     rng = np.random.default_rng(1000 * W + n)
     for mode in (D.DDP_ALLREDUCE, D.DDP_REDUCE_SCATTER):
         nn = n - n % W if mode == D.DDP_REDUCE_SCATTER else n
@@ -140,7 +150,7 @@ SEG_CASES = [(W, dt, mis) for W in (1, 2, 3, 4, 8, 16) for dt in (D.DDP_F32, D.D
 
 
 @pytest.mark.parametrize("W,dtype,misalign", SEG_CASES)
-def test_staged_pack_reduce_unpack(orc, W, dtype, misalign):
+def test_staged_pack_reduce_unpack(orc, W, dtype, misalign, variant):
     rng = np.random.default_rng(W * 31 + dtype * 7 + misalign)
     for trial in range(3):
         bk = random_bucket(rng, W, dtype, int(rng.integers(0, 9)), misalign)
@@ -173,7 +183,7 @@ def test_staged_pack_reduce_unpack(orc, W, dtype, misalign):
 
 
 @pytest.mark.parametrize("W,dtype,misalign", SEG_CASES)
-def test_fused_matches_staged_oracle(orc, W, dtype, misalign):
+def test_fused_matches_staged_oracle(orc, W, dtype, misalign, variant):
     rng = np.random.default_rng(W * 131 + dtype * 17 + misalign)
     for trial in range(4):
         bk = random_bucket(rng, W, dtype, int(rng.integers(0, 9)), misalign)
@@ -213,7 +223,7 @@ def test_fused_matches_staged_oracle(orc, W, dtype, misalign):
         check_guards(buf, start, W * stride)
 
 
-def test_fused_in_place_without_main_grad(orc):
+def test_fused_in_place_without_main_grad(orc, variant):
     """grads_out aliasing fp32 grads, no bucket buffer: DDP without
     gradient_as_bucket_view, reduced straight back into .grad."""
     rng = np.random.default_rng(5)
@@ -256,7 +266,7 @@ def make_session(wl, grads, fused=True, grads_out=None, timing=False):
 
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("name", ["c1", "c2"])
-def test_workload_full_vs_oracle(orc, name, fused):
+def test_workload_full_vs_oracle(orc, name, fused, variant):
     wl = WL.ALL[name]()
     sess = make_session(wl, device_grads(wl), fused=fused)
     sess.step()
@@ -442,4 +452,122 @@ def test_reducer_finalize_timeout_then_recovers(orc):
     torch.cuda.synchronize()
     ref = O.run_workload(wl, orc, copy_back=False)
     assert_bits_equal(sess.plan.bucket_view(sess.main_grad, 0).cpu().numpy(), ref["bucket"][0])
+    sess.close()
+
+
+def test_finalize_orders_the_default_stream(orc):
+    """finalize(consumer = the legacy default stream) must make that stream wait
+    for the side stream: a copy taken on it right after finalize sees the result
+    even though the side stream was held back first."""
+    wl = WL.c1_mlp()
+    sess = make_session(wl, device_grads(wl))
+    sess.main_grad.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(sess.side):
+        torch.cuda._sleep(100_000_000)   # bounded spin, ~50 ms
+    assert torch.cuda.current_stream().cuda_stream == 0   # the legacy default stream
+    sess.step()                                          # producer and consumer: the current stream
+    snap = sess.main_grad.clone()                        # queued on the default stream
+    torch.cuda.synchronize()
+    ref = O.run_workload(wl, orc, copy_back=False)
+    got = sess.plan.bucket_view(snap, 0).cpu().numpy()
+    assert_bits_equal(got, ref["bucket"][0], "default-stream snapshot")
+    sess.close()
+
+
+def test_device_status_clean():
+    assert D.ddp_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 8, 16])
+def test_fused_bucket_group_vs_oracle(orc, W, variant):
+    """Several buckets (mixed dtypes, so the group splits into runs) in one call:
+    every bucket equals the oracle's pack + ring (+ unpack)."""
+    rng = np.random.default_rng(900 + W)
+    for trial in range(3):
+        mode = D.DDP_REDUCE_SCATTER if trial == 1 else D.DDP_ALLREDUCE
+        accumulate = trial == 2
+        dts = [int(d) for d in rng.choice([D.DDP_F32, D.DDP_F32, D.DDP_BF16, D.DDP_F16], size=5)]
+        bks = [random_bucket(rng, W, dt, int(rng.integers(1, 7)), bool(rng.integers(0, 2))) for dt in dts]
+        for bk in bks:   # reduce_scatter needs numel % W == 0: pad the buckets
+            bk["numel"] += (-bk["numel"]) % W
+            bk["desc"].numel = bk["numel"]
+        starts, pos = [], 0
+        for bk in bks:
+            starts.append(pos)
+            pos += (bk["numel"] + 63) // 64 * 64
+        stride = max(pos, 64)
+        # one table for all buckets: bucket i's segment s is parameter cols[i] + s
+        cols = np.cumsum([0] + [bk["nseg"] for bk in bks])
+        ld = int(cols[-1])
+        ptrs = np.zeros(W * ld, np.int64)
+        usedf = np.zeros((W, ld), np.uint8)
+        for i, bk in enumerate(bks):
+            t = bk["tab"].cpu().numpy().reshape(W, bk["nseg"])
+            ptrs.reshape(W, ld)[:, cols[i]:cols[i + 1]] = t
+            usedf[:, cols[i]:cols[i + 1]] = bk["used"]
+            par = torch.arange(cols[i], cols[i + 1], dtype=torch.int32, device=DEV)
+            bk["keep"].append(par)
+            bk["desc"].seg_param = par.data_ptr()
+        tab = torch.from_numpy(ptrs).to(DEV)
+        used_t = torch.from_numpy(usedf.reshape(-1).copy()).to(DEV)
+        gu = usedf.max(axis=0)
+        gu_t = torch.from_numpy(gu.copy()).to(DEV)
+        init = rng.standard_normal((W, stride)).astype(np.float32)
+        mg = torch.from_numpy(init.copy()).to(DEV)
+        outs = [[torch.full((max(n, 1),), 2.0, device=DEV) for bk in bks for n in bk["sizes"]] for _ in range(W)]
+        out_tab = torch.from_numpy(np.array([o.data_ptr() for w in range(W) for o in outs[w]], np.int64)).to(DEV)
+        D.ddp_fused_bucket_group([bk["desc"] for bk in bks], starts, tab, used_t, ld, W, mode, int(accumulate), mg,
+                                 stride, out_tab, gu_t)
+        got = mg.cpu().numpy()
+        for i, bk in enumerate(bks):
+            n, s0 = bk["numel"], starts[i]
+            packed = oracle_pack(orc, bk, W, dts[i], accumulate, init[:, s0:s0 + n].copy())
+            want, _ = orc.ring(packed.copy(), mode)
+            g = got[:, s0:s0 + n]
+            if mode == D.DDP_ALLREDUCE:
+                assert_bits_equal(g, want, f"bucket {i}")
+            else:
+                k = n // W
+                for w in range(W):
+                    assert_bits_equal(g[w, w * k:(w + 1) * k], want[w, w * k:(w + 1) * k], f"bucket {i} shard {w}")
+            exp = orc.unpack(want.copy(), bk["offs"][:-1], bk["sizes"], mode, gu[cols[i]:cols[i + 1]],
+                             outs=[[np.full(s, 2.0, np.float32) for s in bk["sizes"]] for _ in range(W)])
+            for w in range(W):
+                for s in range(bk["nseg"]):
+                    o = outs[w][cols[i] + s][:bk["sizes"][s]].cpu().numpy()
+                    assert_bits_equal(o, exp[w][s], f"copy-back bucket {i} w={w} s={s}")
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+def test_coalesced_reducer_vs_oracle(orc, name):
+    """The reducer issuing every ready bucket in one launch gives the same bits."""
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    wl = WL.ALL[name]()
+    sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                         wl.first_cap_bytes, wl.pad_multiple, device_grads(wl), coalesce=True, timing=True)
+    if wl.mode == D.DDP_REDUCE_SCATTER:
+        sess.main_grad.fill_(float(SENTINEL))
+    sess.step()
+    torch.cuda.synchronize()
+    assert sess.issue_log() == [int(b) for b in sess.plan.bucket_order]
+    assert np.all(sess.bucket_ms() > 0)
+    rng = np.random.default_rng(5)
+    for b in range(sess.plan.nbuckets):
+        got = sess.plan.bucket_view(sess.main_grad, b).cpu().numpy()
+        n = int(sess.plan.bucket_numel[b])
+        if name != "c3":
+            ref = O.run_workload(wl, orc, copy_back=False) if b == 0 else ref
+            assert_bits_equal(got, ref["bucket"][b], f"{name} bucket {b}")
+        else:
+            e = _sample(rng, n, 400)
+            owner = chunk_of(e, n, wl.W)
+            t = np.zeros((wl.W, len(e)), np.float32)
+            for p in sess.plan.members[b]:
+                lo, hi = int(sess.plan.offset_of[p]), int(sess.plan.offset_of[p]) + wl.numels[p]
+                sel = np.nonzero((e >= lo) & (e < hi))[0]
+                if len(sel):
+                    t[:, sel] = packed_at(orc, wl, p, e[sel] - lo, 1)
+            assert_bits_equal(got[owner, e], oracle_at(orc, t, owner), f"c3 bucket {b}")
     sess.close()

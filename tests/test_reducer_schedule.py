@@ -108,6 +108,8 @@ def test_create_validation():
                              replica_stride=8)
     with pytest.raises(D.DdpError):    # bucket past the replica stride
         D.ddp_reducer_create(1, [0], [0], descs, [4], 2, 0, D.DDP_R_DRY_RUN, replica_stride=8)
+    with pytest.raises(D.DdpError):    # coalescing is a property of the fused issue
+        D.ddp_reducer_create(1, [0], [0], descs, [0], 2, 0, D.DDP_R_DRY_RUN | D.DDP_R_COALESCE, replica_stride=8)
 
 
 def test_repeated_iterations_and_timing_refused_in_dry_run():
@@ -121,4 +123,45 @@ def test_repeated_iterations_and_timing_refused_in_dry_run():
     with pytest.raises(D.DdpError) as e:
         D.ddp_reducer_bucket_ms(r, 2)
     assert e.value.status == D.DDP_E_STATE
+    D.ddp_reducer_destroy(r)
+
+
+def test_coalesced_issue_order_dry_run():
+    """Coalescing changes how many launches go out, not the order of buckets."""
+    nb = 4
+    descs = [D.BucketDesc(8, 0, 0, None, None) for _ in range(nb)]
+    r = D.ddp_reducer_create(4, [0, 1, 2, 3], [0, 1, 2, 3], descs, [0] * nb, 2, D.DDP_ALLREDUCE,
+                             D.DDP_R_DRY_RUN | D.DDP_R_FUSED | D.DDP_R_COALESCE, replica_stride=8)
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready_many(r, [3, 2, 1])
+    assert D.ddp_reducer_issue_log(r) == []
+    D.ddp_reducer_mark_ready(r, 0)
+    assert D.ddp_reducer_issue_log(r) == [0, 1, 2, 3]
+    D.ddp_reducer_finalize(r)
+    D.ddp_reducer_destroy(r)
+
+
+def test_mark_many_outside_iteration_issues_nothing():
+    r = make([0, 1])
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_mark_ready_many(r, [1, 0])
+    assert e.value.status == D.DDP_E_STATE
+    assert D.ddp_reducer_issue_log(r) == []
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready_many(r, [1, 0])
+    assert D.ddp_reducer_issue_log(r) == [0, 1]
+    D.ddp_reducer_finalize(r)
+    D.ddp_reducer_destroy(r)
+
+
+def test_mark_many_stops_at_the_duplicate_but_issues_completed_buckets():
+    r = make([0, 1, 1])
+    D.ddp_reducer_prepare(r)
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_mark_ready_many(r, [0, 0, 1])
+    assert e.value.status == D.DDP_E_STATE
+    assert D.ddp_reducer_issue_log(r) == [0]      # bucket 0 was complete before the duplicate
+    D.ddp_reducer_mark_ready_many(r, [1, 2])
+    assert D.ddp_reducer_issue_log(r) == [0, 1]
+    D.ddp_reducer_finalize(r)
     D.ddp_reducer_destroy(r)
