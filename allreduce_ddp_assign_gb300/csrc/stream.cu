@@ -653,7 +653,9 @@ ddp_status launch_instance(StreamArgs& a, void* stream)
         occ = v;
         occ_bytes = p.bytes;
     }
-    const int64_t want = (a.total + 4 * tile - 1) / (4 * tile);
+    // small launches: spread down to 16-element slices so that the pieces (one per ring
+    // chunk, at least) run in parallel CTAs rather than through one CTA's pipeline
+    const int64_t want = (a.total + 15) / 16;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sm_count_tma()) * occ)));
     kern<<<grid, kThreadsTma, p.bytes, static_cast<cudaStream_t>(stream)>>>(a);
     const cudaError_t err = cudaGetLastError();

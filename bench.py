@@ -233,18 +233,28 @@ def run_reference(args, wl):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def profile_traffic(kernel_tag: str):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary,
-    if it was captured on the current kernel source."""
+KERNEL_SOURCES = ("kernels.cu", "stream.cu", "device_common.cuh", "common.h")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the device sources, to tell whether a committed ncu figure is current."""
     import hashlib
 
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "allreduce_ddp_assign_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
+def profile_traffic(kernel_tag: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/traffic.json), or None if it was taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
         rec = json.load(open(path)).get(kernel_tag)
-        src = open(os.path.join(ROOT, "allreduce_ddp_assign_gb300", "csrc", "kernels.cu"), "rb").read()
-        if rec and rec.get("kernels_cu_sha256") == hashlib.sha256(src).hexdigest():
+        if rec and rec.get("kernel_sources_sha256") == kernel_source_hash():
             return rec.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         return None
@@ -282,16 +292,25 @@ def run_ours(args, wl):
               for w in range(wl.W)] for m in range(wl.micro_steps)]
     coalesce = not args.no_coalesce
     sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
-                         wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True, timing=True,
-                         coalesce=coalesce)
+                         wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True,
+                         timing=not coalesce, coalesce=coalesce)
     tabs = [sess.plan.pointer_table(micro[m]) for m in range(wl.micro_steps - 1)]
     compute = torch.cuda.current_stream()
     launches = step_launches(wl, sess.plan)
     step_bytes = sum(x[2] for x in launches)
 
-    def step():
-        for m in range(wl.micro_steps - 1):   # no_sync micro-steps: local accumulation on the compute stream
-            sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
+    pack_ev = []
+
+    def step(timed=False):
+        if wl.micro_steps > 1:
+            if timed:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(compute)
+            for m in range(wl.micro_steps - 1):   # no_sync micro-steps: local accumulation on the compute stream
+                sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
+            if timed:
+                ev[1].record(compute)
+                pack_ev.append(ev)
         sess.backward(compute, accumulate=wl.micro_steps > 1)
         sess.finalize(compute)
 
@@ -310,7 +329,7 @@ def run_ours(args, wl):
         ev0.record(compute)
         for k in range(K):
             side_ev[k][0].record(sess.side)
-            step()
+            step(timed=True)
             side_ev[k][1].record(sess.side)
         ev1.record(compute)
         torch.cuda.synchronize()
@@ -352,11 +371,47 @@ def run_ours(args, wl):
     # no_sync packs of an accumulating workload run on the compute stream)
     fused = [x for x in launches if x[0].startswith("fused")]
     fused_bytes = sum(x[2] for x in fused)
-    kern_ms = side_ms / K
-    achieved = fused_bytes / (kern_ms * 1e-3) / 1e9
-    timing_src = "CUDA events on the side stream around each timed step's fused launches"
-    tag = f"fused_{wl.name}"
+    packs = [x for x in launches if x[0].startswith("pack")]
+    pack_bytes = sum(x[2] for x in packs)
+    if packs:
+        # the side stream's span also holds the wait for the packs: split the step
+        pack_ms = sum(a.elapsed_time(b) for a, b in pack_ev) / K
+        fused_ms = max(side_ms / K - pack_ms, 1e-6)
+    else:
+        pack_ms, fused_ms = 0.0, side_ms / K
+    if pack_ms > fused_ms:   # no_sync workloads: the local accumulation dominates
+        dominant, dom_bytes, kern_ms = "pack", pack_bytes, pack_ms
+        timing_src = "CUDA events on the compute stream around each timed step's no_sync pack launches"
+    else:
+        dominant, dom_bytes, kern_ms = "fused", fused_bytes, fused_ms
+        timing_src = ("CUDA events on the side stream around each timed step's fused launches"
+                      + (" (minus the packs it waits for)" if packs else ""))
+    achieved = dom_bytes / (kern_ms * 1e-3) / 1e9
+    tag = f"{dominant}_{wl.name}"
     traffic = profile_traffic(tag)
+
+    # context: the same fused launches back to back on the side stream, without
+    # the reducer's cross-stream hand-offs (kernel time alone)
+    kernel_only = None
+    if wl.micro_steps == 1:
+        import allreduce_ddp_assign_gb300 as D2
+
+        plan = sess.plan
+        order = [int(b) for b in plan.bucket_order]
+        descs = [plan.descs[b] for b in order]
+        starts = [int(plan.bucket_start[b]) for b in order]
+        ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(sess.side):
+            for r in range(Kp + 3):
+                if r == 3:
+                    ka.record(sess.side)
+                D2.ddp_fused_bucket_group(descs, starts, sess.grads_tab, sess.used_tab, wl.nparams, wl.W, wl.mode, 0,
+                                          sess.main_grad, plan.replica_stride, None, None, sess.side)
+            kb.record(sess.side)
+        torch.cuda.synchronize()
+        kms = ka.elapsed_time(kb) / Kp
+        kernel_only = {"value": round(fused_bytes / (kms * 1e-3) / 1e9, 1), "unit": "GB/s", "us_per_step": round(kms * 1e3, 1),
+                       "frac_of_measured_peak": round(fused_bytes / (kms * 1e-3) / 1e9 / peak, 4)}
 
     # end to end: pinned host buffers in, reduced main_grad out, through the public API
     e2e = None
@@ -414,7 +469,8 @@ def run_ours(args, wl):
                                             "bucket_bytes": [int(x[2]) for x in fused]}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                         "kernel": tag, "timing": timing_src},
+                         "kernel": tag, "timing": timing_src, "kernel_only": kernel_only,
+                         "step_split_ms": {"pack": round(pack_ms, 4), "fused": round(fused_ms, 4)} if packs else None},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": (len(launches) - len(fused) + (-(-len(fused) // 32) if coalesce else len(fused))) * K,
@@ -477,25 +533,49 @@ def run_sweep(args):
     for nbytes, W in points:
         n = nbytes // 4
         x = WL.bucket_torch(nbytes, W, dev)
-        reps = 20 if nbytes * W < (256 << 20) else 5
-        times = []
-        for r in range(reps + 3):
-            flush.fill_(float(r))
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            D.ddp_bucket_allreduce(x, n, n, W, D.DDP_ALLREDUCE)
-            b.record()
-            b.synchronize()
-            if r >= 3:
-                times.append(a.elapsed_time(b))
-        ms = float(np.median(times))
         moved = 2 * W * nbytes
+        if moved < (256 << 20):
+            # launch-latency regime: replay 20 launches from a CUDA graph and take
+            # the GPU time per launch (the data then sit in L2: labelled so)
+            s = torch.cuda.Stream()
+            D.ddp_bucket_allreduce(x, n, n, W, D.DDP_ALLREDUCE, s)   # first call outside capture
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(20):
+                    D.ddp_bucket_allreduce(x, n, n, W, D.DDP_ALLREDUCE, torch.cuda.current_stream())
+            g.replay()
+            torch.cuda.synchronize()
+            times = []
+            for r in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                b.synchronize()
+                times.append(a.elapsed_time(b) / 20)
+            reps, timing = 100, "graph replay, 20 launches x 5, L2-resident"
+            del g
+        else:
+            reps = 5
+            times = []
+            for r in range(reps + 3):
+                flush.fill_(float(r))
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                D.ddp_bucket_allreduce(x, n, n, W, D.DDP_ALLREDUCE)
+                b.record()
+                b.synchronize()
+                if r >= 3:
+                    times.append(a.elapsed_time(b))
+            timing = "one launch per rep, L2 flushed before each"
+        ms = float(np.median(times))
         gbs = moved / (ms * 1e-3) / 1e9
         print(json.dumps({"sweep": True, "bucket_bytes": nbytes, "W": W, "us": round(ms * 1e3, 2),
                           "GBps": round(gbs, 1), "frac_measured": round(gbs / peak, 4),
                           "pct_of_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
                           "buckets_per_s": round(1e3 / ms, 1), "bytes_moved": moved,
-                          "l2_resident": moved < l2, "reps": reps}), flush=True)
+                          "l2_resident": moved < l2, "reps": reps, "timing": timing}), flush=True)
         del x
         torch.cuda.empty_cache()
 
