@@ -24,6 +24,7 @@ DDP_F32, DDP_BF16, DDP_F16 = 0, 1, 2
 DDP_ORDER_REVERSE, DDP_ORDER_FWD_THEN_REVERSE, DDP_ORDER_MEGATRON = 0, 1, 2
 DDP_ALLREDUCE, DDP_REDUCE_SCATTER = 0, 1
 DDP_R_FUSED, DDP_R_COPY_BACK, DDP_R_TIMING, DDP_R_DRY_RUN, DDP_R_COALESCE = 1, 2, 4, 8, 16
+DDP_R_WIRE_BF16, DDP_R_WIRE_F16 = 32, 64
 DDP_KERNEL_AUTO, DDP_KERNEL_PLAIN = 0, 1
 
 
@@ -50,10 +51,16 @@ _SIGS = {
                                        _i32p]),
     "ddp_pack": (C.c_int32, [C.POINTER(BucketDesc), _vp, _vp, C.c_int32, C.c_int32, _vp, C.c_int64, C.c_int32, _vp]),
     "ddp_bucket_allreduce": (C.c_int32, [_vp, C.c_int64, C.c_int64, C.c_int32, C.c_int32, _vp]),
+    "ddp_bucket_allreduce_wire": (C.c_int32, [_vp, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int32, _vp]),
+    "ddp_fused_bucket_group_wire": (C.c_int32, [C.POINTER(BucketDesc), _i64p, C.c_int32, _vp, _vp, C.c_int32,
+                                                C.c_int32, C.c_int32, C.c_int32, _vp, C.c_int64, _vp, _vp, C.c_int32,
+                                                _vp]),
     "ddp_unpack": (C.c_int32, [C.POINTER(BucketDesc), _vp, C.c_int64, C.c_int32, C.c_int32, _vp, C.c_int32, _vp,
                                _vp]),
     "ddp_fused_bucket": (C.c_int32, [C.POINTER(BucketDesc), _vp, _vp, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
                                      _vp, C.c_int64, _vp, _vp, _vp]),
+    "ddp_pack_group": (C.c_int32, [C.POINTER(BucketDesc), _i64p, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, _vp,
+                                   C.c_int64, C.c_int32, _vp]),
     "ddp_fused_bucket_group": (C.c_int32, [C.POINTER(BucketDesc), _i64p, C.c_int32, _vp, _vp, C.c_int32, C.c_int32,
                                            C.c_int32, C.c_int32, _vp, C.c_int64, _vp, _vp, _vp]),
     "ddp_reducer_create": (C.c_int32, [C.c_int32, C.c_int32, _i32p, _i32p, C.POINTER(BucketDesc), _i64p, C.c_int32,
@@ -182,6 +189,12 @@ def ddp_bucket_allreduce(replicas, replica_stride, numel, W, mode=DDP_ALLREDUCE,
                                       _stream(stream)))
 
 
+def ddp_bucket_allreduce_wire(replicas, replica_stride, numel, W, mode=DDP_ALLREDUCE, wire_dtype=DDP_BF16,
+                              stream=None) -> None:
+    _check(lib().ddp_bucket_allreduce_wire(_ptr(replicas), int(replica_stride), int(numel), int(W), int(mode),
+                                           int(wire_dtype), _stream(stream)))
+
+
 def ddp_unpack(desc: BucketDesc, main_grad, replica_stride, W, mode, grads_out, ld, global_used=None,
                stream=None) -> None:
     _check(lib().ddp_unpack(C.byref(desc), _ptr(main_grad), int(replica_stride), int(W), int(mode),
@@ -195,6 +208,15 @@ def ddp_fused_bucket(desc: BucketDesc, grads, used, ld, W, mode, accumulate, mai
                                   _ptr(global_used), _stream(stream)))
 
 
+def ddp_pack_group(descs, bucket_start, grads, used, ld, W, main_grad, replica_stride, accumulate=0,
+                   stream=None) -> None:
+    B = len(descs)
+    arr = (BucketDesc * max(B, 1))(*descs)
+    starts = _a(bucket_start, np.int64)
+    _check(lib().ddp_pack_group(arr, _cp(starts, _i64p), B, _ptr(grads), _ptr(used), int(ld), int(W),
+                                _ptr(main_grad), int(replica_stride), int(accumulate), _stream(stream)))
+
+
 def ddp_fused_bucket_group(descs, bucket_start, grads, used, ld, W, mode, accumulate, main_grad, replica_stride,
                            grads_out=None, global_used=None, stream=None) -> None:
     B = len(descs)
@@ -203,6 +225,17 @@ def ddp_fused_bucket_group(descs, bucket_start, grads, used, ld, W, mode, accumu
     _check(lib().ddp_fused_bucket_group(arr, _cp(starts, _i64p), B, _ptr(grads), _ptr(used), int(ld), int(W),
                                         int(mode), int(accumulate), _ptr(main_grad), int(replica_stride),
                                         _ptr(grads_out), _ptr(global_used), _stream(stream)))
+
+
+def ddp_fused_bucket_group_wire(descs, bucket_start, grads, used, ld, W, mode, accumulate, main_grad,
+                                replica_stride, grads_out=None, global_used=None, wire_dtype=DDP_BF16,
+                                stream=None) -> None:
+    B = len(descs)
+    arr = (BucketDesc * max(B, 1))(*descs)
+    starts = _a(bucket_start, np.int64)
+    _check(lib().ddp_fused_bucket_group_wire(arr, _cp(starts, _i64p), B, _ptr(grads), _ptr(used), int(ld), int(W),
+                                             int(mode), int(accumulate), _ptr(main_grad), int(replica_stride),
+                                             _ptr(grads_out), _ptr(global_used), int(wire_dtype), _stream(stream)))
 
 
 # ---------------------------------------------------------------------------

@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUTDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUTDIR, "libddpbucket.so")
-SOURCES = ["kernels.cu", "stream.cu", "reducer.cpp", "assign.cpp", "status.cpp"]
+SOURCES = ["kernels.cu", "stream_ring.cu", "stream_fused.cu", "stream_pack.cu", "reducer.cpp", "assign.cpp",
+           "status.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,6 +33,7 @@ def nvcc() -> str:
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "common.h"),
                                                         os.path.join(CSRC, "device_common.cuh"),
+                                                        os.path.join(CSRC, "stream_impl.cuh"),
                                                         os.path.join(INCLUDE, "ddp_bucket.h")]
     return files
 

@@ -18,16 +18,23 @@ constexpr int32_t kMaxReplicas = 64;
 // Device data-path launchers (kernels.cu); arguments are already validated.
 ddp_status launch_pack(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
                        int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream);
-ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream);
+ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream,
+                            int32_t wire = DDP_F32);
 ddp_status launch_unpack(const ddp_bucket_desc& b, const float* main_grad, int64_t stride, int32_t W,
                          int32_t mode, void* const* grads_out, int32_t ld, const uint8_t* global_used,
                          void* stream);
 ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
                         int32_t W, int32_t mode, int32_t accumulate, float* main_grad, int64_t stride,
-                        void* const* grads_out, const uint8_t* global_used, void* stream);
+                        void* const* grads_out, const uint8_t* global_used, void* stream, int32_t wire = DDP_F32);
+ddp_status launch_pack_plain(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
+                             int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream);
+ddp_status launch_pack_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
+                             const uint8_t* used, int32_t ld, int32_t W, int32_t accumulate, int64_t stride,
+                             void* stream);
 // Several buckets (bs[i] with main_grad copy mgs[i], may be null) in as few launches as possible.
 ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
                               const uint8_t* used, int32_t ld, int32_t W, int32_t mode, int32_t accumulate,
-                              int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream);
+                              int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream,
+                              int32_t wire = DDP_F32);
 
 }  // namespace ddp

@@ -35,6 +35,7 @@ struct Ctx {
     float* mg;          // replica 0 of the bucket (main_grad), may be null for OP_FUSED
     int64_t stride;     // elements between replicas of mg
     int32_t mg_vec;     // every replica of mg is 16-byte aligned
+    int32_t wire;       // ring arithmetic type: DDP_F32, or DDP_BF16 / DDP_F16 (compression hook)
 };
 
 struct PieceShared {
@@ -110,6 +111,41 @@ __host__ __device__ __forceinline__ int64_t lmax(int64_t a, int64_t b) { return 
 
 template <int DT> __host__ __device__ constexpr int elem_bytes() { return DT == DDP_F32 ? 4 : 2; }
 
+// ---------------------------------------------------------------------------
+// one ring term and one ring addition
+// ---------------------------------------------------------------------------
+// wire == DDP_F32: the contribution is t * fp32(1/W) and partial sums are fp32.
+// wire == DDP_BF16 / DDP_F16 (the compression hook, "DDP: ring AllReduce and
+// gradient buckets" 17.9, 17.20): t is rounded to the wire type, divided by W
+// and rounded again, and every partial sum is rounded to the wire type.  Each
+// step is computed in fp32 and then rounded: for 16-bit wire types (8- and
+// 11-bit significands) an fp32 sum or quotient of two wire values rounded to
+// the wire type equals the correctly rounded result (24 >= 2q + 2).
+__device__ __forceinline__ float wire_round(float x, int wire)
+{
+    return wire == DDP_BF16 ? __bfloat162float(__float2bfloat16_rn(x)) : __half2float(__float2half_rn(x));
+}
+__device__ __forceinline__ float ring_term(float t, float inv_w, float fw, int wire)
+{
+    if (wire == DDP_F32) return __fmul_rn(t, inv_w);
+    return wire_round(__fdiv_rn(wire_round(t, wire), fw), wire);
+}
+__device__ __forceinline__ float ring_add(float acc, float t, int wire)
+{
+    const float s = __fadd_rn(acc, t);
+    return wire == DDP_F32 ? s : wire_round(s, wire);
+}
+__device__ __forceinline__ float4 ring_term(float4 t, float inv_w, float fw, int wire)
+{
+    return make_float4(ring_term(t.x, inv_w, fw, wire), ring_term(t.y, inv_w, fw, wire),
+                       ring_term(t.z, inv_w, fw, wire), ring_term(t.w, inv_w, fw, wire));
+}
+__device__ __forceinline__ float4 ring_add(float4 acc, float4 t, int wire)
+{
+    return make_float4(ring_add(acc.x, t.x, wire), ring_add(acc.y, t.y, wire), ring_add(acc.z, t.z, wire),
+                       ring_add(acc.w, t.w, wire));
+}
+
 // Loads per thread kept in flight: about 16 vectors whatever W is.
 template <int WT> __host__ __device__ constexpr int unroll_for()
 {
@@ -141,6 +177,8 @@ struct StreamArgs {
     int32_t W, mode, accumulate, ld, nb;
     int32_t ns;                  // pipeline stages (set by the launcher)
     int32_t store_bulk;          // results leave through TMA bulk stores (set by the launcher)
+    int* status;                 // device status word (set by the launcher)
+    int32_t wire;                // ring arithmetic type: DDP_F32, DDP_BF16, DDP_F16
     StreamSpan span[kMaxBatch];
 };
 

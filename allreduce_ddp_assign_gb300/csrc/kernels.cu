@@ -79,8 +79,8 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (!live[u]) continue;
-                    const T t = L::mul(value(r, e[u]), cx.inv_w);
-                    acc[u] = (k == 0) ? t : L::add(acc[u], t);
+                    const T t = ring_term(value(r, e[u]), cx.inv_w, static_cast<float>(W), cx.wire);
+                    acc[u] = (k == 0) ? t : ring_add(acc[u], t, cx.wire);
                 }
             };
             if constexpr (WT > 0) {
@@ -332,11 +332,14 @@ namespace ddp {
 
 using namespace ddpk;
 
-ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream)
+ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t W, int32_t mode, void* stream,
+                            int32_t wire)
 {
-    if (n == 0 || W == 1) return ok();  // the mean of one replica is the replica (x * 1 is exact)
+    // the fp32 mean of one replica is the replica (x * 1 is exact); a 16-bit wire still rounds
+    if (n == 0 || (W == 1 && wire == DDP_F32)) return ok();
     Ctx cx = base_ctx(n, W, true, mode);
     set_mg(cx, replicas, stride);
+    cx.wire = wire;
     if (kernel_variant() == DDP_KERNEL_AUTO && cx.mg_vec && stream_supported(OP_RING, W, DDP_F32, false, mode)) {
         StreamArgs a{};
         a.total = n;
@@ -344,6 +347,7 @@ ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t 
         a.inv_w = cx.inv_w;
         a.W = W;
         a.mode = mode;
+        a.wire = wire;
         a.nb = 1;
         a.span[0] = StreamSpan{n, 0, replicas, nullptr, nullptr, 0, 1};
         return launch_stream(OP_RING, a, DDP_F32, stream);
@@ -353,6 +357,17 @@ ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t 
 
 ddp_status launch_pack(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
                        int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream)
+{
+    if (b.numel == 0) return ok();
+    if (kernel_variant() == DDP_KERNEL_AUTO && stream_supported(OP_PACK, W, b.dtype, accumulate != 0, DDP_ALLREDUCE)) {
+        float* mgs[1] = {main_grad};
+        return launch_pack_group(&b, mgs, 1, grads, used, ld, W, accumulate, stride, stream);
+    }
+    return launch_pack_plain(b, grads, used, ld, W, main_grad, stride, accumulate, stream);
+}
+
+ddp_status launch_pack_plain(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
+                             int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream)
 {
     if (b.numel == 0) return ok();
     Ctx cx = base_ctx(b.numel, W, false, DDP_ALLREDUCE);
@@ -381,7 +396,7 @@ ddp_status launch_unpack(const ddp_bucket_desc& b, const float* main_grad, int64
 
 ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
                         int32_t W, int32_t mode, int32_t accumulate, float* main_grad, int64_t stride,
-                        void* const* grads_out, const uint8_t* global_used, void* stream)
+                        void* const* grads_out, const uint8_t* global_used, void* stream, int32_t wire)
 {
     if (b.numel == 0) return ok();
     Ctx cx = base_ctx(b.numel, W, true, mode);
@@ -393,26 +408,28 @@ ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, cons
     cx.grads_out = grads_out;
     cx.global_used = global_used;
     cx.accumulate = accumulate != 0;
+    cx.wire = wire;
     if (kernel_variant() == DDP_KERNEL_AUTO && stream_supported(OP_FUSED, W, b.dtype, cx.accumulate, mode)) {
         float* mgs[1] = {main_grad};
         return launch_fused_group(&b, mgs, 1, grads, used, ld, W, mode, accumulate, stride, grads_out, global_used,
-                                  stream);
+                                  stream, wire);
     }
     return dispatch<OP_FUSED>(cx, b.dtype, stream);
 }
 
-ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
-                              const uint8_t* used, int32_t ld, int32_t W, int32_t mode, int32_t accumulate,
-                              int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream)
+// One streaming launch per run of same-dtype buckets (at most kMaxBatch); buckets the
+// streaming kernel cannot take go one by one through `single`.
+template <typename Single>
+ddp_status launch_group(int op, const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
+                        const uint8_t* used, int32_t ld, int32_t W, int32_t mode, int32_t accumulate, int64_t stride,
+                        void* const* grads_out, const uint8_t* global_used, void* stream, int32_t wire, Single single)
 {
     const bool acc = accumulate != 0;
     int32_t i = 0;
     while (i < nb) {
-        // one streaming launch per run of same-dtype buckets (at most kMaxBatch)
         const int32_t dt = bs[i].dtype;
-        if (kernel_variant() != DDP_KERNEL_AUTO || !stream_supported(OP_FUSED, W, dt, acc, mode)) {
-            const ddp_status st = launch_fused(bs[i], grads, used, ld, W, mode, accumulate, mgs[i], stride, grads_out,
-                                               global_used, stream);
+        if (kernel_variant() != DDP_KERNEL_AUTO || !stream_supported(op, W, dt, acc, mode)) {
+            const ddp_status st = single(i);
             if (st != DDP_OK) return st;
             ++i;
             continue;
@@ -428,6 +445,7 @@ ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int3
         a.mode = mode;
         a.accumulate = acc;
         a.ld = ld;
+        a.wire = wire;
         int64_t total = 0;
         int32_t n = 0;
         while (i < nb && n < kMaxBatch && bs[i].dtype == dt) {
@@ -442,10 +460,32 @@ ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int3
         a.nb = n;
         a.total = total;
         if (total == 0) continue;
-        const ddp_status st = launch_stream(OP_FUSED, a, dt, stream);
+        const ddp_status st = launch_stream(op, a, dt, stream);
         if (st != DDP_OK) return st;
     }
     return ok();
+}
+
+ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
+                              const uint8_t* used, int32_t ld, int32_t W, int32_t mode, int32_t accumulate,
+                              int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream,
+                              int32_t wire)
+{
+    return launch_group(OP_FUSED, bs, mgs, nb, grads, used, ld, W, mode, accumulate, stride, grads_out, global_used,
+                        stream, wire, [&](int32_t i) {
+                            return launch_fused(bs[i], grads, used, ld, W, mode, accumulate, mgs[i], stride,
+                                                grads_out, global_used, stream, wire);
+                        });
+}
+
+ddp_status launch_pack_group(const ddp_bucket_desc* bs, float* const* mgs, int32_t nb, const void* const* grads,
+                             const uint8_t* used, int32_t ld, int32_t W, int32_t accumulate, int64_t stride,
+                             void* stream)
+{
+    return launch_group(OP_PACK, bs, mgs, nb, grads, used, ld, W, DDP_ALLREDUCE, accumulate, stride, nullptr,
+                        nullptr, stream, DDP_F32, [&](int32_t i) {
+                            return launch_pack_plain(bs[i], grads, used, ld, W, mgs[i], stride, accumulate, stream);
+                        });
 }
 
 }  // namespace ddp
@@ -501,17 +541,36 @@ ddp_status check_mg(const char* fn, const float* mg, int64_t stride, int64_t n, 
         if (st_ != DDP_OK) return st_;      \
     } while (0)
 
+ddp_status check_wire(const char* fn, int32_t wire)
+{
+    if (wire != DDP_F32 && wire != DDP_BF16 && wire != DDP_F16)
+        return ddp::fail(DDP_E_INVAL, "%s: unknown wire dtype %d", fn, wire);
+    return DDP_OK;
+}
+
+ddp_status allreduce_checked(const char* fn, float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
+                             int32_t mode, int32_t wire, void* stream)
+{
+    DDP_TRY(check_w(fn, W));
+    DDP_TRY(check_wire(fn, wire));
+    if (numel < 0) return ddp::fail(DDP_E_INVAL, "%s: numel < 0", fn);
+    DDP_TRY(check_mode(fn, mode, numel, W));
+    DDP_TRY(check_mg(fn, replicas, replica_stride, numel, W));
+    return ddp::launch_allreduce(replicas, replica_stride, numel, W, mode, stream, wire);
+}
+
 }  // namespace
 
 extern "C" ddp_status ddp_bucket_allreduce(float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
                                            int32_t mode, void* stream)
 {
-    const char* fn = "ddp_bucket_allreduce";
-    DDP_TRY(check_w(fn, W));
-    if (numel < 0) return ddp::fail(DDP_E_INVAL, "%s: numel < 0", fn);
-    DDP_TRY(check_mode(fn, mode, numel, W));
-    DDP_TRY(check_mg(fn, replicas, replica_stride, numel, W));
-    return ddp::launch_allreduce(replicas, replica_stride, numel, W, mode, stream);
+    return allreduce_checked("ddp_bucket_allreduce", replicas, replica_stride, numel, W, mode, DDP_F32, stream);
+}
+
+extern "C" ddp_status ddp_bucket_allreduce_wire(float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
+                                                int32_t mode, int32_t wire_dtype, void* stream)
+{
+    return allreduce_checked("ddp_bucket_allreduce_wire", replicas, replica_stride, numel, W, mode, wire_dtype, stream);
 }
 
 extern "C" ddp_status ddp_pack(const ddp_bucket_desc* bucket, const void* const* grads, const uint8_t* used,
@@ -539,14 +598,38 @@ extern "C" ddp_status ddp_unpack(const ddp_bucket_desc* bucket, const float* mai
     return ddp::launch_unpack(*bucket, main_grad, replica_stride, W, mode, grads_out, ld, global_used, stream);
 }
 
-extern "C" ddp_status ddp_fused_bucket_group(const ddp_bucket_desc* buckets, const int64_t* bucket_start,
-                                             int32_t nbuckets, const void* const* grads, const uint8_t* used,
-                                             int32_t ld, int32_t W, int32_t mode, int32_t accumulate, float* main_grad,
-                                             int64_t replica_stride, void* const* grads_out,
-                                             const uint8_t* global_used, void* stream)
+extern "C" ddp_status ddp_pack_group(const ddp_bucket_desc* buckets, const int64_t* bucket_start, int32_t nbuckets,
+                                     const void* const* grads, const uint8_t* used, int32_t ld, int32_t W,
+                                     float* main_grad, int64_t replica_stride, int32_t accumulate, void* stream)
 {
-    const char* fn = "ddp_fused_bucket_group";
+    const char* fn = "ddp_pack_group";
     DDP_TRY(check_w(fn, W));
+    if (nbuckets < 0 || (nbuckets > 0 && (!buckets || !bucket_start)))
+        return ddp::fail(DDP_E_INVAL, "%s: bad bucket list", fn);
+    std::vector<float*> mgs(static_cast<size_t>(nbuckets), nullptr);
+    for (int32_t b = 0; b < nbuckets; ++b) {
+        DDP_TRY(check_desc(fn, &buckets[b], ld, true));
+        if (buckets[b].nseg > 0 && !grads) return ddp::fail(DDP_E_INVAL, "%s: grads table is NULL", fn);
+        DDP_TRY(check_mg(fn, main_grad, replica_stride, buckets[b].numel, W));
+        if (bucket_start[b] < 0 || (W > 1 && bucket_start[b] + buckets[b].numel > replica_stride))
+            return ddp::fail(DDP_E_INVAL, "%s: bucket %d [%lld, +%lld) exceeds replica_stride %lld", fn, b,
+                             static_cast<long long>(bucket_start[b]), static_cast<long long>(buckets[b].numel),
+                             static_cast<long long>(replica_stride));
+        mgs[b] = main_grad ? main_grad + bucket_start[b] : nullptr;
+    }
+    return ddp::launch_pack_group(buckets, mgs.data(), nbuckets, grads, used, ld, W, accumulate, replica_stride,
+                                  stream);
+}
+
+namespace {
+
+ddp_status fused_group_checked(const char* fn, const ddp_bucket_desc* buckets, const int64_t* bucket_start,
+                               int32_t nbuckets, const void* const* grads, const uint8_t* used, int32_t ld, int32_t W,
+                               int32_t mode, int32_t accumulate, float* main_grad, int64_t replica_stride,
+                               void* const* grads_out, const uint8_t* global_used, int32_t wire, void* stream)
+{
+    DDP_TRY(check_w(fn, W));
+    DDP_TRY(check_wire(fn, wire));
     if (nbuckets < 0 || (nbuckets > 0 && (!buckets || (main_grad && !bucket_start))))
         return ddp::fail(DDP_E_INVAL, "%s: bad bucket list", fn);
     std::vector<float*> mgs(static_cast<size_t>(nbuckets), nullptr);
@@ -567,7 +650,29 @@ extern "C" ddp_status ddp_fused_bucket_group(const ddp_bucket_desc* buckets, con
         }
     }
     return ddp::launch_fused_group(buckets, mgs.data(), nbuckets, grads, used, ld, W, mode, accumulate,
-                                   replica_stride, grads_out, global_used, stream);
+                                   replica_stride, grads_out, global_used, stream, wire);
+}
+
+}  // namespace
+
+extern "C" ddp_status ddp_fused_bucket_group(const ddp_bucket_desc* buckets, const int64_t* bucket_start,
+                                             int32_t nbuckets, const void* const* grads, const uint8_t* used,
+                                             int32_t ld, int32_t W, int32_t mode, int32_t accumulate, float* main_grad,
+                                             int64_t replica_stride, void* const* grads_out,
+                                             const uint8_t* global_used, void* stream)
+{
+    return fused_group_checked("ddp_fused_bucket_group", buckets, bucket_start, nbuckets, grads, used, ld, W, mode,
+                               accumulate, main_grad, replica_stride, grads_out, global_used, DDP_F32, stream);
+}
+
+extern "C" ddp_status ddp_fused_bucket_group_wire(const ddp_bucket_desc* buckets, const int64_t* bucket_start,
+                                                  int32_t nbuckets, const void* const* grads, const uint8_t* used,
+                                                  int32_t ld, int32_t W, int32_t mode, int32_t accumulate,
+                                                  float* main_grad, int64_t replica_stride, void* const* grads_out,
+                                                  const uint8_t* global_used, int32_t wire_dtype, void* stream)
+{
+    return fused_group_checked("ddp_fused_bucket_group_wire", buckets, bucket_start, nbuckets, grads, used, ld, W,
+                               mode, accumulate, main_grad, replica_stride, grads_out, global_used, wire_dtype, stream);
 }
 
 extern "C" ddp_status ddp_fused_bucket(const ddp_bucket_desc* bucket, const void* const* grads,

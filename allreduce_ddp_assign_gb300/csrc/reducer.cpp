@@ -88,6 +88,11 @@ struct ddp_reducer {
         return s;
     }
 
+    int32_t wire() const
+    {
+        return (flags & DDP_R_WIRE_BF16) ? DDP_BF16 : ((flags & DDP_R_WIRE_F16) ? DDP_F16 : DDP_F32);
+    }
+
     ddp_status launch_bucket(int32_t b)
     {
         const ddp_bucket_desc& d = buckets[b];
@@ -96,9 +101,9 @@ struct ddp_reducer {
         const bool copy_back = flags & DDP_R_COPY_BACK;
         if (flags & DDP_R_FUSED)
             return ddp::launch_fused(d, grads, used, ld, W, mode, accumulate, mgb, stride,
-                                     copy_back ? grads_out : nullptr, global_used, st);
+                                     copy_back ? grads_out : nullptr, global_used, st, wire());
         ddp_status s = ddp::launch_pack(d, grads, used, ld, W, mgb, stride, accumulate, st);
-        if (s == DDP_OK) s = ddp::launch_allreduce(mgb, stride, d.numel, W, mode, st);
+        if (s == DDP_OK) s = ddp::launch_allreduce(mgb, stride, d.numel, W, mode, st, wire());
         if (s == DDP_OK && copy_back)
             s = ddp::launch_unpack(d, mgb, stride, W, mode, grads_out, ld, global_used, st);
         return s;
@@ -130,7 +135,7 @@ struct ddp_reducer {
             }
             st = ddp::launch_fused_group(group_descs.data(), group_mgs.data(), count, grads, used, ld, W, mode,
                                          accumulate, stride, (flags & DDP_R_COPY_BACK) ? grads_out : nullptr,
-                                         global_used, static_cast<void*>(side));
+                                         global_used, static_cast<void*>(side), wire());
             if (st != DDP_OK) return st;
             if (timing)
                 for (int32_t i = 0; i < count; ++i)
@@ -208,8 +213,11 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
         return fail(DDP_E_INVAL, "%s: a per-bucket array is NULL", fn);
     if (W < 1 || W > ddp::kMaxReplicas) return fail(DDP_E_INVAL, "%s: W = %d outside [1, %d]", fn, W, ddp::kMaxReplicas);
     if (mode != DDP_ALLREDUCE && mode != DDP_REDUCE_SCATTER) return fail(DDP_E_INVAL, "%s: unknown mode %d", fn, mode);
-    if (flags & ~(DDP_R_FUSED | DDP_R_COPY_BACK | DDP_R_TIMING | DDP_R_DRY_RUN | DDP_R_COALESCE))
+    if (flags & ~(DDP_R_FUSED | DDP_R_COPY_BACK | DDP_R_TIMING | DDP_R_DRY_RUN | DDP_R_COALESCE | DDP_R_WIRE_BF16 |
+                  DDP_R_WIRE_F16))
         return fail(DDP_E_INVAL, "%s: unknown flag bits 0x%x", fn, flags);
+    if ((flags & DDP_R_WIRE_BF16) && (flags & DDP_R_WIRE_F16))
+        return fail(DDP_E_INVAL, "%s: DDP_R_WIRE_BF16 and DDP_R_WIRE_F16 exclude each other", fn);
     if ((flags & DDP_R_COALESCE) && !(flags & DDP_R_FUSED))
         return fail(DDP_E_INVAL, "%s: DDP_R_COALESCE needs DDP_R_FUSED", fn);
     const bool dry = flags & DDP_R_DRY_RUN;

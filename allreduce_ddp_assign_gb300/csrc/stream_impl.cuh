@@ -1,7 +1,11 @@
-// TMA-pipelined streaming kernel for the two hot operations: the ring-ordered
+// TMA-pipelined streaming kernel: definitions shared by stream_ring.cu,
+// stream_fused.cu and stream_pack.cu, each of which instantiates one operation.
+#pragma once
+// TMA-pipelined streaming kernel for the three hot operations: the ring-ordered
 // reduction of packed replicas (ddp_bucket_allreduce) and the fused
 // pack + reduce (+ unpack) pass over one bucket or a group of buckets
-// (ddp_fused_bucket, ddp_fused_bucket_group, and the reducer's coalesced issue).
+// (ddp_fused_bucket, ddp_fused_bucket_group, and the reducer's coalesced issue),
+// and the no_sync pack of a bucket group (ddp_pack, ddp_pack_group).
 //
 // Arithmetic and decomposition are those of the plain kernels in kernels.cu:
 // the buckets of a launch are laid end to end, each CTA takes an equal
@@ -40,6 +44,9 @@
 #ifndef DDP_STREAM_TILE_W
 #define DDP_STREAM_TILE_W 16384    // tile elements x W (tiles are clamped to 1024..4096 elements)
 #endif
+#ifndef DDP_STREAM_TILE_MAX
+#define DDP_STREAM_TILE_MAX 4096   // largest tile (elements)
+#endif
 #ifndef DDP_STREAM_L2_HINT
 #define DDP_STREAM_L2_HINT 0       // 1: stream operands in with an L2 evict-first policy
 #endif
@@ -61,16 +68,14 @@ constexpr unsigned kFull = 0xffffffffu;
 // elements per tile: DDP_STREAM_TILE_W / W, between 1024 and 4096, so each
 // consumer thread owns 1, 2 or 4 vectors (W = 8: 2048 elements, 64 KB of fp32
 // or 32 KB of bf16 staged per stage)
-template <int OP, int WT, int DT>
+template <int OP, int WT, int DT, bool ACC>
 __host__ __device__ constexpr int tile_of()
 {
     constexpr int w = WT ? WT : 8;
-    constexpr int t = DDP_STREAM_TILE_W / w;
-    return t >= 4096 ? 4096 : (t >= 2048 ? 2048 : 1024);
+    // staging main_grad as well (accumulating) doubles a stage: halve the tile
+    constexpr int t = DDP_STREAM_TILE_W / w / (ACC ? 2 : 1);
+    return (t >= 4096 && DDP_STREAM_TILE_MAX >= 4096) ? 4096 : ((t >= 2048 && DDP_STREAM_TILE_MAX >= 2048) ? 2048 : 1024);
 }
-
-// status word read by ddp_device_status(); written only on a wait timeout
-__device__ int g_device_status = 0;
 
 struct TileDesc {
     float* mg;          // the tile's bucket in main_grad, replica 0 (nullptr: none)
@@ -178,7 +183,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* b, uint32_t parity)
     return false;
 }
 
-__device__ __forceinline__ void record_error(int code) { atomicOr(&g_device_status, code); }
+__device__ __forceinline__ void record_error(int* status, int code) { atomicOr(status, code); }
 
 // -- shared-memory layout (dynamic) -------------------------------------------
 struct Layout {
@@ -250,16 +255,16 @@ __device__ __forceinline__ float4 lds_grad4(const unsigned char* base, int i)
     }
 }
 
-template <int OP, int WT, int DT>
+template <int OP, int WT, int DT, bool ACC>
 __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int kTile = tile_of<OP, WT, DT>();
+    constexpr int kTile = tile_of<OP, WT, DT, ACC>();
     constexpr int kVpt = kTile / (4 * kConsumers);
     constexpr int gb = (OP == OP_RING) ? 4 : elem_bytes<DT>();
     const int W = WT ? WT : a.W;
     const int ns = a.ns;
-    const bool acc = (OP == OP_FUSED) && a.accumulate;
+    constexpr bool acc = ACC;
     const bool sbulk = a.store_bulk != 0;
     const Layout L = layout_for(ns, W, kTile, gb, acc, sbulk);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
             good = __shfl_sync(kFull, good, 0);
             if (!good) {
                 if (lane == 0) {
-                    record_error(kErrWaitTimeout);
+                    record_error(a.status, kErrWaitTimeout);
                     atomicExch(&abort_flag, 1);
                 }
                 ok = false;
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
             while (b + 1 < a.nb && a.span[b].base + a.span[b].numel <= x) ++b;
             const StreamSpan& S = a.span[b];
             const int64_t end = lmin(hi, S.base + S.numel) - S.base;  // bucket-local end of this CTA's part
-            const int64_t chunk = lmax(1, (S.numel + W - 1) / W);
+            const int64_t chunk = (OP == OP_PACK) ? lmax(1, S.numel) : lmax(1, (S.numel + W - 1) / W);
             int64_t e = x - S.base;
             int c = static_cast<int>(e / chunk);
             if (c >= W) c = W - 1;
@@ -439,7 +444,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
     for (int64_t k = 0;; ++k) {
         const int st = static_cast<int>(k % ns);
         const bool got = wait_bounded(&full[st], static_cast<uint32_t>((k / ns) & 1));
-        if (!got) record_error(kErrWaitTimeout);
+        if (!got) record_error(a.status, kErrWaitTimeout);
         if (sbulk && ct == 0) bulk_wait_read<kResDepth - 1>();  // result buffer k % kResDepth is free again
         // one decision for all consumers (this barrier also publishes the line above)
         if (!consumers_all(got && !*static_cast<volatile int*>(&abort_flag))) break;
@@ -450,6 +455,42 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
         const void* const* srcs = srcp + st * W;
         float* const* dsts = dstp + st * W;
         const bool early = (OP == OP_RING) || a.grads_out == nullptr;  // nothing else is read from the stage
+        if constexpr (OP == OP_PACK) {
+            // every replica keeps its own value: copy (or add) the staged gradient into main_grad
+            if (d.bulk) {
+#pragma unroll
+                for (int v = 0; v < kVpt; ++v) {
+                    const int i = 4 * (ct + v * kConsumers);
+                    if (i >= d.len) continue;
+                    const int64_t e = d.e0 + i;
+                    for (int w = 0; w < W; ++w) {
+                        const bool has = (d.src_mask >> w) & 1;
+                        if (acc && !has) continue;  // no gradient: the bucket keeps its sum
+                        float4 t = has ? lds_grad4<DT>(data + (static_cast<size_t>(st) * W + w) * kTile * gb, i)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (acc)
+                            t = Lane<4>::add(*reinterpret_cast<const float4*>(
+                                                 mgd + (static_cast<size_t>(st) * W + w) * kTile * 4 + 4 * i),
+                                             t);
+                        Lane<4>::st(mgb + w * a.stride + e, t);
+                    }
+                }
+            } else {
+                for (int i = ct; i < d.len; i += kConsumers) {
+                    const int64_t e = d.e0 + i;
+                    for (int w = 0; w < W; ++w) {
+                        const void* src = srcs[w];
+                        if (acc && !src) continue;
+                        float t = src ? Lane<1>::template ldg<DT>(src, e - d.off) : 0.f;
+                        if (acc) t = Lane<1>::add(Lane<1>::ld(mgb + w * a.stride + e), t);
+                        Lane<1>::st(mgb + w * a.stride + e, t);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            continue;
+        }
         if (d.bulk) {
             float4 sum[kVpt];
 #pragma unroll
@@ -472,8 +513,8 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
                             t = has ? Lane<4>::add(m, t) : m;
                         }
                     }
-                    t = Lane<4>::mul(t, a.inv_w);
-                    sum[v] = (kk == 0) ? t : Lane<4>::add(sum[v], t);
+                    t = ring_term(t, a.inv_w, static_cast<float>(W), a.wire);
+                    sum[v] = (kk == 0) ? t : ring_add(sum[v], t, a.wire);
                 };
                 if constexpr (WT > 0) {
 #pragma unroll
@@ -561,8 +602,8 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
                         t = src ? Lane<1>::add(m, t) : m;
                     }
                 }
-                t = Lane<1>::mul(t, a.inv_w);
-                sum = (kk == 0) ? t : Lane<1>::add(sum, t);
+                t = ring_term(t, a.inv_w, static_cast<float>(W), a.wire);
+                sum = (kk == 0) ? t : ring_add(sum, t, a.wire);
             }
             if (mgb) {
                 if (a.mode == DDP_ALLREDUCE) {
@@ -590,7 +631,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
 constexpr uint32_t kSmemBudget2 = DDP_STREAM_BUDGET2_KB * 1024;  // two CTAs per SM
 constexpr uint32_t kSmemBudget1 = 220 * 1024;                    // one CTA per SM
 
-int sm_count_tma()
+inline int sm_count_tma()
 {
     static int cached[64] = {0};
     int dev = 0;
@@ -604,7 +645,7 @@ int sm_count_tma()
 }
 
 // stages that fit the budget (0 if fewer than two)
-int stages_for(int W, int tile, int gb, bool acc, bool sbulk, uint32_t budget)
+inline int stages_for(int W, int tile, int gb, bool acc, bool sbulk, uint32_t budget)
 {
     for (int ns = 8; ns >= 2; --ns)
         if (layout_for(ns, W, tile, gb, acc, sbulk).total <= budget) return ns;
@@ -616,7 +657,7 @@ struct StagePlan {
     uint32_t bytes, budget;
 };
 
-bool plan_for(int W, int tile, int gb, bool acc, bool sbulk, StagePlan* p)
+inline bool plan_for(int W, int tile, int gb, bool acc, bool sbulk, StagePlan* p)
 {
     int ns = stages_for(W, tile, gb, acc, sbulk, kSmemBudget2);
     uint32_t budget = kSmemBudget2;
@@ -629,14 +670,14 @@ bool plan_for(int W, int tile, int gb, bool acc, bool sbulk, StagePlan* p)
     return true;
 }
 
-template <int OP, int WT, int DT>
+template <int OP, int WT, int DT, bool ACC>
 ddp_status launch_instance(StreamArgs& a, void* stream)
 {
-    auto kern = stream_kernel<OP, WT, DT>;
-    constexpr int tile = tile_of<OP, WT, DT>();
+    auto kern = stream_kernel<OP, WT, DT, ACC>;
+    constexpr int tile = tile_of<OP, WT, DT, ACC>();
     constexpr int gb = (OP == OP_RING) ? 4 : elem_bytes<DT>();
     StagePlan p{};
-    if (!plan_for(a.W, tile, gb, OP == OP_FUSED && a.accumulate, a.store_bulk, &p))
+    if (!plan_for(a.W, tile, gb, ACC, a.store_bulk, &p))
         return ddp::fail(DDP_E_INVAL, "stream kernel: no stage layout fits for W = %d", a.W);
     a.ns = p.ns;
     static uint32_t configured = 0;
@@ -663,77 +704,45 @@ ddp_status launch_instance(StreamArgs& a, void* stream)
     return ddp::ok();
 }
 
-template <int OP, int DT>
+template <int OP, int DT, bool ACC>
 ddp_status dispatch_w(StreamArgs& a, void* stream)
 {
     switch (a.W) {
-    case 2: return launch_instance<OP, 2, DT>(a, stream);
-    case 4: return launch_instance<OP, 4, DT>(a, stream);
-    case 8: return launch_instance<OP, 8, DT>(a, stream);
-    case 16: return launch_instance<OP, 16, DT>(a, stream);
-    default: return launch_instance<OP, 0, DT>(a, stream);
+    case 2: return launch_instance<OP, 2, DT, ACC>(a, stream);
+    case 4: return launch_instance<OP, 4, DT, ACC>(a, stream);
+    case 8: return launch_instance<OP, 8, DT, ACC>(a, stream);
+    case 16: return launch_instance<OP, 16, DT, ACC>(a, stream);
+    default: return launch_instance<OP, 0, DT, ACC>(a, stream);
     }
 }
 
-template <int OP, int DT>
+template <int OP, bool ACC>
 int tile_for_w(int W)
 {
     switch (W) {
-    case 2: return tile_of<OP, 2, DT>();
-    case 4: return tile_of<OP, 4, DT>();
-    case 8: return tile_of<OP, 8, DT>();
-    case 16: return tile_of<OP, 16, DT>();
-    default: return tile_of<OP, 0, DT>();
+    case 2: return tile_of<OP, 2, DDP_F32, ACC>();
+    case 4: return tile_of<OP, 4, DDP_F32, ACC>();
+    case 8: return tile_of<OP, 8, DDP_F32, ACC>();
+    case 16: return tile_of<OP, 16, DDP_F32, ACC>();
+    default: return tile_of<OP, 0, DDP_F32, ACC>();
+    }
+}
+
+// the operations a launch of one TU covers
+template <int OP>
+ddp_status launch_op(StreamArgs& a, int dtype, void* stream)
+{
+    if constexpr (OP == OP_RING) {
+        return dispatch_w<OP_RING, DDP_F32, false>(a, stream);
+    } else {
+        const bool acc = a.accumulate != 0;
+        switch (dtype) {
+        case DDP_BF16: return acc ? dispatch_w<OP, DDP_BF16, true>(a, stream) : dispatch_w<OP, DDP_BF16, false>(a, stream);
+        case DDP_F16: return acc ? dispatch_w<OP, DDP_F16, true>(a, stream) : dispatch_w<OP, DDP_F16, false>(a, stream);
+        default: return acc ? dispatch_w<OP, DDP_F32, true>(a, stream) : dispatch_w<OP, DDP_F32, false>(a, stream);
+        }
     }
 }
 
 }  // namespace
-
-bool stream_supported(int op, int W, int dtype, bool acc, int mode)
-{
-    if (W < 2 || W > 16) return false;
-    const bool sbulk = mode == DDP_ALLREDUCE;
-    StagePlan p{};
-    if (op == OP_RING) return plan_for(W, tile_for_w<OP_RING, DDP_F32>(W), 4, false, sbulk, &p);
-    switch (dtype) {
-    case DDP_BF16: return plan_for(W, tile_for_w<OP_FUSED, DDP_BF16>(W), 2, acc, sbulk, &p);
-    case DDP_F16: return plan_for(W, tile_for_w<OP_FUSED, DDP_F16>(W), 2, acc, sbulk, &p);
-    default: return plan_for(W, tile_for_w<OP_FUSED, DDP_F32>(W), 4, acc, sbulk, &p);
-    }
-}
-
-ddp_status launch_stream(int op, StreamArgs& a, int dtype, void* stream)
-{
-    a.store_bulk = a.mode == DDP_ALLREDUCE;  // W results per vector: they leave through TMA bulk stores
-    if (op == OP_RING) return dispatch_w<OP_RING, DDP_F32>(a, stream);
-    switch (dtype) {
-    case DDP_BF16: return dispatch_w<OP_FUSED, DDP_BF16>(a, stream);
-    case DDP_F16: return dispatch_w<OP_FUSED, DDP_F16>(a, stream);
-    default: return dispatch_w<OP_FUSED, DDP_F32>(a, stream);
-    }
-}
-
-ddp_status read_device_status(void* stream, int32_t* out, int reset)
-{
-    int v = 0;
-    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost,
-                                              static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e == cudaSuccess && reset && v != 0) {
-        const int zero = 0;
-        e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
-                                    static_cast<cudaStream_t>(stream));
-        if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    }
-    if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_device_status: %s", cudaGetErrorString(e));
-    *out = v;
-    return ddp::ok();
-}
-
 }  // namespace ddpk
-
-extern "C" ddp_status ddp_device_status(void* stream, int32_t* status, int32_t reset)
-{
-    if (!status) return ddp::fail(DDP_E_INVAL, "ddp_device_status: status is NULL");
-    return ddpk::read_device_status(stream, status, reset);
-}

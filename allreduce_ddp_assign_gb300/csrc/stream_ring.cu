@@ -1,0 +1,73 @@
+// The streaming kernel's ring instantiation, the per-operation dispatch, and
+// the device status word the streaming kernels report wait timeouts in.
+#include "stream_impl.cuh"
+
+namespace ddpk {
+
+ddp_status launch_stream_fused(StreamArgs& a, int dtype, void* stream);  // stream_fused.cu
+ddp_status launch_stream_pack(StreamArgs& a, int dtype, void* stream);   // stream_pack.cu
+
+namespace {
+// bit 0: a streaming kernel gave up on an mbarrier wait
+__device__ int g_device_status = 0;
+
+int* status_word()
+{
+    static int* cached[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cached[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<int*>(p);
+    }
+    return cached[dev];
+}
+}  // namespace
+
+bool stream_supported(int op, int W, int dtype, bool acc, int mode)
+{
+    if (W < 2 || W > 16) return false;
+    // the W copies of an allreduce result leave through bulk stores; a pack writes W different values
+    const bool sbulk = op != OP_PACK && mode == DDP_ALLREDUCE;
+    const int gb = (op == OP_RING || dtype == DDP_F32) ? 4 : 2;
+    StagePlan p{};
+    if (op == OP_RING) return plan_for(W, tile_for_w<OP_RING, false>(W), 4, false, sbulk, &p);
+    const int tile = acc ? tile_for_w<OP_FUSED, true>(W) : tile_for_w<OP_FUSED, false>(W);
+    return plan_for(W, tile, gb, acc, sbulk, &p);
+}
+
+ddp_status launch_stream(int op, StreamArgs& a, int dtype, void* stream)
+{
+    a.status = status_word();
+    if (!a.status) return ddp::fail(DDP_E_CUDA, "stream kernel: device status word unavailable");
+    a.store_bulk = op != OP_PACK && a.mode == DDP_ALLREDUCE;
+    if (op == OP_RING) return launch_op<OP_RING>(a, dtype, stream);
+    if (op == OP_PACK) return launch_stream_pack(a, dtype, stream);
+    return launch_stream_fused(a, dtype, stream);
+}
+
+ddp_status read_device_status(void* stream, int32_t* out, int reset)
+{
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                              static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && reset && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                                    static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    }
+    if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_device_status: %s", cudaGetErrorString(e));
+    *out = v;
+    return ddp::ok();
+}
+
+}  // namespace ddpk
+
+extern "C" ddp_status ddp_device_status(void* stream, int32_t* status, int32_t reset)
+{
+    if (!status) return ddp::fail(DDP_E_INVAL, "ddp_device_status: status is NULL");
+    return ddpk::read_device_status(stream, status, reset);
+}

@@ -9,7 +9,9 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, Plan, ddp_pack, ddp_reducer_bucket_ms, ddp_reducer_create,
+from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, DDP_R_WIRE_BF16,
+               DDP_R_WIRE_F16, Plan, ddp_pack, ddp_pack_group,
+               ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
                ddp_reducer_mark_ready_many, ddp_reducer_prepare)
 
@@ -26,10 +28,11 @@ class BucketReducer:
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads, used=None,
                  grads_out=None, fused=True, timing=False, side_stream=None, main_grad=True, grad_reduce_in_fp32=1,
-                 coalesce=False):
+                 coalesce=False, wire=None):
         import torch
 
         self.W, self.mode = int(W), int(mode)
+        self.coalesce = bool(coalesce)
         self.plan = Plan(numels, dtypes, cap_bytes, first_cap_bytes, order, pad_multiple, grad_reduce_in_fp32)
         P = self.plan.nparams
         self.side = side_stream if side_stream is not None else torch.cuda.Stream()
@@ -42,7 +45,8 @@ class BucketReducer:
         self.global_used_tab = None if gu is None else self.plan.flag_table(gu)
         self.out_tab = None if grads_out is None else self.plan.pointer_table(grads_out)
         flags = (DDP_R_FUSED if fused else 0) | (DDP_R_COPY_BACK if grads_out is not None else 0) | \
-                (DDP_R_TIMING if timing else 0) | (DDP_R_COALESCE if coalesce and fused else 0)
+                (DDP_R_TIMING if timing else 0) | (DDP_R_COALESCE if coalesce and fused else 0) | \
+                {None: 0, DDP_BF16: DDP_R_WIRE_BF16, DDP_F16: DDP_R_WIRE_F16}[wire]
         self.handle = ddp_reducer_create(P, self.plan.bucket_of, self.plan.bucket_order, self.plan.descs,
                                          self.plan.bucket_start, self.W, self.mode, flags, self.grads_tab,
                                          self.used_tab, P, self.main_grad, self.plan.replica_stride, self.out_tab,
@@ -54,6 +58,10 @@ class BucketReducer:
         """A no_sync micro-step: add (or, for the first, copy) this micro-step's
         gradients into main_grad without reducing (ddp_pack).  The tensors behind
         grads_tab must stay alive until the stream has run the kernels."""
+        if self.coalesce:
+            ddp_pack_group(self.plan.descs, self.plan.bucket_start, grads_tab, self.used_tab, self.plan.nparams, self.W,
+                           self.main_grad, self.plan.replica_stride, 0 if first else 1, stream)
+            return
         for b in range(self.plan.nbuckets):
             ddp_pack(self.plan.descs[b], grads_tab, self.used_tab, self.plan.nparams, self.W,
                      self.plan.main_grad_at(self.main_grad, b), self.plan.replica_stride, 0 if first else 1, stream)

@@ -233,7 +233,8 @@ def run_reference(args, wl):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-KERNEL_SOURCES = ("kernels.cu", "stream.cu", "device_common.cuh", "common.h")
+KERNEL_SOURCES = ("kernels.cu", "stream_impl.cuh", "stream_ring.cu", "stream_fused.cu", "stream_pack.cu",
+                  "device_common.cuh", "common.h")
 
 
 def kernel_source_hash() -> str:
@@ -473,7 +474,8 @@ def run_ours(args, wl):
                          "step_split_ms": {"pack": round(pack_ms, 4), "fused": round(fused_ms, 4)} if packs else None},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (len(launches) - len(fused) + (-(-len(fused) // 32) if coalesce else len(fused))) * K,
+            "gpu_launches": (((wl.micro_steps - 1) * -(-sess.plan.nbuckets // 32) + -(-len(fused) // 32)) if coalesce
+                             else len(launches)) * K,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -197,6 +197,20 @@ ddp_status ddp_pack(const ddp_bucket_desc* bucket, const void* const* grads, con
                     int32_t ld, int32_t W, float* main_grad, int64_t replica_stride,
                     int32_t accumulate, void* stream);
 
+/*
+ * ddp_pack_group -- ddp_pack over several buckets in as few kernel launches as
+ * possible (one per run of up to 32 buckets of one dtype): a no_sync
+ * micro-step's local accumulation over the whole model in one call.  Results
+ * are those of ddp_pack on each bucket in turn.
+ *   buckets[nbuckets], bucket_start[nbuckets]  HOST, as ddp_fused_bucket_group;
+ *   main_grad   DEVICE start of the per-replica buffer holding all buckets.
+ * Errors: as ddp_pack for any bucket; DDP_E_INVAL if a bucket does not fit in
+ * replica_stride.  Nothing is launched when a bucket is rejected.
+ */
+ddp_status ddp_pack_group(const ddp_bucket_desc* buckets, const int64_t* bucket_start, int32_t nbuckets,
+                          const void* const* grads, const uint8_t* used, int32_t ld, int32_t W, float* main_grad,
+                          int64_t replica_stride, int32_t accumulate, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Step 3: reduce (device)                                                   */
 /* ------------------------------------------------------------------------ */
@@ -228,6 +242,28 @@ ddp_status ddp_pack(const ddp_bucket_desc* bucket, const void* const* grads, con
  */
 ddp_status ddp_bucket_allreduce(float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
                                 int32_t mode, void* stream);
+
+/*
+ * ddp_bucket_allreduce_wire -- ddp_bucket_allreduce through a compression hook:
+ * the allreduce runs in a 16-bit wire type.
+ *
+ * Defined by: DDP chapter 17.9 and 17.20 (bf16_compress_hook /
+ * fp16_compress_hook: the fp32 bucket is converted to bf16 (fp16) and divided
+ * by the world size, the converted tensor is allreduced with a sum, and the
+ * result is copied back into the fp32 bucket).
+ *
+ * For an element of chunk c: z_w = wire(wire(x_w) / W) for every replica w,
+ * where wire() rounds to the wire type, to nearest with ties to even; then
+ * s = z_{c+1}; s = wire(s + z_{c+k}) for k = 2..W (the ring's order, every
+ * partial sum a wire value, as the messages are); the result is s widened to
+ * fp32.  Output placement as for ddp_bucket_allreduce.  W == 1 still rounds to
+ * the wire type.  fp16 saturates to infinity beyond 65504.
+ *
+ * wire_dtype: DDP_BF16 or DDP_F16 (DDP_F32 gives ddp_bucket_allreduce).
+ * Errors: as ddp_bucket_allreduce; DDP_E_INVAL for another wire_dtype.
+ */
+ddp_status ddp_bucket_allreduce_wire(float* replicas, int64_t replica_stride, int64_t numel, int32_t W,
+                                     int32_t mode, int32_t wire_dtype, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Step 4: unpack (device)                                                   */
@@ -301,6 +337,19 @@ ddp_status ddp_fused_bucket_group(const ddp_bucket_desc* buckets, const int64_t*
                                   int32_t mode, int32_t accumulate, float* main_grad, int64_t replica_stride,
                                   void* const* grads_out, const uint8_t* global_used, void* stream);
 
+/*
+ * ddp_fused_bucket_group_wire -- ddp_fused_bucket_group with the reduction
+ * through a compression hook (wire_dtype as for ddp_bucket_allreduce_wire):
+ * the packed value of each replica goes through wire(wire(.) / W) and the ring
+ * sums in the wire type.  Errors: as ddp_fused_bucket_group; DDP_E_INVAL for an
+ * unknown wire_dtype.
+ */
+ddp_status ddp_fused_bucket_group_wire(const ddp_bucket_desc* buckets, const int64_t* bucket_start,
+                                       int32_t nbuckets, const void* const* grads, const uint8_t* used, int32_t ld,
+                                       int32_t W, int32_t mode, int32_t accumulate, float* main_grad,
+                                       int64_t replica_stride, void* const* grads_out, const uint8_t* global_used,
+                                       int32_t wire_dtype, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Step 5: the reducer -- in-order bucket issue on a side stream             */
 /* ------------------------------------------------------------------------ */
@@ -321,8 +370,10 @@ enum {
     DDP_R_COPY_BACK = 2, /* write reduced gradients to grads_out (else main_grad views only) */
     DDP_R_TIMING = 4,    /* record CUDA events around each bucket's kernels (ddp_reducer_bucket_ms) */
     DDP_R_DRY_RUN = 8,   /* schedule only: no CUDA call at all; issues are logged, not launched */
-    DDP_R_COALESCE = 16  /* buckets that become issuable together go out in one launch
+    DDP_R_COALESCE = 16, /* buckets that become issuable together go out in one launch
                             (ddp_fused_bucket_group); needs DDP_R_FUSED */
+    DDP_R_WIRE_BF16 = 32, /* reduce through the bf16 compression hook (ddp_bucket_allreduce_wire) */
+    DDP_R_WIRE_F16 = 64   /* reduce through the fp16 compression hook */
 };
 
 /*

@@ -38,7 +38,7 @@ def build(src: str = SRC, out: str = LIB, extra: tuple = ()) -> str:
     if os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src) and not extra:
         return out
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["cc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", *extra, src, "-o", tmp]
+    cmd = ["cc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", *extra, src, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -58,6 +58,12 @@ class Oracle:
                                     _vpp, C.c_int64]
         lib.oracle_ring_allreduce.restype = C.c_int
         lib.oracle_ring_allreduce.argtypes = [_vpp, C.c_int32, C.c_int64, C.c_int32, _u64p]
+        lib.oracle_ring_allreduce_wire.restype = C.c_int
+        lib.oracle_ring_allreduce_wire.argtypes = [_vpp, C.c_int32, C.c_int64, C.c_int32, C.c_int32, _u64p]
+        lib.oracle_round_wire.restype = C.c_uint16
+        lib.oracle_round_wire.argtypes = [C.c_double, C.c_int32]
+        lib.oracle_wire_value.restype = C.c_double
+        lib.oracle_wire_value.argtypes = [C.c_uint16, C.c_int32]
         lib.oracle_unpack.restype = None
         lib.oracle_unpack.argtypes = [C.c_int32, C.c_int32, _i64p, _i64p, _vpp, C.c_int64, C.c_int32,
                                       _u8p, _vpp]
@@ -143,6 +149,24 @@ class Oracle:
             raise ValueError(f"oracle_ring_allreduce returned {rc}")
         return bufs, sent
 
+    def ring_wire(self, bufs: np.ndarray, mode=ALLREDUCE, wire=BF16):
+        """The compression hook's ring: messages and partial sums in the wire type
+        (bf16 or fp16).  bufs: [W, n] float32, replaced in place."""
+        assert bufs.dtype == np.float32 and bufs.flags.c_contiguous and bufs.ndim == 2
+        W, n = bufs.shape
+        rows = (C.c_void_p * W)(*[bufs[w].ctypes.data for w in range(W)])
+        sent = np.zeros(W, np.uint64)
+        rc = self.lib.oracle_ring_allreduce_wire(rows, W, n, int(mode), int(wire), _p(sent, _u64p))
+        if rc != 0:
+            raise ValueError(f"oracle_ring_allreduce_wire returned {rc}")
+        return bufs, sent
+
+    def round_wire(self, x: float, wire=BF16) -> int:
+        return int(self.lib.oracle_round_wire(float(x), int(wire)))
+
+    def wire_value(self, h: int, wire=BF16) -> float:
+        return float(self.lib.oracle_wire_value(int(h), int(wire)))
+
     # -- unpack -------------------------------------------------------------
     def unpack(self, bucket: np.ndarray, seg_offset, seg_numel, mode=ALLREDUCE, global_used=None, outs=None):
         """bucket: [W, n] fp32. outs: list over replicas of lists over segments (fp32 arrays,
@@ -182,12 +206,13 @@ def load() -> Oracle:
 # ---------------------------------------------------------------------------
 # the whole path over one workload (composition of the four steps above)
 # ---------------------------------------------------------------------------
-def run_workload(wl, orc: Oracle | None = None, grads=None, copy_back: bool = True):
+def run_workload(wl, orc: Oracle | None = None, grads=None, copy_back: bool = True, wire=None):
     """Assign, then for every bucket: pack (accumulating over the workload's
     micro-steps), ring-reduce, unpack.  ``grads[m][w][p]`` may be given (raw
     storage arrays); otherwise they are generated.  Returns a dict with the plan,
     the reduced buckets ``bucket[b]`` ([W, numel]) and, when ``copy_back``, the
-    per-parameter outputs ``out[w][p]`` (None for globally unused parameters)."""
+    per-parameter outputs ``out[w][p]`` (None for globally unused parameters).
+    ``wire`` (BF16 / F16) reduces through the compression hook's ring instead."""
     import workloads as W_
 
     orc = orc or load()
@@ -211,7 +236,7 @@ def run_workload(wl, orc: Oracle | None = None, grads=None, copy_back: bool = Tr
         for m in range(wl.micro_steps):
             gl = [[grads[m][w][p] for p in mem] for w in range(wl.W)]
             buf = orc.pack(gl, offs, nb, [wl.dtype] * len(mem), used[:, mem], accumulate=m > 0, out=buf)
-        buf, s = orc.ring(buf, wl.mode)
+        buf, s = orc.ring(buf, wl.mode) if wire is None else orc.ring_wire(buf, wl.mode, wire)
         buckets.append(buf)
         sent.append(s)
         if copy_back:

@@ -36,8 +36,12 @@
  *     sends chunk (r-s-1) mod W to rank r+1, which adds received + local;
  *     rank r ends the reduce-scatter holding chunk r (Megatron's shard r);
  *   - each rank's contribution is multiplied by fp32(1/W) before the ring;
- *   - reduce_scatter writes only shard r of rank r; the rest is unchanged.
+ *   - reduce_scatter writes only shard r of rank r; the rest is unchanged;
+ *   - a compressed ring (the bf16/fp16 compression hook of [P1 §17.9, §17.20])
+ *     rounds every message and every partial sum to the wire type, to nearest
+ *     with ties to even, and divides by W in the wire type before the ring.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -368,4 +372,140 @@ void oracle_unpack(int32_t W, int32_t nseg, const int64_t* seg_offset, const int
             }
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* 5. compressed ring: the bf16 / fp16 compression hook                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * The hook of [P1 §17.9, §17.20]: the fp32 bucket is converted to the wire
+ * type and divided by the world size (in the wire type), the converted tensor
+ * is allreduced with a sum (every partial sum is a value of the wire type),
+ * and the result is copied back into the fp32 bucket.
+ *
+ * Rounding to a binary format with p significand bits, exponent range
+ * [emin, emax], to nearest with ties to even, written from the format's
+ * definition: scale |x| by the quantum of its binade (or of the subnormal
+ * range), round the integer to nearest even, and encode; a result at or past
+ * 2^(emax+1) becomes infinity.  Inputs are doubles, so every wire value and
+ * every exact sum or quotient of two of them used below is rounded once.
+ */
+static uint16_t encode_rounded(double x, int p, int emin, int emax, int mbits)
+{
+    const int bias = -emin + 1;
+    const uint16_t exp_mask = (uint16_t)(((1u << (15 - mbits)) - 1) << mbits);
+    uint16_t sign = signbit(x) ? (uint16_t)(1u << 15) : 0;
+    if (isnan(x)) return (uint16_t)(exp_mask | (1u << (mbits - 1)));  /* a quiet NaN */
+    double ax = fabs(x);
+    uint16_t inf = sign | exp_mask;
+    if (isinf(ax)) return inf;
+    if (ax == 0.0) return sign;
+    int k;
+    frexp(ax, &k);            /* ax = m * 2^k with m in [0.5, 1): binade exponent k - 1 */
+    int e = k - 1;
+    if (e < emin) e = emin;   /* subnormal range: fixed quantum */
+    double quantum = ldexp(1.0, e - p + 1);
+    double q = rint(ax / quantum);  /* exact scaling by a power of two, then nearest-even */
+    if (q >= ldexp(1.0, p)) {       /* rounded up into the next binade */
+        q = ldexp(1.0, p - 1);
+        e += 1;
+    }
+    if (e > emax) return inf;
+    uint32_t mant = (uint32_t)q;
+    if (mant < (1u << (p - 1))) return sign | (uint16_t)mant;  /* subnormal (exponent field 0) */
+    uint32_t ef = (uint32_t)(e + bias);
+    return sign | (uint16_t)(ef << mbits) | (uint16_t)(mant - (1u << (p - 1)));
+}
+
+static double decode_wire(uint16_t h, int p, int emin, int mbits)
+{
+    const int bias = -emin + 1;
+    int sign = h >> 15;
+    uint32_t ef = (h >> mbits) & ((1u << (15 - mbits)) - 1);
+    uint32_t mant = h & ((1u << mbits) - 1);
+    double v;
+    if (ef == ((1u << (15 - mbits)) - 1)) v = mant ? NAN : INFINITY;
+    else if (ef == 0) v = ldexp((double)mant, emin - p + 1);
+    else v = ldexp((double)(mant | (1u << mbits)), (int)ef - bias - p + 1);
+    return sign ? -v : v;
+}
+
+/* wire formats: bf16 (8-bit significand, exponents -126..127), fp16 (11-bit, -14..15) */
+uint16_t oracle_round_wire(double x, int32_t wire)
+{
+    return wire == DT_BF16 ? encode_rounded(x, 8, -126, 127, 7) : encode_rounded(x, 11, -14, 15, 10);
+}
+
+double oracle_wire_value(uint16_t h, int32_t wire)
+{
+    return wire == DT_BF16 ? decode_wire(h, 8, -126, 7) : decode_wire(h, 11, -14, 10);
+}
+
+/*
+ * Same ring as oracle_ring_allreduce, over wire-typed messages.  bytes_sent
+ * counts 2 bytes per element.  rank_buf is replaced as there (allreduce: all;
+ * reduce_scatter: shard r of rank r) with the widened wire result.
+ */
+int oracle_ring_allreduce_wire(float* const* rank_buf, int32_t W, int64_t n, int32_t mode, int32_t wire,
+                               uint64_t* bytes_sent)
+{
+    if (W < 1 || n < 0 || (wire != DT_BF16 && wire != DT_F16)) return -1;
+    if (mode == MODE_REDUCE_SCATTER && n % W != 0) return -1;
+    for (int32_t r = 0; r < W; r++) bytes_sent[r] = 0;
+    if (n == 0) return 0;
+
+    uint16_t** local = (uint16_t**)malloc(sizeof(uint16_t*) * (size_t)W);
+    uint16_t** msg = (uint16_t**)malloc(sizeof(uint16_t*) * (size_t)W);
+    int64_t maxchunk = (n + W - 1) / W;
+    for (int32_t r = 0; r < W; r++) {
+        local[r] = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n);
+        msg[r] = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)maxchunk);
+        for (int64_t e = 0; e < n; e++) {
+            uint16_t c = oracle_round_wire((double)rank_buf[r][e], wire);              /* compress */
+            local[r][e] = oracle_round_wire(oracle_wire_value(c, wire) / (double)W, wire); /* divide by W */
+        }
+    }
+    for (int32_t s = 0; s < W - 1; s++) {
+        for (int32_t r = 0; r < W; r++) {
+            int32_t c = mod(r - s - 1, W);
+            int64_t b = chunk_begin(n, W, c), e = chunk_end(n, W, c);
+            for (int64_t i = b; i < e; i++) msg[r][i - b] = local[r][i];
+            bytes_sent[r] += (uint64_t)(e - b) * sizeof(uint16_t);
+        }
+        for (int32_t r = 0; r < W; r++) {
+            int32_t from = mod(r - 1, W);
+            int32_t c = mod(from - s - 1, W);
+            int64_t b = chunk_begin(n, W, c), e = chunk_end(n, W, c);
+            for (int64_t i = b; i < e; i++)
+                local[r][i] = oracle_round_wire(oracle_wire_value(msg[from][i - b], wire) +
+                                                    oracle_wire_value(local[r][i], wire), wire);
+        }
+    }
+    if (mode == MODE_ALLREDUCE) {
+        for (int32_t s = 0; s < W - 1; s++) {
+            for (int32_t r = 0; r < W; r++) {
+                int32_t c = mod(r - s, W);
+                int64_t b = chunk_begin(n, W, c), e = chunk_end(n, W, c);
+                for (int64_t i = b; i < e; i++) msg[r][i - b] = local[r][i];
+                bytes_sent[r] += (uint64_t)(e - b) * sizeof(uint16_t);
+            }
+            for (int32_t r = 0; r < W; r++) {
+                int32_t from = mod(r - 1, W);
+                int32_t c = mod(from - s, W);
+                int64_t b = chunk_begin(n, W, c), e = chunk_end(n, W, c);
+                for (int64_t i = b; i < e; i++) local[r][i] = msg[from][i - b];
+            }
+        }
+        for (int32_t r = 0; r < W; r++)
+            for (int64_t e = 0; e < n; e++) rank_buf[r][e] = (float)oracle_wire_value(local[r][e], wire);
+    } else {
+        for (int32_t r = 0; r < W; r++) {
+            int64_t b = chunk_begin(n, W, r), e = chunk_end(n, W, r);
+            for (int64_t i = b; i < e; i++) rank_buf[r][i] = (float)oracle_wire_value(local[r][i], wire);
+        }
+    }
+    for (int32_t r = 0; r < W; r++) { free(local[r]); free(msg[r]); }
+    free(local);
+    free(msg);
+    return 0;
 }

@@ -371,3 +371,107 @@ def pin_unpack_skips_unused_and_shards(orc):
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+# ---------------------------------------------------------------------------
+# compression hook (bf16 / fp16 wire)
+# ---------------------------------------------------------------------------
+BF16_W, F16_W = 1, 2
+
+
+def _rne_fraction(q: Fraction, p: int, emin: int) -> Fraction:
+    """Nearest value with a p-bit significand (exponent >= emin, subnormals below),
+    ties to even, by exact rational arithmetic (no overflow handling)."""
+    if q == 0:
+        return Fraction(0)
+    s = -1 if q < 0 else 1
+    a = abs(q)
+    e = 0
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    quantum = Fraction(2) ** (e - p + 1)
+    k = a // quantum
+    lo, hi = k * quantum, (k + 1) * quantum
+    if a - lo < hi - a or (a - lo == hi - a and k % 2 == 0):
+        return s * lo
+    return s * hi
+
+
+def pin_wire_rounding_f16(orc):
+    """fp16 rounding of doubles: numpy's correctly rounded float64 -> float16."""
+    rng = np.random.default_rng(21)
+    xs = rng.standard_normal(4000) * 10.0 ** rng.integers(-9, 5, 4000)
+    xs = np.concatenate([xs, [65504.0, 65519.99, 5.96e-8, 2.9802322387695312e-08, 1e-9, -0.0, 0.5 + 2 ** -12]])
+    for x in xs:
+        assert orc.round_wire(float(x), F16_W) == int(np.float64(x).astype(np.float16).view(np.uint16)), x
+
+
+def pin_wire_rounding_bf16(orc):
+    """bf16 rounding: of floats, against the upper-half rule with nearest-even carry;
+    of doubles, against exact rational nearest-even."""
+    rng = np.random.default_rng(22)
+    f = (rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000)).astype(np.float32)
+    want = WL.f32_to_bf16_bits_np(f)
+    for x, w in zip(f, want):
+        assert orc.round_wire(float(x), BF16_W) == int(w), x
+    for x in rng.standard_normal(300) * 10.0 ** rng.integers(-5, 5, 300):
+        h = orc.round_wire(float(x), BF16_W)
+        assert Fraction(orc.wire_value(h, BF16_W)) == _rne_fraction(Fraction(float(x)), 8, -126), x
+
+
+def pin_wire_ring_golden(orc):
+    x, exp = ring_fixture("ring_wire_bf16_w4.txt")
+    y, sent = orc.ring_wire(x.copy(), ALLREDUCE, BF16_W)
+    for w in range(4):
+        assert np.array_equal(y[w].view(np.uint32), exp.view(np.uint32)), (w, y[w], exp)
+    assert all(int(s) == 2 * 3 * 2 for s in sent)   # 2(W-1) chunks of one 2-byte element
+
+
+def pin_wire_ring_brute_force(orc):
+    """W = 3 (1/3 is not a power of two, so where the division sits matters) and W = 5:
+    compress, divide, and every ring addition rounded to the wire type, redone with
+    exact rationals in the ring order c+1, ..., c."""
+    rng = np.random.default_rng(23)
+    for wire, p, emin in ((BF16_W, 8, -126), (F16_W, 11, -14)):
+        for W in (3, 5):
+            n = 2 * W
+            x = (rng.standard_normal((W, n)) * 3).astype(np.float32)
+            y, _ = orc.ring_wire(x.copy(), ALLREDUCE, wire)
+            L = -(-n // W)
+            for e in range(n):
+                c = min(e // L, W - 1)
+                z = [_rne_fraction(_rne_fraction(Fraction(float(x[w, e])), p, emin) / W, p, emin) for w in range(W)]
+                s = z[(c + 1) % W]
+                for k in range(2, W + 1):
+                    s = _rne_fraction(s + z[(c + k) % W], p, emin)
+                assert Fraction(float(y[0, e])) == s, (wire, W, e)
+
+
+def pin_wire_w1_rounds(orc):
+    """One rank: the hook still converts to the wire type and back."""
+    x = np.array([[1.0 + 2 ** -9, 3.0, 1e-3, -7.75]], np.float32)
+    y, sent = orc.ring_wire(x.copy(), ALLREDUCE, BF16_W)
+    bf = float(WL.bf16_bits_to_f32_np(WL.f32_to_bf16_bits_np(np.array([1e-3], np.float32)))[0])
+    assert list(y[0]) == [1.0, 3.0, bf, -7.75]
+    assert int(sent[0]) == 0
+
+
+def pin_wire_reduce_scatter_shards(orc):
+    rng = np.random.default_rng(24)
+    W, n = 4, 4 * 9
+    x = rng.standard_normal((W, n)).astype(np.float32)
+    ar, _ = orc.ring_wire(x.copy(), ALLREDUCE, F16_W)
+    rs, sent = orc.ring_wire(x.copy(), REDUCE_SCATTER, F16_W)
+    k = n // W
+    for r in range(W):
+        assert np.array_equal(rs[r, r * k:(r + 1) * k], ar[r, r * k:(r + 1) * k])
+        mask = np.ones(n, bool)
+        mask[r * k:(r + 1) * k] = False
+        assert np.array_equal(rs[r, mask], x[r, mask])
+    assert all(int(s) * W == (W - 1) * 2 * n for s in sent)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -571,3 +571,171 @@ def test_coalesced_reducer_vs_oracle(orc, name):
                     t[:, sel] = packed_at(orc, wl, p, e[sel] - lo, 1)
             assert_bits_equal(got[owner, e], oracle_at(orc, t, owner), f"c3 bucket {b}")
     sess.close()
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 8, 16])
+def test_pack_group_vs_oracle(orc, W, variant):
+    """A no_sync micro-step over several buckets in one call (copy, then accumulate):
+    every bucket equals the oracle's pack."""
+    rng = np.random.default_rng(700 + W)
+    dts = [int(d) for d in rng.choice([D.DDP_F32, D.DDP_F32, D.DDP_BF16, D.DDP_F16], size=5)]
+    bks = [random_bucket(rng, W, dt, int(rng.integers(1, 7)), bool(rng.integers(0, 2))) for dt in dts]
+    starts, pos = [], 0
+    for bk in bks:
+        starts.append(pos)
+        pos += (bk["numel"] + 63) // 64 * 64
+    stride = max(pos, 64)
+    cols = np.cumsum([0] + [bk["nseg"] for bk in bks])
+    ld = int(cols[-1])
+    ptrs = np.zeros(W * ld, np.int64)
+    usedf = np.zeros((W, ld), np.uint8)
+    for i, bk in enumerate(bks):
+        ptrs.reshape(W, ld)[:, cols[i]:cols[i + 1]] = bk["tab"].cpu().numpy().reshape(W, bk["nseg"])
+        usedf[:, cols[i]:cols[i + 1]] = bk["used"]
+        par = torch.arange(cols[i], cols[i + 1], dtype=torch.int32, device=DEV)
+        bk["keep"].append(par)
+        bk["desc"].seg_param = par.data_ptr()
+    tab = torch.from_numpy(ptrs).to(DEV)
+    used_t = torch.from_numpy(usedf.reshape(-1).copy()).to(DEV)
+    init = rng.standard_normal((W, stride)).astype(np.float32)
+    mg = torch.from_numpy(init.copy()).to(DEV)
+    want = init.copy()
+    for accumulate in (0, 1):
+        D.ddp_pack_group([bk["desc"] for bk in bks], starts, tab, used_t, ld, W, mg, stride, accumulate)
+        for i, bk in enumerate(bks):
+            n, s0 = bk["numel"], starts[i]
+            want[:, s0:s0 + n] = oracle_pack(orc, bk, W, dts[i], accumulate, want[:, s0:s0 + n].copy())
+        got = mg.cpu().numpy()
+        for i, bk in enumerate(bks):
+            n, s0 = bk["numel"], starts[i]
+            assert_bits_equal(got[:, s0:s0 + n], want[:, s0:s0 + n], f"bucket {i} accumulate={accumulate}")
+        # nothing outside the buckets was written
+        mask = np.ones(stride, bool)
+        for i, bk in enumerate(bks):
+            mask[starts[i]:starts[i] + bk["numel"]] = False
+        assert_bits_equal(got[:, mask], init[:, mask], "outside the buckets")
+
+
+@pytest.mark.slow
+def test_bert_nosync_coalesced_sampled(orc):
+    """The benchmark's configuration for BERT-large: pack groups for the no_sync
+    micro-steps, coalesced fused issue for the synchronised one."""
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    wl = WL.c4_bert_large()
+    sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                         wl.first_cap_bytes, wl.pad_multiple, device_grads(wl, 3), used=used_flags(wl), coalesce=True)
+    for m in range(3):
+        g = device_grads(wl, m)
+        tab = sess.plan.pointer_table(g)
+        sess.accumulate_local(tab, first=m == 0)
+        torch.cuda.synchronize()
+        del tab, g
+    sess.step(accumulate=True)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(45)
+    plan = sess.plan
+    used = used_flags(wl)
+    for b in range(0, plan.nbuckets, 3):
+        n = int(plan.bucket_numel[b])
+        got = plan.bucket_view(sess.main_grad, b).cpu().numpy()
+        e = _sample(rng, n, 300)
+        t = np.zeros((wl.W, len(e)), np.float32)
+        for p in plan.members[b]:
+            lo, hi = int(plan.offset_of[p]), int(plan.offset_of[p]) + wl.numels[p]
+            sel = np.nonzero((e >= lo) & (e < hi))[0]
+            if len(sel):
+                t[:, sel] = packed_at(orc, wl, p, e[sel] - lo, 4, used[:, p])
+        assert_bits_equal(got[wl.W - 1, e], oracle_at(orc, t, chunk_of(e, n, wl.W)), f"bucket {b}")
+    sess.close()
+
+
+# ---------------------------------------------------------------------------
+# the compression hook (bf16 / fp16 wire)
+# ---------------------------------------------------------------------------
+def assert_wire_equal(got, want, what):
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan), what
+    assert_bits_equal(np.where(nan, 0, got), np.where(nan, 0, want), what)
+
+
+@pytest.mark.parametrize("wire", [D.DDP_BF16, D.DDP_F16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("W,n", [(W, n) for W in (1, 2, 3, 4, 5, 8, 16) for n in (0, 7, 1000, 4099, 65549)])
+def test_allreduce_wire_vs_oracle(orc, W, n, wire, variant):
+    rng = np.random.default_rng(500 * W + n + wire)
+    for mode in (D.DDP_ALLREDUCE, D.DDP_REDUCE_SCATTER):
+        nn = n - n % W if mode == D.DDP_REDUCE_SCATTER else n
+        for misaligned in (False, True):
+            x = (rng.standard_normal((W, nn)) * 10.0 ** rng.integers(-6, 5, (W, nn))).astype(np.float32)
+            if wire == D.DDP_F16 and nn:
+                x[0, 0] = 1e5          # beyond fp16: the hook saturates to infinity
+            stride = max(nn, 1)
+            buf, start = guarded(W * stride, 1 if misaligned else 0)
+            view = buf[start:start + W * stride].view(W, stride)
+            view[:, :nn] = torch.from_numpy(x).to(DEV)
+            D.ddp_bucket_allreduce_wire(buf.data_ptr() + 4 * start, stride, nn, W, mode, wire)
+            want, _ = orc.ring_wire(x.copy(), mode, wire)
+            assert_wire_equal(view[:, :nn].cpu().numpy(), want, f"W={W} n={nn} wire={wire} mode={mode}")
+            check_guards(buf, start, W * stride)
+
+
+@pytest.mark.parametrize("wire", [D.DDP_BF16, D.DDP_F16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("W", [2, 3, 4, 8])
+def test_fused_group_wire_vs_oracle(orc, W, wire, variant):
+    rng = np.random.default_rng(800 + W + 10 * wire)
+    dt = D.DDP_F32
+    bks = [random_bucket(rng, W, dt, int(rng.integers(1, 6)), bool(rng.integers(0, 2))) for _ in range(3)]
+    for mode in (D.DDP_ALLREDUCE, D.DDP_REDUCE_SCATTER):
+        for accumulate in (0, 1):
+            for bk in bks:
+                bk["numel"] += (-bk["numel"]) % W
+                bk["desc"].numel = bk["numel"]
+            starts, pos = [], 0
+            for bk in bks:
+                starts.append(pos)
+                pos += (bk["numel"] + 63) // 64 * 64
+            stride = max(pos, 64)
+            cols = np.cumsum([0] + [bk["nseg"] for bk in bks])
+            ld = int(cols[-1])
+            ptrs = np.zeros(W * ld, np.int64)
+            usedf = np.zeros((W, ld), np.uint8)
+            for i, bk in enumerate(bks):
+                ptrs.reshape(W, ld)[:, cols[i]:cols[i + 1]] = bk["tab"].cpu().numpy().reshape(W, bk["nseg"])
+                usedf[:, cols[i]:cols[i + 1]] = bk["used"]
+                par = torch.arange(cols[i], cols[i + 1], dtype=torch.int32, device=DEV)
+                bk["keep"].append(par)
+                bk["desc"].seg_param = par.data_ptr()
+            tab = torch.from_numpy(ptrs).to(DEV)
+            used_t = torch.from_numpy(usedf.reshape(-1).copy()).to(DEV)
+            init = rng.standard_normal((W, stride)).astype(np.float32)
+            mg = torch.from_numpy(init.copy()).to(DEV)
+            D.ddp_fused_bucket_group_wire([bk["desc"] for bk in bks], starts, tab, used_t, ld, W, mode, accumulate,
+                                          mg, stride, None, None, wire)
+            got = mg.cpu().numpy()
+            for i, bk in enumerate(bks):
+                n, s0 = bk["numel"], starts[i]
+                packed = oracle_pack(orc, bk, W, dt, accumulate, init[:, s0:s0 + n].copy())
+                want, _ = orc.ring_wire(packed.copy(), mode, wire)
+                if mode == D.DDP_ALLREDUCE:
+                    assert_wire_equal(got[:, s0:s0 + n], want, f"bucket {i}")
+                else:
+                    k = n // W
+                    for w in range(W):
+                        assert_wire_equal(got[w, s0 + w * k:s0 + (w + 1) * k], want[w, w * k:(w + 1) * k],
+                                          f"bucket {i} shard {w}")
+
+
+@pytest.mark.parametrize("coalesce", [False, True])
+def test_reducer_bf16_hook_resnet50(orc, coalesce):
+    """ResNet-50 W=8 through the reducer with the bf16 compression hook."""
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    wl = WL.c2_resnet50()
+    sess = BucketReducer(wl.numels, None, wl.W, wl.mode, wl.order, wl.cap_bytes, wl.first_cap_bytes, 1,
+                         device_grads(wl), coalesce=coalesce, wire=D.DDP_BF16)
+    sess.step()
+    torch.cuda.synchronize()
+    ref = O.run_workload(wl, orc, copy_back=False, wire=O.BF16)
+    for b in range(sess.plan.nbuckets):
+        assert_bits_equal(sess.plan.bucket_view(sess.main_grad, b).cpu().numpy(), ref["bucket"][b], f"bucket {b}")
+    sess.close()

@@ -39,6 +39,13 @@ MUTANTS = {
     "f16_bias_wrong": [("u = sign | ((ex + 112) << 23) | (man << 13);", "u = sign | ((ex + 111) << 23) | (man << 13);")],
     "unpack_writes_unused": [("            if (global_used && !global_used[s]) continue;\n", "")],
     "unpack_ignores_shard": [("            lo = chunk_begin(bucket_numel, W, w);\n", "")],
+    "wire_sum_not_rounded": [("                local[r][i] = oracle_round_wire(oracle_wire_value(msg[from][i - b], wire) +\n"
+                              "                                                    oracle_wire_value(local[r][i], wire), wire);",
+                              "                local[r][i] = oracle_round_wire(oracle_wire_value(msg[from][i - b], wire), wire) + 0 * "
+                              "local[r][i];")],
+    "wire_divide_skipped": [("local[r][e] = oracle_round_wire(oracle_wire_value(c, wire) / (double)W, wire);",
+                             "local[r][e] = c;")],
+    "wire_ties_away": [("double q = rint(ax / quantum);", "double q = floor(ax / quantum + 0.5);")],
     "offset_skips_first": [("            offset_of[p] = off;\n            off += numels[p];",
                             "            off += numels[p];\n            offset_of[p] = off - numels[p] + (j > 0);")],
 }
