@@ -49,6 +49,13 @@ _SIGS = {
     "ddp_assign_buckets": (C.c_int32, [_i64p, _i32p, C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_int32,
                                        C.c_int32, _i32p, _i64p, _i32p, _i64p, _i64p, _i32p, _i32p, C.c_int32,
                                        _i32p]),
+    "ddp_assign_buckets_ordered": (C.c_int32, [_i64p, _i32p, C.c_int32, _i32p, C.c_int64, C.c_int64, C.c_int32,
+                                               C.c_int32, _i32p, _i64p, _i32p, _i64p, _i64p, _i32p, _i32p,
+                                               C.c_int32, _i32p]),
+    "ddp_overlap_timeline": (C.c_int32, [C.c_int32, C.POINTER(C.c_double), C.c_int32, _i32p, _i32p, _i64p,
+                                         C.c_double, C.c_double, C.POINTER(C.c_double), C.POINTER(C.c_double),
+                                         C.POINTER(C.c_double), C.POINTER(C.c_double)]),
+    "ddp_reducer_ready_order": (C.c_int32, [_vp, _i32p, C.c_int32, _i32p]),
     "ddp_pack": (C.c_int32, [C.POINTER(BucketDesc), _vp, _vp, C.c_int32, C.c_int32, _vp, C.c_int64, C.c_int32, _vp]),
     "ddp_bucket_allreduce": (C.c_int32, [_vp, C.c_int64, C.c_int64, C.c_int32, C.c_int32, _vp]),
     "ddp_bucket_allreduce_wire": (C.c_int32, [_vp, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int32, _vp]),
@@ -176,6 +183,47 @@ def ddp_assign_buckets(numels, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=
     return out
 
 
+def ddp_assign_buckets_ordered(numels, sequence, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=1 << 20,
+                               pad_multiple=1, grad_reduce_in_fp32=1) -> dict:
+    numels = _a(numels, np.int64)
+    P = len(numels)
+    seq = _a(sequence, np.int32)
+    dtypes = np.zeros(P, np.int32) if dtypes is None else _a(dtypes, np.int32)
+    cap = P + 2
+    out = dict(bucket_of=np.zeros(P, np.int32), offset_of=np.zeros(P, np.int64), members=np.zeros(max(P, 1), np.int32),
+               bucket_numel=np.zeros(cap, np.int64), bucket_bytes=np.zeros(cap, np.int64),
+               bucket_dtype=np.zeros(cap, np.int32), bucket_order=np.zeros(cap, np.int32))
+    nb = C.c_int32(0)
+    _check(lib().ddp_assign_buckets_ordered(_cp(numels, _i64p), _cp(dtypes, _i32p), P, _cp(seq, _i32p),
+                                            int(cap_bytes), int(first_cap_bytes), int(pad_multiple),
+                                            int(grad_reduce_in_fp32), _cp(out["bucket_of"], _i32p),
+                                            _cp(out["offset_of"], _i64p), _cp(out["members"], _i32p),
+                                            _cp(out["bucket_numel"], _i64p), _cp(out["bucket_bytes"], _i64p),
+                                            _cp(out["bucket_dtype"], _i32p), _cp(out["bucket_order"], _i32p), cap,
+                                            C.byref(nb)))
+    B = nb.value
+    for k in ("bucket_numel", "bucket_bytes", "bucket_dtype", "bucket_order"):
+        out[k] = out[k][:B].copy()
+    out["members"] = out["members"][:P].copy()
+    out["nbuckets"] = B
+    return out
+
+
+def ddp_overlap_timeline(ready_ms, bucket_of, bucket_order, bucket_bytes, alpha_ms, ms_per_byte) -> dict:
+    ready = _a(ready_ms, np.float64)
+    bof = _a(bucket_of, np.int32)
+    bord = _a(bucket_order, np.int32)
+    bb = _a(bucket_bytes, np.int64)
+    B = len(bord)
+    start, end = np.zeros(max(B, 1)), np.zeros(max(B, 1))
+    step, serial = C.c_double(0), C.c_double(0)
+    dp = C.POINTER(C.c_double)
+    _check(lib().ddp_overlap_timeline(len(ready), _cp(ready, dp), B, _cp(bof, _i32p), _cp(bord, _i32p),
+                                      _cp(bb, _i64p), float(alpha_ms), float(ms_per_byte), _cp(start, dp),
+                                      _cp(end, dp), C.byref(step), C.byref(serial)))
+    return dict(start_ms=start[:B], end_ms=end[:B], step_ms=step.value, serial_ms=serial.value)
+
+
 # ---------------------------------------------------------------------------
 # steps 2-4
 # ---------------------------------------------------------------------------
@@ -278,6 +326,13 @@ def ddp_reducer_issue_log(r, cap=4096) -> list:
     out = np.zeros(cap, np.int32)
     n = C.c_int32(0)
     _check(lib().ddp_reducer_issue_log(r, _cp(out, _i32p), cap, C.byref(n)))
+    return [int(v) for v in out[:n.value]]
+
+
+def ddp_reducer_ready_order(r, cap=1 << 20) -> list:
+    out = np.zeros(cap, np.int32)
+    n = C.c_int32(0)
+    _check(lib().ddp_reducer_ready_order(r, _cp(out, _i32p), cap, C.byref(n)))
     return [int(v) for v in out[:n.value]]
 
 

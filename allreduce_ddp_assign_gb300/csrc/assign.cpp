@@ -34,14 +34,12 @@ int64_t bytes_per_element(int32_t dtype, bool fp32_buffer)
     return dtype == DDP_F32 ? 4 : 2;
 }
 
-}  // namespace
-
-extern "C" ddp_status ddp_assign_buckets(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
-                                         int64_t cap_bytes, int64_t first_cap_bytes, int32_t order,
-                                         int32_t pad_multiple, int32_t grad_reduce_in_fp32,
-                                         int32_t* bucket_of, int64_t* offset_of, int32_t* members,
-                                         int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
-                                         int32_t* bucket_order, int32_t max_buckets, int32_t* nbuckets)
+// `walk`: the parameters in iteration order (nullptr: derived from `order`).
+ddp_status assign(const int64_t* numels, const int32_t* dtypes, int32_t nparams, const int32_t* walk,
+                  int64_t cap_bytes, int64_t first_cap_bytes, int32_t order, int32_t pad_multiple,
+                  int32_t grad_reduce_in_fp32, int32_t* bucket_of, int64_t* offset_of, int32_t* members,
+                  int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype, int32_t* bucket_order,
+                  int32_t max_buckets, int32_t* nbuckets)
 {
     using ddp::fail;
     if (!nbuckets) return fail(DDP_E_INVAL, "ddp_assign_buckets: nbuckets is NULL");
@@ -76,7 +74,7 @@ extern "C" ddp_status ddp_assign_buckets(const int64_t* numels, const int32_t* d
     };
 
     for (int32_t step = 0; step < nparams; ++step) {
-        const int32_t p = (order == DDP_ORDER_REVERSE) ? (nparams - 1 - step) : step;
+        const int32_t p = walk ? walk[step] : ((order == DDP_ORDER_REVERSE) ? (nparams - 1 - step) : step);
         const int32_t dt = dtypes[p];
         Filling& f = open[dt];
         if (f.first_step < 0) f.first_step = step;
@@ -118,4 +116,45 @@ extern "C" ddp_status ddp_assign_buckets(const int64_t* numels, const int32_t* d
         bucket_order[b] = megatron ? (count - 1 - b) : b;
     }
     return ddp::ok();
+}
+
+}  // namespace
+
+extern "C" ddp_status ddp_assign_buckets(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
+                                         int64_t cap_bytes, int64_t first_cap_bytes, int32_t order,
+                                         int32_t pad_multiple, int32_t grad_reduce_in_fp32,
+                                         int32_t* bucket_of, int64_t* offset_of, int32_t* members,
+                                         int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
+                                         int32_t* bucket_order, int32_t max_buckets, int32_t* nbuckets)
+{
+    return assign(numels, dtypes, nparams, nullptr, cap_bytes, first_cap_bytes, order, pad_multiple,
+                  grad_reduce_in_fp32, bucket_of, offset_of, members, bucket_numel, bucket_bytes, bucket_dtype,
+                  bucket_order, max_buckets, nbuckets);
+}
+
+// Rebuilt buckets over the order the gradients were observed in ("DDP: ring
+// AllReduce and gradient buckets" 17.13): the first gradients to arrive fill
+// bucket 0 under first_cap_bytes, the rest follow under cap_bytes; issue order
+// is bucket index order.
+extern "C" ddp_status ddp_assign_buckets_ordered(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
+                                                 const int32_t* sequence, int64_t cap_bytes, int64_t first_cap_bytes,
+                                                 int32_t pad_multiple, int32_t grad_reduce_in_fp32,
+                                                 int32_t* bucket_of, int64_t* offset_of, int32_t* members,
+                                                 int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
+                                                 int32_t* bucket_order, int32_t max_buckets, int32_t* nbuckets)
+{
+    using ddp::fail;
+    if (nparams > 0 && !sequence) return fail(DDP_E_INVAL, "ddp_assign_buckets_ordered: sequence is NULL");
+    if (nparams > 0) {
+        std::vector<uint8_t> seen(static_cast<size_t>(nparams), 0);
+        for (int32_t k = 0; k < nparams; ++k) {
+            const int32_t p = sequence[k];
+            if (p < 0 || p >= nparams || seen[p])
+                return fail(DDP_E_INVAL, "ddp_assign_buckets_ordered: sequence is not a permutation (position %d)", k);
+            seen[p] = 1;
+        }
+    }
+    return assign(numels, dtypes, nparams, sequence, cap_bytes, first_cap_bytes, DDP_ORDER_REVERSE, pad_multiple,
+                  grad_reduce_in_fp32, bucket_of, offset_of, members, bucket_numel, bucket_bytes, bucket_dtype,
+                  bucket_order, max_buckets, nbuckets);
 }

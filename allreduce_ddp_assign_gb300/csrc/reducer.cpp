@@ -69,6 +69,12 @@ struct ddp_reducer {
     bool timing_valid = false;
     std::vector<ddp_bucket_desc> group_descs;  // scratch for coalesced issue
     std::vector<float*> group_mgs;
+    std::vector<int32_t> seq_now, seq_last;        // gradient-ready order: this iteration, last finalized one
+    std::vector<std::vector<cudaEvent_t>> gates;  // per bucket: the events its issue waits for
+    std::vector<int32_t> batch_done;               // buckets completed in the current batch of marks
+    std::vector<cudaStream_t> batch_streams;
+    std::vector<cudaEvent_t> batch_events;
+    std::vector<cudaEvent_t> waited;
 
     bool dry() const { return flags & DDP_R_DRY_RUN; }
 
@@ -116,10 +122,16 @@ struct ddp_reducer {
         for (int32_t i = 0; i < count; ++i) log.push_back(order[pos + i]);
         if (dry()) return DDP_OK;
         ddp_status st = DDP_OK;
+        // wait once for every distinct gating event of the buckets going out
+        waited.clear();
         for (int32_t i = 0; i < count; ++i) {
-            const int32_t b = order[pos + i];
-            for (size_t j = 0; j < producers[b].size(); ++j)
-                if (!cuda_ok(cudaStreamWaitEvent(side, ready[b][j], 0), "cudaStreamWaitEvent", &st)) return st;
+            for (cudaEvent_t e : gates[order[pos + i]]) {
+                bool seen = false;
+                for (cudaEvent_t x : waited) seen = seen || x == e;
+                if (seen) continue;
+                waited.push_back(e);
+                if (!cuda_ok(cudaStreamWaitEvent(side, e, 0), "cudaStreamWaitEvent", &st)) return st;
+            }
         }
         const bool timing = flags & DDP_R_TIMING;
         if (count > 1) {
@@ -152,20 +164,63 @@ struct ddp_reducer {
         return DDP_OK;
     }
 
-    // Record the events that gate bucket b (its gradients' producers).
-    ddp_status bucket_ready(int32_t b)
+    ddp_status ensure_events(int32_t b)
     {
-        if (!dry()) {
-            ddp_status st = DDP_OK;
-            auto& evs = ready[b];
-            while (evs.size() < producers[b].size()) {
-                cudaEvent_t e = nullptr;
-                if (!cuda_ok(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate", &st)) return st;
-                evs.push_back(e);
-            }
-            for (size_t i = 0; i < producers[b].size(); ++i)
-                if (!cuda_ok(cudaEventRecord(evs[i], producers[b][i]), "cudaEventRecord", &st)) return st;
+        ddp_status st = DDP_OK;
+        auto& evs = ready[b];
+        while (evs.size() < producers[b].size()) {
+            cudaEvent_t e = nullptr;
+            if (!cuda_ok(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate", &st)) return st;
+            evs.push_back(e);
         }
+        return DDP_OK;
+    }
+
+    // Bucket b's count reached zero: record the events that gate it (one per
+    // stream that produced its gradients).  With `defer` the recording waits for
+    // the end of the batch (gate_batch), which records one event per stream for
+    // every bucket the batch completed.
+    ddp_status bucket_ready(int32_t b, bool defer)
+    {
+        if (dry()) return DDP_OK;
+        if (defer) {
+            batch_done.push_back(b);
+            return DDP_OK;
+        }
+        ddp_status st = ensure_events(b);
+        if (st != DDP_OK) return st;
+        gates[b].clear();
+        for (size_t i = 0; i < producers[b].size(); ++i) {
+            if (!cuda_ok(cudaEventRecord(ready[b][i], producers[b][i]), "cudaEventRecord", &st)) return st;
+            gates[b].push_back(ready[b][i]);
+        }
+        return DDP_OK;
+    }
+
+    // End of a batch of marks: one event per producer stream gates all the buckets
+    // the batch completed (events on one stream are ordered, so the last suffices).
+    ddp_status gate_batch()
+    {
+        if (dry() || batch_done.empty()) return DDP_OK;
+        ddp_status st = DDP_OK;
+        batch_streams.clear();
+        batch_events.clear();
+        for (int32_t b : batch_done) {
+            if ((st = ensure_events(b)) != DDP_OK) return st;
+            gates[b].clear();
+            for (size_t i = 0; i < producers[b].size(); ++i) {
+                const cudaStream_t s = producers[b][i];
+                size_t j = 0;
+                while (j < batch_streams.size() && batch_streams[j] != s) ++j;
+                if (j == batch_streams.size()) {  // first bucket of the batch on this stream: record its event
+                    if (!cuda_ok(cudaEventRecord(ready[b][i], s), "cudaEventRecord", &st)) return st;
+                    batch_streams.push_back(s);
+                    batch_events.push_back(ready[b][i]);
+                }
+                gates[b].push_back(batch_events[j]);
+            }
+        }
+        batch_done.clear();
         return DDP_OK;
     }
 
@@ -282,6 +337,7 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
     r->marked.assign(nparams, 0);
     r->producers.resize(nbuckets);
     r->ready.resize(nbuckets);
+    r->gates.resize(nbuckets);
 
     if (!dry) {
         ddp_status st = DDP_OK;
@@ -323,8 +379,11 @@ extern "C" ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate)
     for (int32_t b = 0; b < r->nbuckets; ++b) {
         r->pending[b] = r->bucket_params[b];
         r->producers[b].clear();
+        r->gates[b].clear();
     }
+    r->batch_done.clear();
     std::fill(r->marked.begin(), r->marked.end(), 0);
+    r->seq_now.clear();
     r->next = 0;
     r->log.clear();
     r->accumulate = accumulate != 0;
@@ -347,6 +406,7 @@ ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool d
         return ddp::fail(DDP_E_STATE, "ddp_reducer_mark_ready: parameter %d was marked ready twice in one iteration",
                          param);
     r->marked[param] = 1;
+    r->seq_now.push_back(param);
     const int32_t b = r->bucket_of[param];
     if (!r->dry()) {
         auto& ps = r->producers[b];
@@ -356,7 +416,7 @@ ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool d
         if (!have) ps.push_back(s);
     }
     if (--r->pending[b] == 0) {
-        ddp_status st = r->bucket_ready(b);
+        ddp_status st = r->bucket_ready(b, defer);
         if (st == DDP_OK && !defer) st = r->issue_ready();
         if (st != DDP_OK) return st;
     }
@@ -378,7 +438,8 @@ extern "C" ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t*
     for (int32_t i = 0; i < n && st == DDP_OK; ++i) st = mark_one(r, params[i], producer_stream, true);
     // one issue pass for everything the list completed (coalesced when enabled),
     // also after a failure so that the parameters already marked are not stranded
-    const ddp_status st2 = r ? r->issue_ready() : DDP_OK;
+    ddp_status st2 = r ? r->gate_batch() : DDP_OK;
+    if (st2 == DDP_OK && r) st2 = r->issue_ready();
     if (st != DDP_OK) return st;
     return st2 == DDP_OK ? ddp::ok() : st2;
 }
@@ -401,6 +462,7 @@ extern "C" ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream
         }
         r->phase = Phase::Finalized;
         r->timing_valid = (r->flags & DDP_R_TIMING) != 0;
+        r->seq_last = r->seq_now;
     }
     if (timeout_us > 0 && !r->dry()) {
         const auto deadline = std::chrono::steady_clock::now() + std::chrono::microseconds(timeout_us);
@@ -424,6 +486,16 @@ extern "C" ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, 
     if (cap < *n || (!out && *n > 0))
         return ddp::fail(DDP_E_CAPACITY, "ddp_reducer_issue_log: %d entries, room for %d", *n, cap);
     for (int32_t i = 0; i < *n; ++i) out[i] = r->log[i];
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_ready_order(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n)
+{
+    if (!r || !n) return ddp::fail(DDP_E_INVAL, "ddp_reducer_ready_order: NULL argument");
+    *n = static_cast<int32_t>(r->seq_last.size());
+    if (*n == 0) return ddp::fail(DDP_E_STATE, "ddp_reducer_ready_order: no finalized iteration");
+    if (cap < *n || !out) return ddp::fail(DDP_E_CAPACITY, "ddp_reducer_ready_order: %d entries, room for %d", *n, cap);
+    for (int32_t i = 0; i < *n; ++i) out[i] = r->seq_last[i];
     return ddp::ok();
 }
 

@@ -582,6 +582,112 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_overlap(args, wl=None):
+    """The reducer's overlap with a synthetic backward ("Lecture 15: PyTorch DDP" 3.1):
+    the compute stream runs one bounded spin kernel per parameter, in reverse order,
+    with a length proportional to the parameter, and marks it ready; buckets go out on
+    the side stream as they fill.  Measured: backward alone, reduction alone, the
+    overlapped step, the serial step.  Predicted: ddp_overlap_timeline from the
+    recorded ready times and per-bucket times.  One JSON line."""
+    import torch
+
+    import allreduce_ddp_assign_gb300 as D
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    wl = wl or WL.c2_resnet50()
+    dev = torch.device("cuda", 0)
+    D.lib()
+    grads = [[WL.grad_torch(wl, p, w, 0, dev) for p in range(wl.nparams)] for w in range(wl.W)]
+    sess = BucketReducer(wl.numels, None, wl.W, wl.mode, wl.order, wl.cap_bytes, wl.first_cap_bytes,
+                         wl.pad_multiple, grads, timing=True)
+    comp = torch.cuda.current_stream()
+    # calibrate the spin kernel: cycles per millisecond at the clock it actually runs at
+    probe = 2_000_000
+    for _ in range(3):
+        torch.cuda._sleep(probe)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(torch.cuda.current_stream())
+    torch.cuda._sleep(probe)
+    e1.record(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    clock_hz = probe / (e0.elapsed_time(e1) * 1e-3)
+    total = sum(wl.numels)
+    bwd_ms = args.backward_ms
+    cycles = [max(1000, int(bwd_ms * 1e-3 * clock_hz * n / total)) for n in wl.numels]
+    order = list(range(wl.nparams - 1, -1, -1))
+
+    def backward(mark: bool, evs=None):
+        for i, p in enumerate(order):
+            torch.cuda._sleep(cycles[p])
+            if evs is not None:
+                evs[i].record(comp)
+            if mark:
+                D.ddp_reducer_mark_ready(sess.handle, p, comp)
+
+    def timed(fn, reps=5):
+        out = []
+        for r in range(reps + 2):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(comp)
+            fn()
+            b.record(comp)
+            torch.cuda.synchronize()
+            if r >= 2:
+                out.append(a.elapsed_time(b))
+        return float(np.median(out))
+
+    t_bwd = timed(lambda: backward(False))
+
+    def reduce_only():
+        D.ddp_reducer_prepare(sess.handle, 0)
+        D.ddp_reducer_mark_ready_many(sess.handle, order, comp)
+        D.ddp_reducer_finalize(sess.handle, comp, 0)
+
+    t_red = timed(reduce_only)
+    per_bucket_ms = [float(x) for x in sess.bucket_ms()]
+
+    def overlapped():
+        D.ddp_reducer_prepare(sess.handle, 0)
+        backward(True)
+        D.ddp_reducer_finalize(sess.handle, comp, 0)
+
+    t_ovl = timed(overlapped)
+
+    def serial():
+        backward(False)
+        reduce_only()
+
+    t_ser = timed(serial)
+    # ready times of one overlapped step, for the model
+    evs = [torch.cuda.Event(enable_timing=True) for _ in order]
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    a.record(comp)
+    D.ddp_reducer_prepare(sess.handle, 0)
+    backward(True, evs)
+    D.ddp_reducer_finalize(sess.handle, comp, 0)
+    torch.cuda.synchronize()
+    ready = np.zeros(wl.nparams)
+    for i, p in enumerate(order):
+        ready[p] = a.elapsed_time(evs[i])
+    plan = sess.plan
+    nbytes = np.array([2 * wl.W * 4 * int(plan.bucket_numel[b]) for b in range(plan.nbuckets)], np.float64)
+    slope, icpt = np.polyfit(nbytes, np.array(per_bucket_ms), 1)
+    model = D.ddp_overlap_timeline(ready, plan.bucket_of, plan.bucket_order, nbytes.astype(np.int64),
+                                   max(float(icpt), 0.0), max(float(slope), 0.0))
+    line = {"overlap": True, "workload": wl.name, "backward_ms": round(t_bwd, 4), "reduce_ms": round(t_red, 4),
+            "overlapped_step_ms": round(t_ovl, 4), "serial_step_ms": round(t_ser, 4),
+            "exposed_ms": round(t_ovl - t_bwd, 4), "hidden_fraction": round(1 - (t_ovl - t_bwd) / t_red, 4),
+            "model": {"alpha_ms": round(max(float(icpt), 0.0), 5), "ms_per_GB": round(max(float(slope), 0.0) * 1e9, 5),
+                      "step_ms": round(model["step_ms"], 4), "serial_ms": round(model["serial_ms"], 4)},
+            "per_bucket_ms": [round(x, 4) for x in per_bucket_ms],
+            "bucket_ready_ms": [round(float(max(ready[p] for p in plan.members[b])), 4) for b in range(plan.nbuckets)]}
+    print(json.dumps(line), flush=True)
+    sess.close()
+    return line
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,9 +701,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--sweep", action="store_true", help="bandwidth sweep of ddp_bucket_allreduce (JSON per point)")
     ap.add_argument("--sweep-max-bytes", type=int, default=0)
+    ap.add_argument("--overlap", action="store_true", help="overlap with a synthetic backward (JSON line)")
+    ap.add_argument("--backward-ms", type=float, default=3.0)
     args = ap.parse_args(argv)
     if args.sweep:
         return run_sweep(args)
+    if args.overlap:
+        return run_overlap(args)
     wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, wl)

@@ -129,6 +129,47 @@ ddp_status ddp_assign_buckets(const int64_t* numels, const int32_t* dtypes, int3
                               int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
                               int32_t* bucket_order, int32_t max_buckets, int32_t* nbuckets);
 
+/*
+ * ddp_assign_buckets_ordered -- rebuilt buckets: the same rule as
+ * ddp_assign_buckets, walking the parameters in `sequence` (the order their
+ * gradients were observed in; see ddp_reducer_ready_order).
+ *
+ * Defined by: DDP chapter 17.13 (the first backward records the order
+ * gradients arrive in; the next forward re-buckets in that order, the earliest
+ * gradients into bucket 0 under the 1 MiB first cap, the rest under
+ * bucket_cap_mb).  Issue order is bucket index order (bucket_order[k] = k).
+ * Each dtype group keeps its own cap sequence, as in ddp_assign_buckets.
+ *
+ * HOST in: sequence[nparams], a permutation of 0..nparams-1; the rest and the
+ * outputs as ddp_assign_buckets (without `order`).
+ * Errors: as ddp_assign_buckets; DDP_E_INVAL if sequence is not a permutation.
+ */
+ddp_status ddp_assign_buckets_ordered(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
+                                      const int32_t* sequence, int64_t cap_bytes, int64_t first_cap_bytes,
+                                      int32_t pad_multiple, int32_t grad_reduce_in_fp32, int32_t* bucket_of,
+                                      int64_t* offset_of, int32_t* members, int64_t* bucket_numel,
+                                      int64_t* bucket_bytes, int32_t* bucket_dtype, int32_t* bucket_order,
+                                      int32_t max_buckets, int32_t* nbuckets);
+
+/*
+ * ddp_overlap_timeline -- the overlap model of the lecture (section 3.1,
+ * exercises 4 and 5), on the host.  Gradient p appears at ready_ms[p]; bucket
+ * b (of bucket_bytes[b] bytes) is reduced as soon as its last gradient exists
+ * and the bucket issued before it (bucket_order) is done, taking
+ * alpha_ms + ms_per_byte * bucket_bytes[b].  (A ring over K ranks with latency
+ * alpha and bandwidth beta: alpha_ms = 2(K-1)alpha, ms_per_byte = 2(K-1)/(K beta).)
+ *
+ * HOST out: start_ms[b], end_ms[b] (indexed by bucket id); *step_ms = when the
+ * gradients and every reduction are done; *serial_ms = the step without
+ * overlap (every reduction after the last gradient).
+ * Errors: DDP_E_INVAL (NULL array, negative size or cost, bucket_of out of
+ * range, bucket_order not a permutation).
+ */
+ddp_status ddp_overlap_timeline(int32_t nparams, const double* ready_ms, int32_t nbuckets, const int32_t* bucket_of,
+                                const int32_t* bucket_order, const int64_t* bucket_bytes, double alpha_ms,
+                                double ms_per_byte, double* start_ms, double* end_ms, double* step_ms,
+                                double* serial_ms);
+
 /* ------------------------------------------------------------------------ */
 /* Bucket descriptor used by the device steps                                */
 /* ------------------------------------------------------------------------ */
@@ -448,6 +489,14 @@ ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream, int64_t t
 
 /* Buckets issued in this iteration, in issue order (HOST out[cap]); *n = count. */
 ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n);
+
+/*
+ * ddp_reducer_ready_order -- the order in which the last finalized iteration
+ * marked its parameters ready (the gradient-ready order DDP records for the
+ * bucket rebuild, DDP chapter 17.13).  HOST out[cap]; *n = nparams marked.
+ * Errors: DDP_E_STATE if no iteration was finalized; DDP_E_CAPACITY.
+ */
+ddp_status ddp_reducer_ready_order(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n);
 
 /*
  * Per-bucket GPU time in milliseconds of the last finalized iteration (needs

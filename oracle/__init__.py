@@ -53,6 +53,14 @@ class Oracle:
         lib.oracle_assign.argtypes = [_i64p, _i32p, C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                       C.c_int32, C.c_int32, _i32p, _i64p, _i64p, _i64p, _i32p,
                                       _i32p, _i32p, C.c_int32, _i32p]
+        lib.oracle_assign_sequence.restype = C.c_int
+        lib.oracle_assign_sequence.argtypes = [_i64p, _i32p, C.c_int32, _i32p, C.c_int64, C.c_int64, C.c_int32,
+                                               C.c_int32, _i32p, _i64p, _i64p, _i64p, _i32p, _i32p, _i32p,
+                                               C.c_int32, _i32p]
+        _dp = C.POINTER(C.c_double)
+        lib.oracle_overlap_timeline.restype = C.c_int
+        lib.oracle_overlap_timeline.argtypes = [C.c_int32, _dp, C.c_int32, _i32p, _i32p, _i64p, C.c_double,
+                                                C.c_double, _dp, _dp, _dp, _dp]
         lib.oracle_pack.restype = None
         lib.oracle_pack.argtypes = [C.c_int32, C.c_int32, _i64p, _i64p, _i32p, _vpp, _u8p, C.c_int32,
                                     _vpp, C.c_int64]
@@ -98,6 +106,58 @@ class Oracle:
         return dict(bucket_of=bucket_of, offset_of=offset_of, bucket_numel=bn[:B].copy(),
                     bucket_bytes=bb[:B].copy(), bucket_dtype=bd[:B].copy(), bucket_order=bo[:B].copy(),
                     members=members, nbuckets=B)
+
+    def assign_sequence(self, numels, sequence, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=1 << 20,
+                        pad_multiple=1, grad_reduce_in_fp32=1) -> dict:
+        """Rebuilt buckets over an observed gradient-ready order."""
+        numels = np.ascontiguousarray(numels, dtype=np.int64)
+        P = len(numels)
+        seq = np.ascontiguousarray(sequence, dtype=np.int32)
+        dtypes = np.zeros(P, np.int32) if dtypes is None else np.ascontiguousarray(dtypes, dtype=np.int32)
+        out = self._assign_out(P)
+        nb = C.c_int32(0)
+        rc = self.lib.oracle_assign_sequence(_p(numels, _i64p), _p(dtypes, _i32p), P, _p(seq, _i32p),
+                                             int(cap_bytes), int(first_cap_bytes), int(pad_multiple),
+                                             int(grad_reduce_in_fp32), *out["ptrs"], out["cap"], C.byref(nb))
+        if rc != 0:
+            raise ValueError(f"oracle_assign_sequence returned {rc}")
+        return self._assign_result(out, nb.value, P)
+
+    def _assign_out(self, P):
+        cap = P + 3
+        arrs = dict(bucket_of=np.full(P, -1, np.int32), offset_of=np.full(P, -1, np.int64),
+                    bucket_numel=np.zeros(cap, np.int64), bucket_bytes=np.zeros(cap, np.int64),
+                    bucket_dtype=np.zeros(cap, np.int32), bucket_order=np.zeros(cap, np.int32),
+                    mem=np.zeros(max(P, 1), np.int32))
+        ptrs = [_p(arrs["bucket_of"], _i32p), _p(arrs["offset_of"], _i64p), _p(arrs["bucket_numel"], _i64p),
+                _p(arrs["bucket_bytes"], _i64p), _p(arrs["bucket_dtype"], _i32p), _p(arrs["bucket_order"], _i32p),
+                _p(arrs["mem"], _i32p)]
+        return dict(arrs=arrs, ptrs=ptrs, cap=cap)
+
+    def _assign_result(self, out, B, P):
+        a = out["arrs"]
+        members = [[] for _ in range(B)]
+        for p in a["mem"][:P]:
+            members[a["bucket_of"][p]].append(int(p))
+        return dict(bucket_of=a["bucket_of"], offset_of=a["offset_of"], bucket_numel=a["bucket_numel"][:B].copy(),
+                    bucket_bytes=a["bucket_bytes"][:B].copy(), bucket_dtype=a["bucket_dtype"][:B].copy(),
+                    bucket_order=a["bucket_order"][:B].copy(), members=members, nbuckets=B)
+
+    def overlap_timeline(self, ready_ms, bucket_of, bucket_order, bucket_bytes, alpha_ms, ms_per_byte) -> dict:
+        ready = np.ascontiguousarray(ready_ms, dtype=np.float64)
+        bof = np.ascontiguousarray(bucket_of, dtype=np.int32)
+        bord = np.ascontiguousarray(bucket_order, dtype=np.int32)
+        bb = np.ascontiguousarray(bucket_bytes, dtype=np.int64)
+        B = len(bord)
+        start, end = np.zeros(max(B, 1)), np.zeros(max(B, 1))
+        step, serial = C.c_double(0), C.c_double(0)
+        _dp = C.POINTER(C.c_double)
+        rc = self.lib.oracle_overlap_timeline(len(ready), _p(ready, _dp), B, _p(bof, _i32p), _p(bord, _i32p),
+                                              _p(bb, _i64p), float(alpha_ms), float(ms_per_byte), _p(start, _dp),
+                                              _p(end, _dp), C.byref(step), C.byref(serial))
+        if rc != 0:
+            raise ValueError(f"oracle_overlap_timeline returned {rc}")
+        return dict(start_ms=start[:B], end_ms=end[:B], step_ms=step.value, serial_ms=serial.value)
 
     # -- pack ---------------------------------------------------------------
     def pack(self, grads, seg_offset, bucket_numel, seg_dtype=None, used=None, accumulate=False,

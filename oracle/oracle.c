@@ -115,6 +115,14 @@ static float load_as_f32(const void* p, int32_t dt, int64_t i)
  *   members[nparams]: the parameters of bucket 0 in layout order, then bucket 1's, ...
  * Returns 0, or -1 on bad arguments, -2 if more than max_buckets are needed.
  */
+static int assign_impl(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
+                       int64_t cap_bytes, int64_t first_cap_bytes, int32_t order, const int32_t* given,
+                       int32_t pad_multiple, int32_t grad_reduce_in_fp32,
+                       int32_t* bucket_of, int64_t* offset_of,
+                       int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
+                       int32_t* bucket_order, int32_t* members_out, int32_t max_buckets,
+                       int32_t* nbuckets);
+
 int oracle_assign(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
                   int64_t cap_bytes, int64_t first_cap_bytes, int32_t order,
                   int32_t pad_multiple, int32_t grad_reduce_in_fp32,
@@ -123,13 +131,52 @@ int oracle_assign(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
                   int32_t* bucket_order, int32_t* members_out, int32_t max_buckets,
                   int32_t* nbuckets)
 {
-    if (nparams < 0 || cap_bytes <= 0 || first_cap_bytes <= 0 || pad_multiple < 1) return -1;
     if (order < ORDER_REVERSE || order > ORDER_MEGATRON) return -1;
+    return assign_impl(numels, dtypes, nparams, cap_bytes, first_cap_bytes, order, NULL, pad_multiple,
+                       grad_reduce_in_fp32, bucket_of, offset_of, bucket_numel, bucket_bytes, bucket_dtype,
+                       bucket_order, members_out, max_buckets, nbuckets);
+}
 
-    /* iteration order */
+/*
+ * Rebuilt buckets [P1 §17.13]: the order in which the first backward produced
+ * the gradients is recorded, and the next forward re-buckets the parameters in
+ * that order -- the earliest gradients into bucket 0 under the 1 MiB first cap,
+ * the rest under bucket_cap_mb -- issued 0, 1, 2, ...  `sequence` is that
+ * recorded order (a permutation of 0..nparams-1).
+ */
+int oracle_assign_sequence(const int64_t* numels, const int32_t* dtypes, int32_t nparams, const int32_t* sequence,
+                           int64_t cap_bytes, int64_t first_cap_bytes, int32_t pad_multiple,
+                           int32_t grad_reduce_in_fp32, int32_t* bucket_of, int64_t* offset_of,
+                           int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
+                           int32_t* bucket_order, int32_t* members_out, int32_t max_buckets, int32_t* nbuckets)
+{
+    if (nparams < 0 || (nparams > 0 && !sequence)) return -1;
+    /* the sequence must name every parameter once */
+    uint8_t* seen = (uint8_t*)calloc((size_t)(nparams > 0 ? nparams : 1), 1);
+    for (int32_t k = 0; k < nparams; k++) {
+        if (sequence[k] < 0 || sequence[k] >= nparams || seen[sequence[k]]) { free(seen); return -1; }
+        seen[sequence[k]] = 1;
+    }
+    free(seen);
+    return assign_impl(numels, dtypes, nparams, cap_bytes, first_cap_bytes, ORDER_REVERSE, sequence, pad_multiple,
+                       grad_reduce_in_fp32, bucket_of, offset_of, bucket_numel, bucket_bytes, bucket_dtype,
+                       bucket_order, members_out, max_buckets, nbuckets);
+}
+
+static int assign_impl(const int64_t* numels, const int32_t* dtypes, int32_t nparams,
+                       int64_t cap_bytes, int64_t first_cap_bytes, int32_t order, const int32_t* given,
+                       int32_t pad_multiple, int32_t grad_reduce_in_fp32,
+                       int32_t* bucket_of, int64_t* offset_of,
+                       int64_t* bucket_numel, int64_t* bucket_bytes, int32_t* bucket_dtype,
+                       int32_t* bucket_order, int32_t* members_out, int32_t max_buckets,
+                       int32_t* nbuckets)
+{
+    if (nparams < 0 || cap_bytes <= 0 || first_cap_bytes <= 0 || pad_multiple < 1) return -1;
+
+    /* iteration order: the given sequence, reversed parameters, or forward parameters */
     int32_t* seq = (int32_t*)malloc(sizeof(int32_t) * (size_t)(nparams > 0 ? nparams : 1));
     for (int32_t k = 0; k < nparams; k++)
-        seq[k] = (order == ORDER_REVERSE) ? nparams - 1 - k : k;
+        seq[k] = given ? given[k] : ((order == ORDER_REVERSE) ? nparams - 1 - k : k);
 
     /* per-dtype open bucket: its members in append order, bytes, caps used */
     int32_t* open_list[3];
@@ -507,5 +554,43 @@ int oracle_ring_allreduce_wire(float* const* rank_buf, int32_t W, int64_t n, int
     for (int32_t r = 0; r < W; r++) { free(local[r]); free(msg[r]); }
     free(local);
     free(msg);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 6. overlap timeline (the lecture's alpha-beta model)                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * [P2 §3.1, exercises 4 and 5]: one compute stream produces the gradients
+ * (parameter p at ready_ms[p]); one communication stream reduces the buckets
+ * one at a time in issue order, each as soon as its last gradient exists and
+ * the previous bucket is done; a bucket of n bytes takes alpha_ms +
+ * ms_per_byte * n.  Outputs per bucket (indexed by bucket id): start_ms,
+ * end_ms; step_ms = when both streams are done; serial_ms = the step with no
+ * overlap (all communication after the last gradient).
+ */
+int oracle_overlap_timeline(int32_t nparams, const double* ready_ms, int32_t nbuckets, const int32_t* bucket_of,
+                            const int32_t* bucket_order, const int64_t* bucket_bytes, double alpha_ms,
+                            double ms_per_byte, double* start_ms, double* end_ms, double* step_ms,
+                            double* serial_ms)
+{
+    if (nparams < 0 || nbuckets < 0) return -1;
+    double backward_end = 0.0;
+    for (int32_t p = 0; p < nparams; p++)
+        if (ready_ms[p] > backward_end) backward_end = ready_ms[p];
+    double comm_total = 0.0, comm_free = 0.0;
+    for (int32_t k = 0; k < nbuckets; k++) {
+        int32_t b = bucket_order[k];
+        double ready = 0.0;
+        for (int32_t p = 0; p < nparams; p++)
+            if (bucket_of[p] == b && ready_ms[p] > ready) ready = ready_ms[p];
+        double t = alpha_ms + ms_per_byte * (double)bucket_bytes[b];
+        start_ms[b] = ready > comm_free ? ready : comm_free;
+        end_ms[b] = start_ms[b] + t;
+        comm_free = end_ms[b];
+        comm_total += t;
+    }
+    *step_ms = comm_free > backward_end ? comm_free : backward_end;
+    *serial_ms = backward_end + comm_total;
     return 0;
 }

@@ -475,3 +475,88 @@ def pin_wire_reduce_scatter_shards(orc):
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+# ---------------------------------------------------------------------------
+# rebuilt buckets and the overlap timeline
+# ---------------------------------------------------------------------------
+def _exercise3_plan(orc, single=False):
+    g = read_golden("lecture15_exercise3.txt")
+    MB = 10 ** 6
+    n = [mb * MB // 4 for mb in g["param_mb"]]
+    cap = (10 ** 12) if single else g["cap_mb"][0] * MB
+    return orc.assign(n, cap_bytes=cap, first_cap_bytes=cap, order=REVERSE)
+
+
+def pin_timeline_exercise4(orc):
+    g = read_golden("lecture15_exercise4.txt")
+    r = _exercise3_plan(orc)
+    ready = [t / 10 for t in g["ready_tenths_p0_p1_p2_p3_p4"]]
+    t = orc.overlap_timeline(ready, r["bucket_of"], r["bucket_order"], r["bucket_bytes"], g["alpha_tenths"][0] / 10,
+                             0.1 / 10 ** 6)
+    assert [round(x * 10) for x in t["start_ms"]] == g["bucket_start_tenths"]
+    assert [round(x * 10) for x in t["end_ms"]] == g["bucket_end_tenths"]
+    assert round(t["step_ms"] * 10) == g["step_tenths"][0]
+    assert round(t["serial_ms"] * 10) == g["serial_tenths"][0]
+    one = _exercise3_plan(orc, single=True)
+    t1 = orc.overlap_timeline(ready, one["bucket_of"], one["bucket_order"], one["bucket_bytes"],
+                              g["alpha_tenths"][0] / 10, 0.1 / 10 ** 6)
+    assert one["nbuckets"] == 1 and round(t1["step_ms"] * 10) == g["single_bucket_step_tenths"][0]
+
+
+def pin_timeline_properties(orc):
+    """The step lies between the backward alone and the serial step; with free
+    communication it equals the backward; the last bucket issued cannot start before
+    its last gradient ("the last bucket is always exposed", Lecture 15 section 3.1)."""
+    rng = np.random.default_rng(31)
+    for trial in range(100):
+        P = int(rng.integers(1, 15))
+        n = [int(v) for v in rng.integers(1, 50, P)]
+        r = orc.assign(n, cap_bytes=int(rng.integers(4, 200)), first_cap_bytes=int(rng.integers(4, 200)))
+        ready = np.sort(rng.random(P) * 10)[::-1].copy()   # backward: last parameter first
+        a, b = float(rng.random()), float(rng.random()) * 0.05
+        t = orc.overlap_timeline(ready, r["bucket_of"], r["bucket_order"], r["bucket_bytes"], a, b)
+        assert ready.max() - 1e-12 <= t["step_ms"] <= t["serial_ms"] + 1e-9
+        last = r["bucket_order"][-1]
+        assert t["start_ms"][last] >= max(ready[p] for p in range(P) if r["bucket_of"][p] == last) - 1e-12
+        z = orc.overlap_timeline(ready, r["bucket_of"], r["bucket_order"], r["bucket_bytes"], 0.0, 0.0)
+        assert abs(z["step_ms"] - ready.max()) < 1e-12
+
+
+def pin_rebuild_linear12(orc):
+    """Gradients observed in exactly reversed parameter order: the rebuilt buckets are the
+    printed ones (DDP chapter 17.13)."""
+    g = read_golden("linear12_bucket_bytes.txt")
+    n = WL.numels(WL.linear12())
+    r = orc.assign_sequence(n, list(range(len(n) - 1, -1, -1)), cap_bytes=g["cap_bytes"][0],
+                            first_cap_bytes=g["first_cap_bytes"][0])
+    assert list(r["bucket_bytes"]) == g["rebuilt_bucket_bytes"]
+    assert sorted(r["members"][0]) == g["rebuilt_bucket0_params"]
+    assert list(r["bucket_order"]) == [0, 1, 2]
+
+
+def pin_rebuild_characterised(orc):
+    """Any observed order: buckets are consecutive runs of the sequence (per dtype) that
+    close on reaching the cap, the first under the first cap."""
+    rng = np.random.default_rng(32)
+    for trial in range(200):
+        P = int(rng.integers(1, 14))
+        numels = [int(v) for v in rng.integers(0, 40, P)]
+        dtypes = [int(v) for v in rng.integers(0, 2, P)] if trial % 2 else [0] * P
+        seq = [int(v) for v in rng.permutation(P)]
+        cap, first = int(rng.integers(1, 120)), int(rng.integers(1, 120))
+        r = orc.assign_sequence(numels, seq, dtypes, cap, first, 1, 1)
+        pos = {p: k for k, p in enumerate(seq)}
+        for g in sorted(set(dtypes)):
+            gb = sorted((m for m in r["members"] if dtypes[m[0]] == g), key=lambda m: pos[m[0]])
+            assert [p for m in gb for p in m] == [p for p in seq if dtypes[p] == g]
+            for k, m in enumerate(gb):
+                c = first if k == 0 else cap
+                by = sum(numels[p] * 4 for p in m)
+                if k < len(gb) - 1:
+                    assert by >= c and by - numels[m[-1]] * 4 < c
+                else:
+                    assert by - numels[m[-1]] * 4 < c
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

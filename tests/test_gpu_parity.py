@@ -739,3 +739,17 @@ def test_reducer_bf16_hook_resnet50(orc, coalesce):
     for b in range(sess.plan.nbuckets):
         assert_bits_equal(sess.plan.bucket_view(sess.main_grad, b).cpu().numpy(), ref["bucket"][b], f"bucket {b}")
     sess.close()
+
+
+def test_overlap_hides_reduction():
+    """With a synthetic backward of about 3 ms, the reductions run on the side stream while
+    it proceeds: the overlapped step is shorter than the serial one, and the model's
+    prediction from the recorded ready times lands near the measured step."""
+    import argparse
+
+    import bench
+
+    line = bench.run_overlap(argparse.Namespace(backward_ms=3.0))
+    assert line["overlapped_step_ms"] < line["serial_step_ms"]
+    assert line["overlapped_step_ms"] >= line["backward_ms"] * 0.98
+    assert abs(line["model"]["step_ms"] - line["overlapped_step_ms"]) < 0.25 * line["overlapped_step_ms"]

@@ -43,3 +43,38 @@ def test_random(orc):
         pad = int(rng.integers(1, 9))
         fp32 = int(rng.integers(0, 2))
         same(D.ddp_assign_buckets(n, dt, cap, first, order, pad, fp32), orc.assign(n, dt, cap, first, order, pad, fp32))
+
+
+def test_ordered_assignment_vs_oracle(orc):
+    rng = np.random.default_rng(4)
+    for trial in range(300):
+        P = int(rng.integers(0, 30))
+        n = rng.integers(0, 5000, size=P)
+        dt = rng.integers(0, 3, size=P) if trial % 3 else np.zeros(P, np.int64)
+        seq = rng.permutation(P)
+        cap, first = int(rng.integers(1, 20000)), int(rng.integers(1, 20000))
+        pad, fp32 = int(rng.integers(1, 9)), int(rng.integers(0, 2))
+        same(D.ddp_assign_buckets_ordered(n, seq, dt, cap, first, pad, fp32),
+             orc.assign_sequence(n, seq, dt, cap, first, pad, fp32))
+
+
+def test_ordered_assignment_rejects_non_permutation():
+    with pytest.raises(D.DdpError):
+        D.ddp_assign_buckets_ordered([1, 2, 3], [0, 0, 1])
+    with pytest.raises(D.DdpError):
+        D.ddp_assign_buckets_ordered([1, 2, 3], [0, 1, 3])
+
+
+def test_overlap_timeline_vs_oracle(orc):
+    rng = np.random.default_rng(6)
+    for trial in range(200):
+        P = int(rng.integers(1, 40))
+        n = rng.integers(1, 10 ** 6, P)
+        r = D.ddp_assign_buckets(n, None, int(rng.integers(10 ** 5, 10 ** 7)), int(rng.integers(10 ** 4, 10 ** 6)),
+                                 int(rng.integers(0, 3)))
+        ready = rng.random(P) * 20
+        a, b = float(rng.random()), float(rng.random()) * 1e-6
+        got = D.ddp_overlap_timeline(ready, r["bucket_of"], r["bucket_order"], r["bucket_bytes"], a, b)
+        want = orc.overlap_timeline(ready, r["bucket_of"], r["bucket_order"], r["bucket_bytes"], a, b)
+        assert np.array_equal(got["start_ms"], want["start_ms"]) and np.array_equal(got["end_ms"], want["end_ms"])
+        assert got["step_ms"] == want["step_ms"] and got["serial_ms"] == want["serial_ms"]

@@ -46,6 +46,9 @@ MUTANTS = {
     "wire_divide_skipped": [("local[r][e] = oracle_round_wire(oracle_wire_value(c, wire) / (double)W, wire);",
                              "local[r][e] = c;")],
     "wire_ties_away": [("double q = rint(ax / quantum);", "double q = floor(ax / quantum + 0.5);")],
+    "timeline_ignores_readiness": [("start_ms[b] = ready > comm_free ? ready : comm_free;", "start_ms[b] = comm_free;")],
+    "timeline_serial_without_backward": [("*serial_ms = backward_end + comm_total;", "*serial_ms = comm_total;")],
+    "rebuild_ignores_sequence": [("seq[k] = given ? given[k] :", "seq[k] = 0 ? given[k] :")],
     "offset_skips_first": [("            offset_of[p] = off;\n            off += numels[p];",
                             "            off += numels[p];\n            offset_of[p] = off - numels[p] + (j > 0);")],
 }

@@ -165,3 +165,21 @@ def test_mark_many_stops_at_the_duplicate_but_issues_completed_buckets():
     assert D.ddp_reducer_issue_log(r) == [0, 1]
     D.ddp_reducer_finalize(r)
     D.ddp_reducer_destroy(r)
+
+
+def test_ready_order_recorded_for_rebuild():
+    """The reducer keeps the order gradients arrived in; re-bucketing over it puts the
+    first arrivals in bucket 0 (DDP chapter 17.13)."""
+    r = make([0, 0, 1, 1, 2])
+    with pytest.raises(D.DdpError) as e:
+        D.ddp_reducer_ready_order(r)
+    assert e.value.status == D.DDP_E_STATE
+    D.ddp_reducer_prepare(r)
+    order = [4, 2, 3, 0, 1]
+    for p in order:
+        D.ddp_reducer_mark_ready(r, p)
+    D.ddp_reducer_finalize(r)
+    assert D.ddp_reducer_ready_order(r) == order
+    plan = D.ddp_assign_buckets_ordered([10, 10, 10, 10, 10], order, None, 80, 40)
+    assert [int(p) for p in plan["members"]][:1] == [4]
+    D.ddp_reducer_destroy(r)
