@@ -72,6 +72,8 @@ class Oracle:
         lib.oracle_round_wire.argtypes = [C.c_double, C.c_int32]
         lib.oracle_wire_value.restype = C.c_double
         lib.oracle_wire_value.argtypes = [C.c_uint16, C.c_int32]
+        lib.oracle_used_allreduce.restype = C.c_int
+        lib.oracle_used_allreduce.argtypes = [C.c_int32, C.c_int32, _u8p, _i32p, _u8p]
         lib.oracle_unpack.restype = None
         lib.oracle_unpack.argtypes = [C.c_int32, C.c_int32, _i64p, _i64p, _vpp, C.c_int64, C.c_int32,
                                       _u8p, _vpp]
@@ -227,6 +229,20 @@ class Oracle:
     def wire_value(self, h: int, wire=BF16) -> float:
         return float(self.lib.oracle_wire_value(int(h), int(wire)))
 
+    # -- local-used bitmap ---------------------------------------------------
+    def used_allreduce(self, local_used) -> tuple:
+        """local_used [W, P] (nonzero = used) -> (global_count int32[P], global_used uint8[P])."""
+        lu = np.ascontiguousarray(np.asarray(local_used, np.uint8))
+        if lu.ndim != 2:
+            raise ValueError("local_used must be [W, P]")
+        W, P = lu.shape
+        count = np.zeros(max(P, 1), np.int32)
+        glob = np.zeros(max(P, 1), np.uint8)
+        rc = self.lib.oracle_used_allreduce(W, P, _p(lu, _u8p), _p(count, _i32p), _p(glob, _u8p))
+        if rc != 0:
+            raise ValueError("oracle_used_allreduce rejected its arguments")
+        return count[:P], glob[:P]
+
     # -- unpack -------------------------------------------------------------
     def unpack(self, bucket: np.ndarray, seg_offset, seg_numel, mode=ALLREDUCE, global_used=None, outs=None):
         """bucket: [W, n] fp32. outs: list over replicas of lists over segments (fp32 arrays,
@@ -282,10 +298,8 @@ def run_workload(wl, orc: Oracle | None = None, grads=None, copy_back: bool = Tr
     if grads is None:
         grads = [[[W_.grad_raw_np(wl, p, w, m) for p in range(P)] for w in range(wl.W)]
                  for m in range(wl.micro_steps)]
-    used = np.ones((wl.W, P), np.uint8)
-    for p in wl.unused:
-        used[:, p] = 0
-    global_used = used.max(axis=0)
+    used = W_.local_used_np(wl)
+    global_used = orc.used_allreduce(used)[1]
     buckets, sent = [], []
     out = [[None] * P for _ in range(wl.W)]
     for b in range(plan["nbuckets"]):

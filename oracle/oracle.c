@@ -22,6 +22,10 @@
  *        main_grad buffer and max(40MB, 1MB x DP) buckets, §3 start_grad_sync
  *        (all_reduce or reduce_scatter with rank r keeping shard r, scaling by
  *        1/DP before the collective).
+ *   [P4] "DDP: PyTorch Distributed-Experiences on Accelerating Data Parallel
+ *        Training" (a summary of the DDP paper): §2.2 unused parameters and
+ *        the global bitmap, §3.2 the bitmap kept on the host, copied to the
+ *        device and all-reduced once per iteration.
  *
  * Readings taken where the pages leave a step open (each is a parameter or a
  * documented convention):
@@ -419,6 +423,40 @@ void oracle_unpack(int32_t W, int32_t nseg, const int64_t* seg_offset, const int
             }
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* 4b. the local-used bitmap all-reduce                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * [P2 §4.2], [P4 §2.2, §3.2]: every rank records, one integer per parameter of
+ * the whole model, whether it used the parameter this iteration (1) or not
+ * (0), and the ranks sum these bitmaps in one extra all-reduce.  A parameter
+ * whose sum is 0 was used by no rank: it is globally unused and its .grad is
+ * left alone; any other parameter is reduced as usual, the ranks that did not
+ * use it contributing zeros.  A sum of integers does not depend on the order
+ * of its additions, so the ring's order is not reproduced here; every rank
+ * ends with the same sums, written once.
+ *
+ * local_used[w * nparams + p]: rank w's byte for p, nonzero meaning used.
+ * global_count[p]  (may be NULL): number of ranks that used p.
+ * global_used[p]   (may be NULL): 1 if at least one rank used p, else 0.
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_used_allreduce(int32_t W, int32_t nparams, const uint8_t* local_used, int32_t* global_count,
+                          uint8_t* global_used)
+{
+    if (W < 1 || nparams < 0 || (nparams > 0 && !local_used)) return -1;
+    for (int32_t p = 0; p < nparams; p++) {
+        int32_t sum = 0;
+        for (int32_t w = 0; w < W; w++) {
+            int32_t bit = local_used[(int64_t)w * nparams + p] != 0 ? 1 : 0;
+            sum += bit;
+        }
+        if (global_count) global_count[p] = sum;
+        if (global_used) global_used[p] = sum > 0 ? 1 : 0;
+    }
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -560,3 +560,58 @@ def pin_rebuild_characterised(orc):
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+# ---------------------------------------------------------------------------
+# the local-used bitmap (find_unused_parameters)
+# ---------------------------------------------------------------------------
+def pin_bitmap_lecture_two_ranks(orc):
+    """Lecture 15 section 4.2, two processes: a parameter that only rank 0 used is still
+    all-reduced, rank 1 contributing zero, so rank 0 ends with exactly half of its own
+    gradient; a parameter no rank used keeps its .grad untouched; one both used is the
+    plain mean.  Parameters a (both), b (rank 0 only), c (neither)."""
+    local = np.array([[1, 1, 0], [1, 0, 0]], np.uint8)
+    count, glob = orc.used_allreduce(local)
+    assert list(count) == [2, 1, 0] and list(glob) == [1, 1, 0]
+    a = [np.array([0.5, -1.25], np.float32), np.array([1.5, 0.25], np.float32)]
+    b0 = np.array([3.0, -0.75, 1e-3], np.float32)
+    c = np.array([9.0], np.float32)
+    grads = [[a[0], b0, c], [a[1], np.full(3, 123.0, np.float32), c]]
+    offs, sizes = [0, 2, 5], [2, 3, 1]
+    buf = orc.pack(grads, offs, 6, used=local)
+    buf, _ = orc.ring(buf, ALLREDUCE)
+    outs = [[np.full(k, -7.0, np.float32) for k in sizes] for _ in range(2)]
+    orc.unpack(buf, offs, sizes, ALLREDUCE, global_used=glob, outs=outs)
+    for w in range(2):
+        assert list(outs[w][0]) == [1.0, -0.5]
+        assert np.array_equal(outs[w][1], b0 / np.float32(2))
+        assert list(outs[w][2]) == [-7.0]
+
+
+def pin_bitmap_library(orc):
+    """Against numpy's count_nonzero / any over the replica axis, with nonzero bytes
+    other than 1 (any nonzero byte marks use), W from 1 to 64, ragged P, P = 0."""
+    rng = np.random.default_rng(41)
+    for W, P in [(1, 7), (2, 1), (3, 33), (4, 391), (8, 161), (16, 5), (64, 70), (5, 0)]:
+        vals = np.array([0, 0, 0, 1, 1, 2, 0x80, 0xFF], np.uint8)
+        local = vals[rng.integers(0, len(vals), (W, P))]
+        count, glob = orc.used_allreduce(local)
+        assert np.array_equal(count, np.count_nonzero(local, axis=0).astype(np.int32))
+        assert np.array_equal(glob, np.any(local != 0, axis=0).astype(np.uint8))
+
+
+def pin_bitmap_replica_symmetry(orc):
+    """The all-reduce treats the ranks alike: permuting them changes nothing; the count
+    lies in [0, W] and equals W exactly where every rank used the parameter."""
+    rng = np.random.default_rng(42)
+    W, P = 6, 50
+    local = (rng.random((W, P)) < 0.6).astype(np.uint8)
+    count, glob = orc.used_allreduce(local)
+    for perm in ([5, 4, 3, 2, 1, 0], [1, 2, 3, 4, 5, 0]):
+        c2, g2 = orc.used_allreduce(local[perm])
+        assert np.array_equal(c2, count) and np.array_equal(g2, glob)
+    assert count.min() >= 0 and count.max() <= W
+    assert np.array_equal(count == W, local.all(axis=0))
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -49,6 +49,12 @@ MUTANTS = {
     "timeline_ignores_readiness": [("start_ms[b] = ready > comm_free ? ready : comm_free;", "start_ms[b] = comm_free;")],
     "timeline_serial_without_backward": [("*serial_ms = backward_end + comm_total;", "*serial_ms = comm_total;")],
     "rebuild_ignores_sequence": [("seq[k] = given ? given[k] :", "seq[k] = 0 ? given[k] :")],
+    "bitmap_or_as_and": [("global_used[p] = sum > 0 ? 1 : 0;", "global_used[p] = sum == W ? 1 : 0;")],
+    "bitmap_skips_last_replica": [("for (int32_t w = 0; w < W; w++) {\n            int32_t bit",
+                                   "for (int32_t w = 0; w < W - 1; w++) {\n            int32_t bit")],
+    "bitmap_counts_raw_bytes": [("int32_t bit = local_used[(int64_t)w * nparams + p] != 0 ? 1 : 0;",
+                                 "int32_t bit = local_used[(int64_t)w * nparams + p];")],
+    "bitmap_transposed_index": [("local_used[(int64_t)w * nparams + p] != 0", "local_used[(int64_t)p * W + w] != 0")],
     "offset_skips_first": [("            offset_of[p] = off;\n            off += numels[p];",
                             "            off += numels[p];\n            offset_of[p] = off - numels[p] + (j > 0);")],
 }

@@ -249,6 +249,7 @@ class Workload:
     micro_steps: int = 1       # > 1: no_sync accumulation of this many micro-steps
     unused: list = field(default_factory=list)   # params unused on every replica
     grad_reduce_in_fp32: int = 1
+    partial_unused: float = 0.0  # seeded fraction of the other (replica, param) pairs left unused
 
     @property
     def numels(self) -> list[int]:
@@ -286,6 +287,18 @@ def c4_bert_large(unused_layer: int = 11) -> Workload:
                     unused=list(range(first, first + BERT_LAYER_PARAMS)))
 
 
+def c6_bert_find_unused() -> Workload:
+    """BERT-large, W = 4: encoder layer 11 unused by every replica and, as with experts
+    that receive no tokens on some ranks, 5% of the other (replica, parameter) pairs
+    unused locally -- the find_unused_parameters case."""
+    wl = c4_bert_large()
+    wl.name = "bert_large_w4_find_unused_allreduce"
+    wl.micro_steps = 1
+    wl.seed = 1006
+    wl.partial_unused = 0.05
+    return wl
+
+
 def c5_sweep_points() -> list[tuple[int, int]]:
     """(bucket bytes, W) of the bandwidth sweep: 1 KiB .. 1 GiB in powers of 4, W in {2, 4, 8, 16}."""
     return [(1024 * 4 ** k, W) for k in range(11) for W in (2, 4, 8, 16)]
@@ -297,7 +310,24 @@ def c5_bucket(nbytes: int, W: int) -> Workload:
                     F32, "uniform", 1.0, 1005)
 
 
-ALL = {"c1": c1_mlp, "c2": c2_resnet50, "c3": c3_gpt2, "c4": c4_bert_large}
+ALL = {"c1": c1_mlp, "c2": c2_resnet50, "c3": c3_gpt2, "c4": c4_bert_large, "c6": c6_bert_find_unused}
+
+USED_MAP_STREAM = 1 << 40   # generator stream of the local-used bitmaps (beyond every gradient stream)
+
+
+def local_used_np(wl: Workload) -> np.ndarray:
+    """[W, P] uint8 local-used bitmap of one iteration: 0 on every replica for the
+    parameters in ``wl.unused``; 0 for the seeded fraction ``wl.partial_unused`` of
+    the remaining (replica, parameter) pairs; 1 elsewhere."""
+    W, P = wl.W, wl.nparams
+    used = np.ones((W, P), np.uint8)
+    if wl.partial_unused > 0 and P > 0:
+        r = bits_np(stream_key(wl.seed, USED_MAP_STREAM), 0, W * P) >> np.uint64(11)
+        u = r.astype(np.float64) * 2.0 ** -53
+        used[(u < wl.partial_unused).reshape(W, P)] = 0
+    if wl.unused:
+        used[:, list(wl.unused)] = 0
+    return used
 
 
 # ---------------------------------------------------------------------------
