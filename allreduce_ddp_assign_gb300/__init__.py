@@ -74,6 +74,9 @@ _SIGS = {
                                        C.c_int32, C.c_int32, _vp, _vp, C.c_int32, _vp, C.c_int64, _vp, _vp, _vp,
                                        C.POINTER(_vp)]),
     "ddp_reducer_prepare": (C.c_int32, [_vp, C.c_int32]),
+    "ddp_used_allreduce": (C.c_int32, [_vp, C.c_int32, C.c_int32, C.c_int32, _vp, _vp, _vp]),
+    "ddp_reducer_find_unused": (C.c_int32, [_vp, _vp, _vp, _vp]),
+    "ddp_reducer_set_local_used": (C.c_int32, [_vp, _vp, C.c_int32]),
     "ddp_reducer_mark_ready": (C.c_int32, [_vp, C.c_int32, _vp]),
     "ddp_reducer_mark_ready_many": (C.c_int32, [_vp, _i32p, C.c_int32, _vp]),
     "ddp_reducer_finalize": (C.c_int32, [_vp, _vp, C.c_int64]),
@@ -303,6 +306,23 @@ def ddp_reducer_create(nparams, bucket_of, bucket_order, descs, bucket_start, W,
                                     int(ld), _ptr(main_grad), int(replica_stride), _ptr(grads_out), _ptr(global_used),
                                     side, C.byref(h)))
     return h.value
+
+
+def ddp_used_allreduce(local_used, ld, W, nparams, global_count=None, global_used=None, stream=None) -> None:
+    _check(lib().ddp_used_allreduce(_ptr(local_used), int(ld), int(W), int(nparams), _ptr(global_count),
+                                    _ptr(global_used), _stream(stream)))
+
+
+def ddp_reducer_find_unused(r, local_used, global_used, global_count=None) -> None:
+    _check(lib().ddp_reducer_find_unused(r, _ptr(local_used), _ptr(global_used), _ptr(global_count)))
+
+
+def ddp_reducer_set_local_used(r, flags, ld=None) -> None:
+    """flags: host uint8 array [W, >= nparams] (nonzero = replica w used parameter p)."""
+    f = np.ascontiguousarray(np.asarray(flags), dtype=np.uint8)
+    if f.ndim != 2:
+        raise ValueError("flags must be [W, nparams]")
+    _check(lib().ddp_reducer_set_local_used(r, f.ctypes.data_as(_vp), int(f.shape[1] if ld is None else ld)))
 
 
 def ddp_reducer_prepare(r, accumulate=0) -> None:

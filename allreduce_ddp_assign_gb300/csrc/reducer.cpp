@@ -16,6 +16,12 @@
 // side stream waits for those events and the bucket's kernels are launched on
 // it.  Finalize records one event on the side stream and makes the consumer
 // wait for it; with a timeout it also polls that event on the host.
+//
+// find_unused_parameters ("Lecture 15: PyTorch DDP" section 4.2; "DDP: PyTorch
+// Distributed-Experiences on Accelerating Data Parallel Training" sections 2.2
+// and 3.2): the local-used bitmap lives in pinned host memory; prepare copies
+// it to the device and runs the bitmap all-reduce on the side stream ahead of
+// every bucket, and marks ready on the host the parameters no replica used.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -76,7 +82,21 @@ struct ddp_reducer {
     std::vector<cudaEvent_t> batch_events;
     std::vector<cudaEvent_t> waited;
 
+    // find_unused_parameters
+    bool find_unused = false;
+    uint8_t* fu_local = nullptr;     // DEVICE W x ld: the copied local-used bitmap
+    uint8_t* fu_global = nullptr;    // DEVICE nparams: the all-reduced flags
+    int32_t* fu_count = nullptr;     // DEVICE nparams or null: the all-reduced counts
+    uint8_t* fu_host = nullptr;      // HOST W x nparams, pinned (dry-run: fu_host_dry)
+    std::vector<uint8_t> fu_host_dry;
+    cudaEvent_t fu_copied = nullptr; // the last host-to-device copy of the bitmap has been read
+    bool fu_copy_pending = false;
+
     bool dry() const { return flags & DDP_R_DRY_RUN; }
+    uint8_t* host_bitmap() { return dry() ? fu_host_dry.data() : fu_host; }
+    // flags the packs read (replica w used p) and the ones unpack reads (anyone used p)
+    const uint8_t* pack_used() const { return used ? used : (find_unused ? fu_local : nullptr); }
+    const uint8_t* unpack_used() const { return find_unused ? fu_global : global_used; }
 
     std::string unmarked_list() const
     {
@@ -106,12 +126,12 @@ struct ddp_reducer {
         void* st = static_cast<void*>(side);
         const bool copy_back = flags & DDP_R_COPY_BACK;
         if (flags & DDP_R_FUSED)
-            return ddp::launch_fused(d, grads, used, ld, W, mode, accumulate, mgb, stride,
-                                     copy_back ? grads_out : nullptr, global_used, st, wire());
-        ddp_status s = ddp::launch_pack(d, grads, used, ld, W, mgb, stride, accumulate, st);
+            return ddp::launch_fused(d, grads, pack_used(), ld, W, mode, accumulate, mgb, stride,
+                                     copy_back ? grads_out : nullptr, unpack_used(), st, wire());
+        ddp_status s = ddp::launch_pack(d, grads, pack_used(), ld, W, mgb, stride, accumulate, st);
         if (s == DDP_OK) s = ddp::launch_allreduce(mgb, stride, d.numel, W, mode, st, wire());
         if (s == DDP_OK && copy_back)
-            s = ddp::launch_unpack(d, mgb, stride, W, mode, grads_out, ld, global_used, st);
+            s = ddp::launch_unpack(d, mgb, stride, W, mode, grads_out, ld, unpack_used(), st);
         return s;
     }
 
@@ -145,9 +165,9 @@ struct ddp_reducer {
                 group_descs.push_back(buckets[b]);
                 group_mgs.push_back(mg ? mg + start[b] : nullptr);
             }
-            st = ddp::launch_fused_group(group_descs.data(), group_mgs.data(), count, grads, used, ld, W, mode,
-                                         accumulate, stride, (flags & DDP_R_COPY_BACK) ? grads_out : nullptr,
-                                         global_used, static_cast<void*>(side), wire());
+            st = ddp::launch_fused_group(group_descs.data(), group_mgs.data(), count, grads, pack_used(), ld, W,
+                                         mode, accumulate, stride, (flags & DDP_R_COPY_BACK) ? grads_out : nullptr,
+                                         unpack_used(), static_cast<void*>(side), wire());
             if (st != DDP_OK) return st;
             if (timing)
                 for (int32_t i = 0; i < count; ++i)
@@ -240,6 +260,8 @@ struct ddp_reducer {
         return DDP_OK;
     }
 
+    ddp_status start_find_unused();
+
     void destroy_events()
     {
         if (dry()) return;
@@ -248,6 +270,8 @@ struct ddp_reducer {
         for (cudaEvent_t e : t_begin) cudaEventDestroy(e);
         for (cudaEvent_t e : t_end) cudaEventDestroy(e);
         if (done) cudaEventDestroy(done);
+        if (fu_copied) cudaEventDestroy(fu_copied);
+        if (fu_host) cudaFreeHost(fu_host);
     }
 };
 
@@ -388,13 +412,18 @@ extern "C" ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate)
     r->log.clear();
     r->accumulate = accumulate != 0;
     r->phase = Phase::Backward;
+    if (r->find_unused) {
+        const ddp_status s2 = r->start_find_unused();
+        if (s2 != DDP_OK) return s2;
+    }
     return st == DDP_OK ? ddp::ok() : st;
 }
 
 namespace {
 
-// Mark one parameter; with defer the issue pass is left to the caller.
-ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool defer)
+// Mark one parameter; with defer the issue pass is left to the caller.  A
+// parameter marked without a producer (has_producer false) gates nothing.
+ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool defer, bool has_producer)
 {
     if (!r) return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready: reducer is NULL");
     if (param < 0 || param >= r->nparams)
@@ -408,7 +437,7 @@ ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool d
     r->marked[param] = 1;
     r->seq_now.push_back(param);
     const int32_t b = r->bucket_of[param];
-    if (!r->dry()) {
+    if (!r->dry() && has_producer) {
         auto& ps = r->producers[b];
         const cudaStream_t s = static_cast<cudaStream_t>(producer_stream);
         bool have = false;
@@ -425,9 +454,95 @@ ddp_status mark_one(ddp_reducer* r, int32_t param, void* producer_stream, bool d
 
 }  // namespace
 
+// prepare's find_unused steps: copy the host bitmap to the device and all-reduce
+// it on the side stream (ahead of every bucket of the iteration), then mark
+// ready, without a producer, every parameter no replica used.
+ddp_status ddp_reducer::start_find_unused()
+{
+    ddp_status st = DDP_OK;
+    const uint8_t* host = host_bitmap();
+    if (!dry() && nparams > 0) {
+        if (!cuda_ok(cudaMemcpy2DAsync(fu_local, static_cast<size_t>(ld), host, static_cast<size_t>(nparams),
+                                       static_cast<size_t>(nparams), static_cast<size_t>(W), cudaMemcpyHostToDevice,
+                                       side),
+                     "cudaMemcpy2DAsync", &st))
+            return st;
+        if (!cuda_ok(cudaEventRecord(fu_copied, side), "cudaEventRecord", &st)) return st;
+        fu_copy_pending = true;
+        st = ddp_used_allreduce(fu_local, ld, W, nparams, fu_count, fu_global, static_cast<void*>(side));
+        if (st != DDP_OK) return st;
+    }
+    for (int32_t p = 0; p < nparams && st == DDP_OK; ++p) {
+        bool any = false;
+        for (int32_t w = 0; w < W && !any; ++w) any = host[static_cast<int64_t>(w) * nparams + p] != 0;
+        if (!any) st = mark_one(this, p, nullptr, true, false);
+    }
+    const ddp_status s2 = gate_batch();
+    if (st != DDP_OK) return st;
+    if (s2 != DDP_OK) return s2;
+    return issue_ready();
+}
+
+extern "C" ddp_status ddp_reducer_find_unused(ddp_reducer* r, uint8_t* local_used, uint8_t* global_used,
+                                              int32_t* global_count)
+{
+    using ddp::fail;
+    const char* fn = "ddp_reducer_find_unused";
+    if (!r) return fail(DDP_E_INVAL, "%s: reducer is NULL", fn);
+    if (r->phase == Phase::Backward) return fail(DDP_E_STATE, "%s: called inside an iteration", fn);
+    if (r->find_unused) return fail(DDP_E_STATE, "%s: already on", fn);
+    if (r->global_used)
+        return fail(DDP_E_INVAL, "%s: the reducer was created with its own global_used flags", fn);
+    const size_t bytes = static_cast<size_t>(r->W) * static_cast<size_t>(r->nparams);
+    if (r->dry()) {
+        r->fu_host_dry.assign(bytes > 0 ? bytes : 1, 1);
+    } else {
+        if (r->nparams > 0 && (!local_used || !global_used))
+            return fail(DDP_E_INVAL, "%s: local_used or global_used is NULL", fn);
+        if (r->ld < r->nparams) return fail(DDP_E_INVAL, "%s: ld = %d < nparams = %d", fn, r->ld, r->nparams);
+        ddp_status st = DDP_OK;
+        if (!cuda_ok(cudaEventCreateWithFlags(&r->fu_copied, cudaEventDisableTiming), "cudaEventCreate", &st))
+            return st;
+        void* h = nullptr;
+        if (!cuda_ok(cudaHostAlloc(&h, bytes > 0 ? bytes : 1, cudaHostAllocDefault), "cudaHostAlloc", &st)) {
+            cudaEventDestroy(r->fu_copied);
+            r->fu_copied = nullptr;
+            return st;
+        }
+        r->fu_host = static_cast<uint8_t*>(h);
+        std::fill(r->fu_host, r->fu_host + bytes, static_cast<uint8_t>(1));
+    }
+    r->fu_local = local_used;
+    r->fu_global = global_used;
+    r->fu_count = global_count;
+    r->find_unused = true;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_set_local_used(ddp_reducer* r, const uint8_t* flags, int32_t ld)
+{
+    using ddp::fail;
+    const char* fn = "ddp_reducer_set_local_used";
+    if (!r) return fail(DDP_E_INVAL, "%s: reducer is NULL", fn);
+    if (!r->find_unused) return fail(DDP_E_STATE, "%s: find_unused is off (call ddp_reducer_find_unused)", fn);
+    if (r->phase == Phase::Backward) return fail(DDP_E_STATE, "%s: called inside an iteration", fn);
+    if (r->nparams > 0 && !flags) return fail(DDP_E_INVAL, "%s: flags is NULL", fn);
+    if (ld < r->nparams) return fail(DDP_E_INVAL, "%s: ld = %d < nparams = %d", fn, ld, r->nparams);
+    ddp_status st = DDP_OK;
+    if (r->fu_copy_pending) {
+        if (!cuda_ok(cudaEventSynchronize(r->fu_copied), "cudaEventSynchronize", &st)) return st;
+        r->fu_copy_pending = false;
+    }
+    uint8_t* host = r->host_bitmap();
+    for (int32_t w = 0; w < r->W; ++w)
+        for (int32_t p = 0; p < r->nparams; ++p)
+            host[static_cast<int64_t>(w) * r->nparams + p] = flags[static_cast<int64_t>(w) * ld + p] != 0;
+    return ddp::ok();
+}
+
 extern "C" ddp_status ddp_reducer_mark_ready(ddp_reducer* r, int32_t param, void* producer_stream)
 {
-    return mark_one(r, param, producer_stream, false);
+    return mark_one(r, param, producer_stream, false, true);
 }
 
 extern "C" ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t* params, int32_t n,
@@ -435,7 +550,7 @@ extern "C" ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t*
 {
     if (n < 0 || (n > 0 && !params)) return ddp::fail(DDP_E_INVAL, "ddp_reducer_mark_ready_many: bad list");
     ddp_status st = DDP_OK;
-    for (int32_t i = 0; i < n && st == DDP_OK; ++i) st = mark_one(r, params[i], producer_stream, true);
+    for (int32_t i = 0; i < n && st == DDP_OK; ++i) st = mark_one(r, params[i], producer_stream, true, true);
     // one issue pass for everything the list completed (coalesced when enabled),
     // also after a failure so that the parameters already marked are not stranded
     ddp_status st2 = r ? r->gate_batch() : DDP_OK;

@@ -13,7 +13,8 @@ from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, 
                DDP_R_WIRE_F16, Plan, ddp_pack, ddp_pack_group,
                ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
-               ddp_reducer_mark_ready_many, ddp_reducer_prepare)
+               ddp_reducer_find_unused, ddp_reducer_mark_ready_many, ddp_reducer_prepare,
+               ddp_reducer_set_local_used)
 
 
 class BucketReducer:
@@ -40,18 +41,33 @@ class BucketReducer:
         self._tensors = (grads, grads_out)   # the pointer tables below point into these
         self.grads_tab = self.plan.pointer_table(grads)
         self.used_np = None if used is None else np.ascontiguousarray(used, dtype=np.uint8).reshape(self.W, P)
-        self.used_tab = None if used is None else self.plan.flag_table(self.used_np)
-        gu = None if used is None else self.used_np.max(axis=0)
-        self.global_used_tab = None if gu is None else self.plan.flag_table(gu)
+        self.used_tab = None if used is None else self.plan.flag_table(self.used_np)   # no_sync packs
         self.out_tab = None if grads_out is None else self.plan.pointer_table(grads_out)
         flags = (DDP_R_FUSED if fused else 0) | (DDP_R_COPY_BACK if grads_out is not None else 0) | \
                 (DDP_R_TIMING if timing else 0) | (DDP_R_COALESCE if coalesce and fused else 0) | \
                 {None: 0, DDP_BF16: DDP_R_WIRE_BF16, DDP_F16: DDP_R_WIRE_F16}[wire]
         self.handle = ddp_reducer_create(P, self.plan.bucket_of, self.plan.bucket_order, self.plan.descs,
                                          self.plan.bucket_start, self.W, self.mode, flags, self.grads_tab,
-                                         self.used_tab, P, self.main_grad, self.plan.replica_stride, self.out_tab,
-                                         self.global_used_tab, self.side)
+                                         None, P, self.main_grad, self.plan.replica_stride, self.out_tab,
+                                         None, self.side)
         self.ready_order = np.arange(P - 1, -1, -1, dtype=np.int32)
+        if used is not None:
+            # find_unused_parameters: the reducer uploads the host bitmap at every prepare,
+            # all-reduces it on the side stream and marks the parameters nobody used
+            dev = self.plan.device
+            self.local_used_dev = torch.zeros(max(self.W * P, 1), dtype=torch.uint8, device=dev)
+            self.global_used_dev = torch.zeros(max(P, 1), dtype=torch.uint8, device=dev)
+            self.global_count_dev = torch.zeros(max(P, 1), dtype=torch.int32, device=dev)
+            ddp_reducer_find_unused(self.handle, self.local_used_dev, self.global_used_dev, self.global_count_dev)
+            self.set_local_used(self.used_np)
+
+    def set_local_used(self, used):
+        """This iteration's local-used bitmap [W, P] (find_unused_parameters)."""
+        self.used_np = np.ascontiguousarray(used, dtype=np.uint8).reshape(self.W, self.plan.nparams)
+        ddp_reducer_set_local_used(self.handle, self.used_np)
+        # parameters nobody used are marked by prepare; the backward produces the rest
+        produced = self.used_np.any(axis=0)
+        self.ready_order = np.array([p for p in range(self.plan.nparams - 1, -1, -1) if produced[p]], np.int32)
 
     # -- one iteration ----------------------------------------------------
     def accumulate_local(self, grads_tab, first: bool, stream=None):

@@ -45,6 +45,7 @@ WORKLOADS = {
     "resnet50_w8_allreduce": WL.c2_resnet50,
     "gpt2_small_w8_reduce_scatter": WL.c3_gpt2,
     "bert_large_w4_nosync4_allreduce": WL.c4_bert_large,
+    "bert_large_w4_find_unused_allreduce": WL.c6_bert_find_unused,
 }
 DEFAULT = "resnet50_w8_allreduce"
 ELEM = {WL.F32: 4, WL.BF16: 2}
@@ -54,36 +55,37 @@ ELEM = {WL.F32: 4, WL.BF16: 2}
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 def bucket_bytes(wl, numel: int, param_elems: int, used_elems: int, kind: str) -> int:
-    """Bytes one launch must move for one bucket.
+    """Bytes one launch must move for one bucket.  used_elems: gradient elements the
+    replicas used, summed over the replicas.
     fused:  every used gradient read, main_grad read when accumulating, result written
             (allreduce: W replicas; reduce_scatter: one shard per replica = one bucket);
     pack0:  gradients read, bucket written (copy); packN: gradients + bucket read, bucket written
             (only used segments are touched when accumulating)."""
     W, b_in = wl.W, ELEM[wl.dtype]
     if kind == "fused":
-        rd = W * used_elems * b_in
+        rd = used_elems * b_in
         wr = W * numel * 4 if wl.mode == WL.ALLREDUCE else numel * 4
         return rd + wr
     if kind == "fused_acc":
-        rd = W * used_elems * b_in + W * numel * 4
+        rd = used_elems * b_in + W * numel * 4
         wr = W * numel * 4 if wl.mode == WL.ALLREDUCE else numel * 4
         return rd + wr
     if kind == "pack0":
-        return W * used_elems * b_in + W * numel * 4
+        return used_elems * b_in + W * numel * 4
     if kind == "packN":
-        return W * used_elems * (b_in + 8)
+        return used_elems * (b_in + 8)
     raise ValueError(kind)
 
 
 def step_launches(wl, plan):
     """[(kind, bucket, bytes)] of one step, in launch order."""
-    used = set(range(wl.nparams)) - set(wl.unused)
+    used = WL.local_used_np(wl)
     out = []
     per_bucket = []
     for b in range(plan.nbuckets):
         mem = plan.members[b]
         pe = sum(wl.numels[p] for p in mem)
-        ue = sum(wl.numels[p] for p in mem if p in used)
+        ue = sum(wl.numels[p] * int(np.count_nonzero(used[:, p])) for p in mem)
         per_bucket.append((int(plan.bucket_numel[b]), pe, ue))
     for m in range(wl.micro_steps - 1):
         for b in range(plan.nbuckets):
@@ -177,11 +179,8 @@ def oracle_sample(wl, seconds: float, min_reps: int = 1):
     mem = plan["members"][0]
     offs = [int(plan["offset_of"][p]) for p in mem]
     numel = int(plan["bucket_numel"][0])
-    used = np.ones((wl.W, len(mem)), np.uint8)
-    for j, p in enumerate(mem):
-        if p in wl.unused:
-            used[:, j] = 0
-    ue = sum(wl.numels[p] for p in mem if p not in wl.unused)
+    used = WL.local_used_np(wl)[:, mem]
+    ue = sum(wl.numels[p] * int(np.count_nonzero(used[:, j])) for j, p in enumerate(mem))
     pe = sum(wl.numels[p] for p in mem)
     nbytes = 0
     for m in range(wl.micro_steps - 1):
@@ -285,10 +284,7 @@ def run_ours(args, wl):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     # inputs resident in HBM
-    used = None
-    if wl.unused:
-        used = np.ones((wl.W, wl.nparams), np.uint8)
-        used[:, wl.unused] = 0
+    used = WL.local_used_np(wl) if (wl.unused or wl.partial_unused) else None
     micro = [[[None if p in wl.unused else WL.grad_torch(wl, p, w, m, dev) for p in range(wl.nparams)]
               for w in range(wl.W)] for m in range(wl.micro_steps)]
     coalesce = not args.no_coalesce
@@ -474,8 +470,8 @@ def run_ours(args, wl):
                          "step_split_ms": {"pack": round(pack_ms, 4), "fused": round(fused_ms, 4)} if packs else None},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (((wl.micro_steps - 1) * -(-sess.plan.nbuckets // 32) + -(-len(fused) // 32)) if coalesce
-                             else len(launches)) * K,
+            "gpu_launches": ((((wl.micro_steps - 1) * -(-sess.plan.nbuckets // 32) + -(-len(fused) // 32)) if coalesce
+                              else len(launches)) + (1 if used is not None else 0)) * K,   # + the used-bitmap kernel
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -580,6 +576,102 @@ def run_sweep(args):
                           "l2_resident": moved < l2, "reps": reps, "timing": timing}), flush=True)
         del x
         torch.cuda.empty_cache()
+
+
+def run_bitmap(args):
+    """find_unused_parameters' bitmap all-reduce ("Lecture 15: PyTorch DDP" 4.2).
+    (1) ddp_used_allreduce alone on 16M parameters x 8 replicas (HBM-bound: W*P bytes
+    read, 5*P written), L2 flushed before each rep; (2) at BERT-large's 391 parameters,
+    W = 4, back-to-back launches (launch-bound); (3) the reducer's step on BERT-large
+    with the bitmap path (upload, all-reduce, host marking) against the same step
+    without it, all parameters used -- the cost the lecture says find_unused adds to
+    every iteration.  One JSON line."""
+    import torch
+
+    import allreduce_ddp_assign_gb300 as D
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    dev = torch.device("cuda", 0)
+    D.lib()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    W, P = 8, 1 << 24
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    local = (torch.rand((W, P), generator=g, device=dev) < 0.02).to(torch.uint8)
+    cnt = torch.empty(P, dtype=torch.int32, device=dev)
+    flg = torch.empty(P, dtype=torch.uint8, device=dev)
+    times = []
+    for r in range(13):
+        flush.fill_(float(r))
+        a, b = ev(), ev()
+        a.record()
+        D.ddp_used_allreduce(local, P, W, P, cnt, flg)
+        b.record()
+        b.synchronize()
+        if r >= 3:
+            times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    moved = W * P + 5 * P
+    large = {"W": W, "params": P, "bytes": moved, "us": round(ms * 1e3, 2),
+             "GBps": round(moved / (ms * 1e-3) / 1e9, 1),
+             "frac_measured": round(moved / (ms * 1e-3) / 1e9 / peak, 4), "timing": "L2 flushed before each rep"}
+    del local, cnt, flg
+
+    wl = WL.c6_bert_find_unused()
+    Wm, Pm = wl.W, wl.nparams
+    lu = torch.ones(Wm * Pm, dtype=torch.uint8, device=dev)
+    c2 = torch.empty(Pm, dtype=torch.int32, device=dev)
+    f2 = torch.empty(Pm, dtype=torch.uint8, device=dev)
+    for _ in range(10):
+        D.ddp_used_allreduce(lu, Pm, Wm, Pm, c2, f2)
+    torch.cuda.synchronize()
+    a, b = ev(), ev()
+    a.record()
+    for _ in range(1000):
+        D.ddp_used_allreduce(lu, Pm, Wm, Pm, c2, f2)
+    b.record()
+    b.synchronize()
+    model = {"W": Wm, "params": Pm, "us_per_call": round(a.elapsed_time(b), 3),
+             "timing": "1000 back-to-back launches, GPU time per launch (includes launch gaps)"}
+
+    grads = [[WL.grad_torch(wl, p, w, 0, dev) for p in range(Pm)] for w in range(Wm)]
+
+    def step_ms(used):
+        sess = BucketReducer(wl.numels, None, Wm, wl.mode, wl.order, wl.cap_bytes, wl.first_cap_bytes,
+                             wl.pad_multiple, grads, used=used, coalesce=True)
+        comp = torch.cuda.current_stream()
+        for _ in range(5):
+            sess.step(comp, comp)
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(comp)
+        for _ in range(args.steps):
+            if used is not None:
+                sess.set_local_used(used)
+            sess.step(comp, comp)
+        b.record(comp)
+        b.synchronize()
+        sess.close()
+        return a.elapsed_time(b) / args.steps
+
+    t_plain = step_ms(None)
+    t_fu_all = step_ms(np.ones((Wm, Pm), np.uint8))
+    t_fu = step_ms(WL.local_used_np(wl))
+    line = {"bitmap": True, "kernel_large": large, "kernel_model_size": model,
+            "reducer_step_ms": {"workload": wl.name, "without_bitmap": round(t_plain, 4),
+                                "find_unused_all_used": round(t_fu_all, 4),
+                                "find_unused_workload_bitmap": round(t_fu, 4),
+                                "overhead_ms": round(t_fu_all - t_plain, 4), "steps": args.steps}}
+    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_overlap(args, wl=None):
@@ -702,12 +794,15 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="bandwidth sweep of ddp_bucket_allreduce (JSON per point)")
     ap.add_argument("--sweep-max-bytes", type=int, default=0)
     ap.add_argument("--overlap", action="store_true", help="overlap with a synthetic backward (JSON line)")
+    ap.add_argument("--bitmap", action="store_true", help="find_unused bitmap all-reduce (JSON line)")
     ap.add_argument("--backward-ms", type=float, default=3.0)
     args = ap.parse_args(argv)
     if args.sweep:
         return run_sweep(args)
     if args.overlap:
         return run_overlap(args)
+    if args.bitmap:
+        return run_bitmap(args)
     wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, wl)

@@ -331,6 +331,42 @@ ddp_status ddp_unpack(const ddp_bucket_desc* bucket, const float* main_grad, int
                       const uint8_t* global_used, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* The local-used bitmap all-reduce (device)                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * ddp_used_allreduce -- sum the replicas' local-used bitmaps into the global
+ * one that decides which gradients unpack may write.
+ *
+ * Defined by: lecture 4.2 (with find_unused_parameters each rank records in a
+ * bitmap which parameters it used and the ranks all-reduce it in one extra
+ * collective, kept apart from the gradient buckets because its element type
+ * differs; a parameter no rank used keeps its .grad untouched, one that some
+ * ranks used is reduced with zeros from the others); the summary of Li et
+ * al. 2020, sections 2.2 and 3.2 (one bitmap for the whole model, kept on the
+ * host, copied to the device without blocking, then all-reduced).
+ *
+ *   global_count[p] = number of replicas w with local_used[w * ld + p] != 0
+ *   global_used[p]  = global_count[p] > 0 ? 1 : 0
+ * for p in [0, nparams).  Any nonzero byte counts as one use.  Integer sums do
+ * not depend on the order of the additions, so the ring's order needs no
+ * reproduction: every rank of an all-reduce ends with these values, and they
+ * are written once.
+ *
+ *   local_used     DEVICE uint8[W * ld], replica-major (row w = replica w).
+ *   ld             row stride in bytes, >= nparams.
+ *   W              replicas, 1..64.
+ *   global_count   DEVICE int32[nparams], or NULL.
+ *   global_used    DEVICE uint8[nparams], or NULL (not both NULL).
+ * nparams == 0 launches nothing.  16-byte-aligned local_used with ld a
+ * multiple of 16 takes the vector path (16 parameters per thread).
+ *
+ * Errors: DDP_E_INVAL (W outside [1, 64], nparams < 0, ld < nparams, null
+ * local_used, both outputs NULL); DDP_E_CUDA (launch failure).
+ */
+ddp_status ddp_used_allreduce(const uint8_t* local_used, int32_t ld, int32_t W, int32_t nparams,
+                              int32_t* global_count, uint8_t* global_used, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Steps 2-4 fused (device)                                                  */
 /* ------------------------------------------------------------------------ */
 /*
@@ -454,6 +490,49 @@ ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, const int32_t* 
  * that did not receive a gradient.  The reducer is reset anyway.
  */
 ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate);
+
+/*
+ * ddp_reducer_find_unused -- turn on find_unused_parameters (lecture 4.2; the
+ * summary of Li et al. 2020, sections 2.2 and 3.2; DDP chapter 17.33).
+ *
+ * From then on the reducer keeps a HOST bitmap, W rows of nparams bytes (row
+ * w = replica w's local use, all 1 at first), set by ddp_reducer_set_local_used.
+ * Every ddp_reducer_prepare then, on the side stream:
+ *   1. copies the host bitmap into local_used (rows of stride ld);
+ *   2. runs ddp_used_allreduce(local_used, ld, W, nparams, global_count,
+ *      global_used) -- the extra all-reduce;
+ * and on the host marks ready, without a producer stream, every parameter
+ * that no replica used (the backward will not produce it), so that its
+ * bucket can complete.  Unpack and copy-back then skip the globally unused
+ * parameters (they read global_used), and a replica that did not use a
+ * parameter contributes zero to its bucket: the packs read local_used as
+ * their `used` flags when ddp_reducer_create was given none.
+ *
+ *   local_used    DEVICE uint8[W * ld] (ld from ddp_reducer_create, >= nparams),
+ *                 written by the reducer.
+ *   global_used   DEVICE uint8[nparams], written by the reducer.
+ *   global_count  DEVICE int32[nparams] or NULL, written by the reducer.
+ * With DDP_R_DRY_RUN all three may be NULL (the host marking still happens).
+ * Call outside an iteration, once per reducer.  The host bitmap is pinned
+ * host memory owned by the reducer.
+ * Errors: DDP_E_INVAL (null reducer or pointers, ld < nparams, or the reducer
+ * was created with its own global_used); DDP_E_STATE (inside an iteration, or
+ * already on); DDP_E_CUDA (host allocation or event creation).
+ */
+ddp_status ddp_reducer_find_unused(ddp_reducer* r, uint8_t* local_used, uint8_t* global_used,
+                                   int32_t* global_count);
+
+/*
+ * ddp_reducer_set_local_used -- this iteration's local-used bitmap: HOST
+ * flags[w * ld + p] nonzero if replica w used parameter p (for a no_sync
+ * window, whether it used p in any of the window's micro-steps).  Copied into
+ * the reducer's host bitmap; if the copy to the device issued by the last
+ * prepare has not finished, waits for it first.  Call before the prepare of
+ * the iteration it describes.
+ * Errors: DDP_E_INVAL (null reducer or flags, ld < nparams); DDP_E_STATE
+ * (find_unused is off, or inside an iteration); DDP_E_CUDA.
+ */
+ddp_status ddp_reducer_set_local_used(ddp_reducer* r, const uint8_t* flags, int32_t ld);
 
 /*
  * ddp_reducer_mark_ready -- the autograd hook of parameter `param` fired: its

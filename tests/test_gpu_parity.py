@@ -311,7 +311,7 @@ def test_mlp_copy_back_partial_use(orc):
         buf = orc.pack([[raw[0][w][p] for p in mem] for w in range(wl.W)], offs, int(plan["bucket_numel"][0]),
                        used=used[:, mem])
         buf, _ = orc.ring(buf)
-        exp = orc.unpack(buf, offs, [wl.numels[p] for p in mem], 0, used.max(axis=0)[mem],
+        exp = orc.unpack(buf, offs, [wl.numels[p] for p in mem], 0, orc.used_allreduce(used)[1][mem],
                          outs=[[np.full(wl.numels[p], 9.0, np.float32) for p in mem] for _ in range(wl.W)])
         for w in range(wl.W):
             for j, p in enumerate(mem):

@@ -183,3 +183,94 @@ def test_ready_order_recorded_for_rebuild():
     plan = D.ddp_assign_buckets_ordered([10, 10, 10, 10, 10], order, None, 80, 40)
     assert [int(p) for p in plan["members"]][:1] == [4]
     D.ddp_reducer_destroy(r)
+
+
+# ---------------------------------------------------------------------------
+# find_unused_parameters (dry run: the host side of the bitmap path)
+# ---------------------------------------------------------------------------
+def make_fu(bucket_of, W=2, **kw):
+    nb = max(bucket_of) + 1
+    descs = [D.BucketDesc(8, 0, 0, None, None) for _ in range(nb)]
+    return D.ddp_reducer_create(len(bucket_of), bucket_of, list(range(nb)), descs, [0] * nb, W, D.DDP_ALLREDUCE,
+                                D.DDP_R_DRY_RUN | D.DDP_R_FUSED, replica_stride=8, ld=len(bucket_of), **kw)
+
+
+def test_find_unused_marks_parameters_no_replica_used():
+    """Lecture 15 section 4.2: parameters nobody used are marked ready at the start of
+    the backward, so a bucket made only of them goes out at once and the others
+    complete without their marks; a parameter one replica used still needs its mark."""
+    r = make_fu([0, 0, 1, 2, 2])
+    D.ddp_reducer_find_unused(r, None, None)
+    D.ddp_reducer_set_local_used(r, [[1, 0, 0, 1, 0], [1, 0, 0, 0, 0]])
+    D.ddp_reducer_prepare(r)
+    assert D.ddp_reducer_issue_log(r) == []          # bucket 0 still waits for parameter 0
+    D.ddp_reducer_mark_ready(r, 3)                    # used by replica 0 only
+    D.ddp_reducer_mark_ready(r, 0)                    # bucket 0, then 1 (p2 unused) and 2 (p4 unused)
+    assert D.ddp_reducer_issue_log(r) == [0, 1, 2]
+    D.ddp_reducer_finalize(r)
+    # an automatically marked parameter marked again is the double-mark error
+    D.ddp_reducer_set_local_used(r, [[1, 1, 1, 1, 0], [1, 1, 1, 1, 0]])
+    D.ddp_reducer_prepare(r)
+    with pytest.raises(D.DdpError, match="twice"):
+        D.ddp_reducer_mark_ready(r, 4)
+    D.ddp_reducer_destroy(r)
+
+
+def test_find_unused_all_unused_bucket_issued_at_prepare():
+    r = make_fu([0, 1, 1])
+    D.ddp_reducer_find_unused(r, None, None)
+    D.ddp_reducer_set_local_used(r, [[0, 1, 1], [0, 0, 1]])
+    D.ddp_reducer_prepare(r)
+    assert D.ddp_reducer_issue_log(r) == [0]
+    D.ddp_reducer_mark_ready_many(r, [2, 1])
+    assert D.ddp_reducer_issue_log(r) == [0, 1]
+    D.ddp_reducer_finalize(r)
+    # the ready order seen by a rebuild starts with the parameters marked at prepare
+    assert D.ddp_reducer_ready_order(r) == [0, 2, 1]
+    D.ddp_reducer_destroy(r)
+
+
+def test_find_unused_default_bitmap_is_all_used():
+    r = make_fu([0, 1])
+    D.ddp_reducer_find_unused(r, None, None)
+    D.ddp_reducer_prepare(r)
+    assert D.ddp_reducer_issue_log(r) == []
+    D.ddp_reducer_mark_ready_many(r, [1, 0])
+    assert D.ddp_reducer_issue_log(r) == [0, 1]
+    D.ddp_reducer_finalize(r)
+    D.ddp_reducer_destroy(r)
+
+
+def test_find_unused_state_and_argument_errors():
+    r = make_fu([0, 1])
+    with pytest.raises(D.DdpError, match="find_unused is off"):
+        D.ddp_reducer_set_local_used(r, [[1, 1], [1, 1]])
+    D.ddp_reducer_find_unused(r, None, None)
+    with pytest.raises(D.DdpError, match="already on"):
+        D.ddp_reducer_find_unused(r, None, None)
+    with pytest.raises(D.DdpError, match="ld = 1 < nparams = 2"):
+        D.ddp_reducer_set_local_used(r, [[1], [1]])
+    D.ddp_reducer_prepare(r)
+    with pytest.raises(D.DdpError, match="inside an iteration"):
+        D.ddp_reducer_set_local_used(r, [[1, 1], [1, 1]])
+    D.ddp_reducer_destroy(r)
+    r = make_fu([0, 1], global_used=0x1000)   # dry run: the address is never dereferenced
+    with pytest.raises(D.DdpError, match="its own global_used"):
+        D.ddp_reducer_find_unused(r, None, None)
+    D.ddp_reducer_destroy(r)
+
+
+def test_used_allreduce_validation_without_launch():
+    """Argument errors are found on the host, before anything is launched; an empty
+    bitmap launches nothing (so this runs without a GPU)."""
+    with pytest.raises(D.DdpError, match="W = 0"):
+        D.ddp_used_allreduce(None, 4, 0, 4, None, 0x1000, stream=0)
+    with pytest.raises(D.DdpError, match="W = 65"):
+        D.ddp_used_allreduce(None, 4, 65, 4, None, 0x1000, stream=0)
+    with pytest.raises(D.DdpError, match="ld = 3 < nparams = 4"):
+        D.ddp_used_allreduce(0x1000, 3, 2, 4, None, 0x1000, stream=0)
+    with pytest.raises(D.DdpError, match="both outputs"):
+        D.ddp_used_allreduce(0x1000, 4, 2, 4, None, None, stream=0)
+    with pytest.raises(D.DdpError, match="local_used is NULL"):
+        D.ddp_used_allreduce(None, 4, 2, 4, None, 0x1000, stream=0)
+    D.ddp_used_allreduce(None, 0, 2, 0, None, 0x1000, stream=0)
