@@ -488,6 +488,9 @@ ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, const int32_t* 
  * but never finished (the DDP chapter 17.6 error "Expected to have finished
  * reduction in the prior iteration"); the message lists the parameter indices
  * that did not receive a gradient.  The reducer is reset anyway.
+ * With find_unused on (ddp_reducer_find_unused) it also uploads the bitmap,
+ * launches the bitmap all-reduce on the side stream and marks ready the
+ * parameters no replica used; buckets made only of those are issued here.
  */
 ddp_status ddp_reducer_prepare(ddp_reducer* r, int32_t accumulate);
 
@@ -573,6 +576,7 @@ ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, int32_t cap
  * ddp_reducer_ready_order -- the order in which the last finalized iteration
  * marked its parameters ready (the gradient-ready order DDP records for the
  * bucket rebuild, DDP chapter 17.13).  HOST out[cap]; *n = nparams marked.
+ * Parameters marked by prepare under find_unused come first.
  * Errors: DDP_E_STATE if no iteration was finalized; DDP_E_CAPACITY.
  */
 ddp_status ddp_reducer_ready_order(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n);
