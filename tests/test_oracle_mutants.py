@@ -6,6 +6,9 @@ temporary directory.  The test requires that the substitution applies, that the
 mutant compiles, and that at least one pin of ``oracle_pins`` fails on it.
 """
 import os
+import sys
+
+import numpy as np
 
 import pytest
 
@@ -75,5 +78,52 @@ def test_mutant_is_caught(name, tmp_path):
         try:
             pin(orc)
         except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passes every pin"
+
+
+# ---------------------------------------------------------------------------
+# the PowerSGD oracle (Python): each mutant is a patched copy of the module
+# ---------------------------------------------------------------------------
+PSGD_MUTANTS = {
+    "p_not_all_reduced": [("p = sum(mw[w] @ q for w in range(W))", "p = mw[0] @ q")],
+    "p_not_orthogonalised": [("        p = _orthonormal(p)\n", "")],
+    "q_not_divided_by_world": [("qn = sum(mw[w].T @ p for w in range(W)) / W", "qn = sum(mw[w].T @ p for w in range(W))")],
+    "error_not_fed_back": [("mw.append(g + state.error[w][t] if state.error_feedback else g)", "mw.append(g)")],
+    "error_sign_flipped": [("state.error[w][t] = mw[w] - approx", "state.error[w][t] = approx - mw[w]")],
+    "warm_start_dropped": [("        state.q[t] = qn\n", "")],
+    "rank_not_clamped": [("    return min(rank, m, n)", "    return rank")],
+    "vectors_left_alone": [("                out[:, seg_offset[t]:seg_offset[t] + k] = mean[:, pos:pos + k]", "                pass")],
+    "warmup_ignored": [("    if state.iter < state.start_iter:", "    if False:")],
+    "view_last_dim": [("    return shape[0], n", "    return n, shape[0]")],
+    "qr_sign_not_fixed": [("    qm = qm * np.where(d < 0, -1.0, 1.0)\n", "")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(PSGD_MUTANTS))
+def test_powersgd_mutant_is_caught(name, tmp_path, orc):
+    import importlib.util
+
+    from oracle import powersgd
+    from oracle_pins_powersgd import POWERSGD_PINS
+
+    src = open(powersgd.__file__).read()
+    for old, new in PSGD_MUTANTS[name]:
+        assert src.count(old) >= 1, f"substitution for {name} no longer applies: {old!r}"
+        src = src.replace(old, new, 1)
+    path = tmp_path / f"powersgd_{name}.py"
+    path.write_text(src)
+    spec = importlib.util.spec_from_file_location(f"powersgd_{name}", path)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[spec.name] = mod          # dataclasses look the module up while it loads
+    try:
+        spec.loader.exec_module(mod)
+    finally:
+        del sys.modules[spec.name]
+    failed = []
+    for pin in POWERSGD_PINS:
+        try:
+            pin(orc, mod)
+        except (AssertionError, ValueError, np.linalg.LinAlgError, IndexError):
             failed.append(pin.__name__)
     assert failed, f"mutant {name} passes every pin"

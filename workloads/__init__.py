@@ -315,6 +315,25 @@ ALL = {"c1": c1_mlp, "c2": c2_resnet50, "c3": c3_gpt2, "c4": c4_bert_large, "c6"
 USED_MAP_STREAM = 1 << 40   # generator stream of the local-used bitmaps (beyond every gradient stream)
 
 
+POWERSGD_Q_STREAM = 1 << 41   # generator streams of PowerSGD's initial Q matrices (one per tensor)
+
+
+def powersgd_q0_np(seed: int, tensor: int, n: int, r: int) -> np.ndarray:
+    """The initial Q of one tensor (N x R, fp32): the hook's random normal draw,
+    stood in for by the generator's ``normal`` values (unit variance)."""
+    bits = bits_np(stream_key(seed, POWERSGD_Q_STREAM + tensor), 0, n * r)
+    return values_np(bits, "normal", 1.0).reshape(n, r)
+
+
+def c7_resnet50_powersgd(rank: int = 4) -> Workload:
+    """ResNet-50, W = 8, DDP buckets, every bucket reduced through the PowerSGD hook
+    at the given rank (the page's example rank is 4)."""
+    wl = c2_resnet50()
+    wl.name = f"resnet50_w8_powersgd_r{rank}"
+    wl.seed = 1007
+    return wl
+
+
 def local_used_np(wl: Workload) -> np.ndarray:
     """[W, P] uint8 local-used bitmap of one iteration: 0 on every replica for the
     parameters in ``wl.unused``; 0 for the seeded fraction ``wl.partial_unused`` of
