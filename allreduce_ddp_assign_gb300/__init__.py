@@ -76,6 +76,16 @@ _SIGS = {
     "ddp_reducer_prepare": (C.c_int32, [_vp, C.c_int32]),
     "ddp_used_allreduce": (C.c_int32, [_vp, C.c_int32, C.c_int32, C.c_int32, _vp, _vp, _vp]),
     "ddp_reducer_find_unused": (C.c_int32, [_vp, _vp, _vp, _vp]),
+    "ddp_reducer_register_powersgd": (C.c_int32, [_vp, C.c_int32, _vp]),
+    "ddp_powersgd_create": (C.c_int32, [C.c_int32, C.c_int32, C.c_int32, _i64p, _i64p, _i64p, C.c_int64, C.c_int32,
+                                        C.c_int32, C.POINTER(_vp)]),
+    "ddp_powersgd_sizes": (C.c_int32, [_vp, _i64p, _i64p, _i32p]),
+    "ddp_powersgd_matrix": (C.c_int32, [_vp, C.c_int32, _i64p, _i32p, _i32p, _i32p, _i32p]),
+    "ddp_powersgd_bind": (C.c_int32, [_vp, _vp, C.c_int64, _vp, _vp, C.c_int64, _vp]),
+    "ddp_powersgd_set_q": (C.c_int32, [_vp, C.c_int32, _vp, _vp]),
+    "ddp_powersgd_reduce": (C.c_int32, [_vp, _vp, C.c_int64, _vp]),
+    "ddp_powersgd_iter": (C.c_int32, [_vp, _i32p]),
+    "ddp_powersgd_destroy": (None, [_vp]),
     "ddp_reducer_set_local_used": (C.c_int32, [_vp, _vp, C.c_int32]),
     "ddp_reducer_mark_ready": (C.c_int32, [_vp, C.c_int32, _vp]),
     "ddp_reducer_mark_ready_many": (C.c_int32, [_vp, _i32p, C.c_int32, _vp]),
@@ -323,6 +333,61 @@ def ddp_reducer_set_local_used(r, flags, ld=None) -> None:
     if f.ndim != 2:
         raise ValueError("flags must be [W, nparams]")
     _check(lib().ddp_reducer_set_local_used(r, f.ctypes.data_as(_vp), int(f.shape[1] if ld is None else ld)))
+
+
+# ---------------------------------------------------------------------------
+# the PowerSGD hook
+# ---------------------------------------------------------------------------
+def ddp_powersgd_create(W, rank, seg_offset, seg_numel, seg_rows, bucket_numel, error_feedback=1, start_iter=0):
+    off = _a(seg_offset, np.int64)
+    num = _a(seg_numel, np.int64)
+    rows = _a(seg_rows, np.int64)
+    h = _vp()
+    _check(lib().ddp_powersgd_create(int(W), int(rank), len(off), _cp(off, _i64p), _cp(num, _i64p), _cp(rows, _i64p),
+                                     int(bucket_numel), int(error_feedback), int(start_iter), C.byref(h)))
+    return h.value
+
+
+def ddp_powersgd_sizes(h) -> dict:
+    ws, q, nm = C.c_int64(0), C.c_int64(0), C.c_int32(0)
+    _check(lib().ddp_powersgd_sizes(h, C.byref(ws), C.byref(q), C.byref(nm)))
+    return dict(workspace_bytes=ws.value, q_elems=q.value, nmatrices=nm.value)
+
+
+def ddp_powersgd_matrix(h, seg) -> dict:
+    off, rows, cols, re, rp = C.c_int64(0), C.c_int32(0), C.c_int32(0), C.c_int32(0), C.c_int32(0)
+    _check(lib().ddp_powersgd_matrix(h, int(seg), C.byref(off), C.byref(rows), C.byref(cols), C.byref(re),
+                                     C.byref(rp)))
+    return dict(q_offset=off.value, rows=rows.value, cols=cols.value, rank_eff=re.value, rank_pad=rp.value)
+
+
+def ddp_powersgd_bind(h, workspace, workspace_bytes, q_state, error=None, error_stride=0, stream=None) -> None:
+    _check(lib().ddp_powersgd_bind(h, _ptr(workspace), int(workspace_bytes), _ptr(q_state), _ptr(error),
+                                   int(error_stride), _stream(stream)))
+
+
+def ddp_powersgd_set_q(h, seg, q, stream=None) -> None:
+    qa = np.ascontiguousarray(q, dtype=np.float32)
+    _check(lib().ddp_powersgd_set_q(h, int(seg), qa.ctypes.data, _stream(stream)))
+
+
+def ddp_powersgd_reduce(h, main_grad, replica_stride, stream=None) -> None:
+    _check(lib().ddp_powersgd_reduce(h, _ptr(main_grad), int(replica_stride), _stream(stream)))
+
+
+def ddp_powersgd_iter(h) -> int:
+    it = C.c_int32(0)
+    _check(lib().ddp_powersgd_iter(h, C.byref(it)))
+    return it.value
+
+
+def ddp_powersgd_destroy(h) -> None:
+    if h:
+        lib().ddp_powersgd_destroy(h)
+
+
+def ddp_reducer_register_powersgd(r, bucket, h) -> None:
+    _check(lib().ddp_reducer_register_powersgd(r, int(bucket), h))
 
 
 def ddp_reducer_prepare(r, accumulate=0) -> None:

@@ -37,4 +37,8 @@ ddp_status launch_fused_group(const ddp_bucket_desc* bs, float* const* mgs, int3
                               int64_t stride, void* const* grads_out, const uint8_t* global_used, void* stream,
                               int32_t wire = DDP_F32);
 
+// Replicas and bucket size a PowerSGD state was planned for (powersgd.cu).
+int32_t powersgd_replicas(const ddp_powersgd* h);
+int64_t powersgd_numel(const ddp_powersgd* h);
+
 }  // namespace ddp

@@ -1,0 +1,686 @@
+// The PowerSGD communication hook on one bucket of W replicas.
+//
+// "DDP: ring AllReduce and gradient buckets" section 17.27: every tensor of
+// two or more dimensions, viewed as M x N, is replaced by a rank-R
+// approximation computed with one step of a warm-started power iteration --
+// P = M Q, all-reduce P, orthonormalise P, Q = M^T P, all-reduce Q and divide
+// by the world size, reconstruct P Q^T -- with error feedback (M = G + E,
+// E <- M - P Q^T); 1-D tensors take a plain all-reduce; the first
+// start_powerSGD_iter iterations take a plain all-reduce of the whole bucket.
+//
+// Kernels per compressed iteration (one launch each, over every tensor of the
+// bucket through tile tables built on the host):
+//   psgd_vec_kernel     1-D tensors: ring-ordered mean over their concatenation
+//   psgd_p_kernel       per (row, replica): M = G + E (stored back into E),
+//                       P_w[row] = M[row, :] Q; then the sum over replicas
+//   psgd_orth_kernel    per tensor: modified Gram-Schmidt on P's columns
+//   psgd_qpart_kernel   per (column block, row split, replica): partial M^T P
+//   psgd_qfinal_kernel  Q = (sum over replicas of the sum over splits) / W
+//   psgd_out_kernel     per row: G^ = P Q^T written to every replica, E = M - G^
+// Every kernel streams its matrix once: the contraction is rank R (1..8)
+// against a row or column of M, R fused multiply-adds per element and 4 to 12
+// bytes per element, far below the CUDA cores' arithmetic ridge, so the work is
+// HBM-bound and stays on the CUDA cores in fp32.  The orthonormalisation
+// accumulates its dot products in fp64 (M x R values, negligible time).
+//
+// Rank is padded to RP in {1, 2, 4, 8}: Q and P carry RP columns, those past a
+// tensor's effective rank min(R, M, N) are zero and stay zero.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "common.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsOut = kWarps;       // rows per output tile: one per warp
+constexpr int kRowsPerSplit = 256;     // rows of one partial M^T P
+constexpr int kFinalPerTile = 1024;    // Q elements per finalising tile
+constexpr int kMaxPairs = 256;         // (row, replica) pairs per P tile
+constexpr int64_t kVecPiece = 16384;   // elements of a 1-D tensor per block
+
+struct PsgdMat {
+    int64_t off;     // element offset of the tensor in the bucket
+    int64_t p_off;   // into P: M x RP
+    int64_t q_off;   // into the Q state: N x RP
+    int64_t qp_off;  // into the partial sums: S x W x N x RP
+    int32_t M, N;
+    int32_t r;       // effective rank
+    int32_t vec;     // offset and N are multiples of 4 (16-byte rows when the buffers are aligned)
+    int32_t S;       // row splits of M^T P
+    int32_t cbw;     // column block width of M^T P (128 on the 16-byte path, 32 otherwise)
+};
+
+struct PsgdVec {
+    int64_t off;     // element offset in the bucket
+    int64_t vpos;    // position in the concatenation of the 1-D tensors
+    int64_t len;
+};
+
+struct PsgdArgs {
+    float* mg;
+    int64_t stride;
+    float* err;
+    int64_t estride;
+    float* P;
+    float* Q;
+    float* QP;
+    const PsgdMat* mats;
+    const int4* tiles;
+    const PsgdVec* vecs;
+    int32_t W;
+    int32_t ef;
+    int32_t vec_ok;
+    int32_t rows_p;   // rows per P tile
+    float inv_w;
+    int64_t nvec;     // length of the concatenation of the 1-D tensors
+};
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+template <int RP>
+__device__ __forceinline__ void load_row(const float* __restrict__ src, float (&v)[RP])
+{
+    if constexpr (RP % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < RP; k += 4) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(src + k));
+            v[k] = x.x;
+            v[k + 1] = x.y;
+            v[k + 2] = x.z;
+            v[k + 3] = x.w;
+        }
+    } else if constexpr (RP == 2) {
+        const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+        v[0] = x.x;
+        v[1] = x.y;
+    } else {
+        v[0] = __ldg(src);
+    }
+}
+
+__device__ __forceinline__ float comp(const float4& v, int c) { return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w; }
+
+// ---------------------------------------------------------------------------
+// 1-D tensors: the ring mean over the concatenation (chunk c summed from
+// replica c+1 round to replica c, each term scaled by fp32(1/W))
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) psgd_vec_kernel(const PsgdArgs a)
+{
+    const PsgdVec v = a.vecs[blockIdx.x];
+    const int64_t L = (a.nvec + a.W - 1) / a.W;
+    for (int64_t i = threadIdx.x; i < v.len; i += kThreads) {
+        const int64_t e = v.off + i;
+        const int c = static_cast<int>((v.vpos + i) / L);
+        float acc = 0.f;
+        for (int k = 0; k < a.W; ++k) {
+            int w = c + 1 + k;
+            w -= (w >= a.W) ? a.W : 0;
+            w -= (w >= a.W) ? a.W : 0;
+            const float t = __fmul_rn(a.mg[w * a.stride + e], a.inv_w);
+            acc = k == 0 ? t : __fadd_rn(acc, t);
+        }
+        for (int w = 0; w < a.W; ++w) a.mg[w * a.stride + e] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// P = sum_w (G_w + E_w) Q  (tile: {mat, row0, nrows}; one warp per (row, replica))
+// ---------------------------------------------------------------------------
+template <int RP>
+__global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
+{
+    __shared__ float part[kMaxPairs][RP];
+    const int4 t = a.tiles[blockIdx.x];
+    const PsgdMat m = a.mats[t.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pairs = t.z * a.W;
+    const bool vec = m.vec && a.vec_ok;
+    const float* q = a.Q + m.q_off;
+    for (int u = warp; u < pairs; u += kWarps) {
+        const int row = t.y + u / a.W, w = u % a.W;
+        float* g = a.mg + w * a.stride + m.off + static_cast<int64_t>(row) * m.N;
+        float* e = a.ef ? a.err + w * a.estride + m.off + static_cast<int64_t>(row) * m.N : nullptr;
+        float acc[RP];
+#pragma unroll
+        for (int r = 0; r < RP; ++r) acc[r] = 0.f;
+        if (vec) {
+            for (int j = 4 * lane; j < m.N; j += 128) {
+                float4 x = ld4(g + j);
+                if (e) {
+                    const float4 y = ld4(e + j);
+                    x = make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z), __fadd_rn(x.w, y.w));
+                    st4(e + j, x);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float qv[RP];
+                    load_row<RP>(q + static_cast<int64_t>(j + c) * RP, qv);
+                    const float xc = comp(x, c);
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) acc[r] = fmaf(xc, qv[r], acc[r]);
+                }
+            }
+        } else {
+            for (int j = lane; j < m.N; j += 32) {
+                float x = g[j];
+                if (e) {
+                    x = __fadd_rn(x, e[j]);
+                    e[j] = x;
+                }
+                float qv[RP];
+                load_row<RP>(q + static_cast<int64_t>(j) * RP, qv);
+#pragma unroll
+                for (int r = 0; r < RP; ++r) acc[r] = fmaf(x, qv[r], acc[r]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RP; ++r)
+#pragma unroll
+            for (int o = 16; o; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+        if (lane == 0)
+#pragma unroll
+            for (int r = 0; r < RP; ++r) part[u][r] = acc[r];
+    }
+    __syncthreads();
+    // the all-reduce of P: replicas summed in order 0 .. W-1
+    for (int k = threadIdx.x; k < t.z * RP; k += kThreads) {
+        const int rl = k / RP, r = k % RP;
+        float s = 0.f;
+        for (int w = 0; w < a.W; ++w) s = __fadd_rn(s, part[rl * a.W + w][r]);
+        a.P[m.p_off + static_cast<int64_t>(t.y + rl) * RP + r] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// orthonormal columns of P (one block per tensor): modified Gram-Schmidt with
+// fp64 dot products; a column whose norm is 0 becomes 0
+// ---------------------------------------------------------------------------
+__device__ double block_sum(double v, double* red)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    double s = 0.0;
+    for (int k = 0; k < kWarps; ++k) s += red[k];
+    return s;
+}
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
+{
+    __shared__ double red[kWarps];
+    const PsgdMat m = a.mats[blockIdx.x];
+    float* p = a.P + m.p_off;
+    for (int r = 0; r < m.r; ++r) {
+        for (int k = 0; k < r; ++k) {
+            double d = 0.0;
+            for (int i = threadIdx.x; i < m.M; i += kThreads)
+                d += static_cast<double>(p[static_cast<int64_t>(i) * RP + k]) * p[static_cast<int64_t>(i) * RP + r];
+            const float df = static_cast<float>(block_sum(d, red));
+            for (int i = threadIdx.x; i < m.M; i += kThreads) {
+                float* x = p + static_cast<int64_t>(i) * RP;
+                x[r] = fmaf(-df, x[k], x[r]);
+            }
+            __syncthreads();
+        }
+        double nn = 0.0;
+        for (int i = threadIdx.x; i < m.M; i += kThreads) {
+            const double x = p[static_cast<int64_t>(i) * RP + r];
+            nn += x * x;
+        }
+        nn = block_sum(nn, red);
+        const float inv = nn > 0.0 ? static_cast<float>(1.0 / sqrt(nn)) : 0.f;
+        for (int i = threadIdx.x; i < m.M; i += kThreads) {
+            float* x = p + static_cast<int64_t>(i) * RP + r;
+            *x = nn > 0.0 ? __fmul_rn(*x, inv) : 0.f;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// partial Q_w = M_w^T P over one row split and one column block (tile: {mat,
+// column block, first unit, units}; unit = split * W + replica, one per warp)
+// ---------------------------------------------------------------------------
+template <int RP>
+__global__ void __launch_bounds__(kThreads) psgd_qpart_kernel(const PsgdArgs a)
+{
+    const int4 t = a.tiles[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= t.w) return;
+    const PsgdMat m = a.mats[t.x];
+    const int u = t.z + warp;
+    const int s = u / a.W, w = u % a.W;
+    const int i0 = s * kRowsPerSplit, i1 = min(m.M, i0 + kRowsPerSplit);
+    const float* src = (a.ef ? a.err + w * a.estride : a.mg + w * a.stride) + m.off;
+    const float* p = a.P + m.p_off;
+    float* out = a.QP + m.qp_off + static_cast<int64_t>(u) * m.N * RP;
+    const bool vec = m.vec && a.vec_ok;
+    if (vec) {
+        const int c = t.y * m.cbw + 4 * lane;
+        if (c >= m.N) return;
+        float acc[4][RP];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int r = 0; r < RP; ++r) acc[k][r] = 0.f;
+#pragma unroll 4
+        for (int i = i0; i < i1; ++i) {
+            const float4 x = ld4(src + static_cast<int64_t>(i) * m.N + c);
+            float pv[RP];
+            load_row<RP>(p + static_cast<int64_t>(i) * RP, pv);
+#pragma unroll
+            for (int r = 0; r < RP; ++r) {
+                acc[0][r] = fmaf(x.x, pv[r], acc[0][r]);
+                acc[1][r] = fmaf(x.y, pv[r], acc[1][r]);
+                acc[2][r] = fmaf(x.z, pv[r], acc[2][r]);
+                acc[3][r] = fmaf(x.w, pv[r], acc[3][r]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int r = 0; r < RP; ++r) out[static_cast<int64_t>(c + k) * RP + r] = acc[k][r];
+    } else {
+        // the block's columns 32 at a time (the block is 128 wide when the plan
+        // allowed 16-byte rows but the buffers are not aligned)
+        const int c1 = min(m.N, (t.y + 1) * m.cbw);
+        for (int c = t.y * m.cbw + lane; c < c1; c += 32) {
+            float acc[RP];
+#pragma unroll
+            for (int r = 0; r < RP; ++r) acc[r] = 0.f;
+#pragma unroll 4
+            for (int i = i0; i < i1; ++i) {
+                const float x = src[static_cast<int64_t>(i) * m.N + c];
+                float pv[RP];
+                load_row<RP>(p + static_cast<int64_t>(i) * RP, pv);
+#pragma unroll
+                for (int r = 0; r < RP; ++r) acc[r] = fmaf(x, pv[r], acc[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < RP; ++r) out[static_cast<int64_t>(c) * RP + r] = acc[r];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Q = (sum_w sum_s partial[s][w]) / W  (tile: {mat, first element, count})
+// ---------------------------------------------------------------------------
+template <int RP>
+__global__ void __launch_bounds__(kThreads) psgd_qfinal_kernel(const PsgdArgs a)
+{
+    const int4 t = a.tiles[blockIdx.x];
+    const PsgdMat m = a.mats[t.x];
+    const int64_t plane = static_cast<int64_t>(m.N) * RP;
+    const float wf = static_cast<float>(a.W);
+    for (int k = threadIdx.x; k < t.z; k += kThreads) {
+        const int64_t el = t.y + k;
+        float tot = 0.f;
+        for (int w = 0; w < a.W; ++w) {
+            float qw = 0.f;
+            for (int s = 0; s < m.S; ++s) qw = __fadd_rn(qw, a.QP[m.qp_off + (static_cast<int64_t>(s) * a.W + w) * plane + el]);
+            tot = __fadd_rn(tot, qw);
+        }
+        a.Q[m.q_off + el] = __fdiv_rn(tot, wf);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// G^ = P Q^T on every replica, E = M - G^  (tile: {mat, row0, nrows}; one warp per row)
+// ---------------------------------------------------------------------------
+template <int RP>
+__global__ void __launch_bounds__(kThreads) psgd_out_kernel(const PsgdArgs a)
+{
+    const int4 t = a.tiles[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= t.z) return;
+    const PsgdMat m = a.mats[t.x];
+    const int row = t.y + warp;
+    float pr[RP];
+    load_row<RP>(a.P + m.p_off + static_cast<int64_t>(row) * RP, pr);
+    const float* q = a.Q + m.q_off;
+    const int64_t base = m.off + static_cast<int64_t>(row) * m.N;
+    const bool vec = m.vec && a.vec_ok;
+    if (vec) {
+        for (int j = 4 * lane; j < m.N; j += 128) {
+            float h[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float qv[RP];
+                load_row<RP>(q + static_cast<int64_t>(j + c) * RP, qv);
+                float s = 0.f;
+#pragma unroll
+                for (int r = 0; r < RP; ++r) s = fmaf(pr[r], qv[r], s);
+                h[c] = s;
+            }
+            const float4 hv = make_float4(h[0], h[1], h[2], h[3]);
+            for (int w = 0; w < a.W; ++w) {
+                if (a.ef) {
+                    float* e = a.err + w * a.estride + base + j;
+                    const float4 x = ld4(e);
+                    st4(e, make_float4(__fsub_rn(x.x, h[0]), __fsub_rn(x.y, h[1]), __fsub_rn(x.z, h[2]),
+                                       __fsub_rn(x.w, h[3])));
+                }
+                st4(a.mg + w * a.stride + base + j, hv);
+            }
+        }
+    } else {
+        for (int j = lane; j < m.N; j += 32) {
+            float qv[RP];
+            load_row<RP>(q + static_cast<int64_t>(j) * RP, qv);
+            float h = 0.f;
+#pragma unroll
+            for (int r = 0; r < RP; ++r) h = fmaf(pr[r], qv[r], h);
+            for (int w = 0; w < a.W; ++w) {
+                if (a.ef) {
+                    float* e = a.err + w * a.estride + base + j;
+                    *e = __fsub_rn(*e, h);
+                }
+                a.mg[w * a.stride + base + j] = h;
+            }
+        }
+    }
+}
+
+int round_rank(int r) { return r <= 1 ? 1 : r <= 2 ? 2 : r <= 4 ? 4 : 8; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int64_t align4(int64_t x) { return (x + 3) & ~static_cast<int64_t>(3); }
+
+}  // namespace
+
+struct ddp_powersgd {
+    int32_t W = 1, rank = 1, RP = 1, ef = 1, start_iter = 0, iter = 0;
+    int64_t bucket_numel = 0;
+    int32_t nseg = 0;
+    std::vector<int32_t> seg_mat;   // matrix index of each segment, -1 for 1-D
+    std::vector<PsgdMat> mats;
+    std::vector<PsgdVec> vecs;
+    int64_t nvec = 0;
+    std::vector<int4> t_p, t_q, t_f, t_o;
+    int32_t rows_p = 1;
+    int64_t q_elems = 0, p_elems = 0, qp_elems = 0;
+    size_t off_mats = 0, off_tp = 0, off_tq = 0, off_tf = 0, off_to = 0, off_vecs = 0, off_P = 0, off_QP = 0;
+    size_t ws_bytes = 0;
+    // bound buffers
+    uint8_t* ws = nullptr;
+    float* q = nullptr;
+    float* err = nullptr;
+    int64_t estride = 0;
+};
+
+namespace {
+
+template <int RP>
+ddp_status launch_all(const ddp_powersgd& h, const PsgdArgs& base, cudaStream_t s)
+{
+    PsgdArgs a = base;
+    if (!h.vecs.empty()) {
+        a.vecs = reinterpret_cast<const PsgdVec*>(h.ws + h.off_vecs);
+        psgd_vec_kernel<<<static_cast<unsigned>(h.vecs.size()), kThreads, 0, s>>>(a);
+    }
+    if (!h.mats.empty()) {
+        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tp);
+        psgd_p_kernel<RP><<<static_cast<unsigned>(h.t_p.size()), kThreads, 0, s>>>(a);
+        psgd_orth_kernel<RP><<<static_cast<unsigned>(h.mats.size()), kThreads, 0, s>>>(a);
+        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tq);
+        psgd_qpart_kernel<RP><<<static_cast<unsigned>(h.t_q.size()), kThreads, 0, s>>>(a);
+        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tf);
+        psgd_qfinal_kernel<RP><<<static_cast<unsigned>(h.t_f.size()), kThreads, 0, s>>>(a);
+        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_to);
+        psgd_out_kernel<RP><<<static_cast<unsigned>(h.t_o.size()), kThreads, 0, s>>>(a);
+    }
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_powersgd_reduce: kernel launch failed: %s", cudaGetErrorString(err));
+    return DDP_OK;
+}
+
+}  // namespace
+
+extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg, const int64_t* seg_offset,
+                                          const int64_t* seg_numel, const int64_t* seg_rows, int64_t bucket_numel,
+                                          int32_t error_feedback, int32_t start_iter, ddp_powersgd** out)
+{
+    using ddp::fail;
+    const char* fn = "ddp_powersgd_create";
+    if (!out) return fail(DDP_E_INVAL, "%s: out is NULL", fn);
+    *out = nullptr;
+    if (W < 1 || W > ddp::kMaxReplicas) return fail(DDP_E_INVAL, "%s: W = %d outside [1, %d]", fn, W, ddp::kMaxReplicas);
+    if (rank < 1 || rank > 8) return fail(DDP_E_INVAL, "%s: rank = %d outside [1, 8]", fn, rank);
+    if (nseg < 0 || bucket_numel < 0 || start_iter < 0) return fail(DDP_E_INVAL, "%s: negative size", fn);
+    if (nseg > 0 && (!seg_offset || !seg_numel || !seg_rows)) return fail(DDP_E_INVAL, "%s: a segment array is NULL", fn);
+    auto h = new ddp_powersgd();
+    auto reject = [&](ddp_status s) {
+        delete h;
+        return s;
+    };
+    h->W = W;
+    h->rank = rank;
+    h->RP = round_rank(rank);
+    h->ef = error_feedback != 0;
+    h->start_iter = start_iter;
+    h->bucket_numel = bucket_numel;
+    h->nseg = nseg;
+    h->seg_mat.assign(nseg, -1);
+    h->rows_p = std::max(1, 32 / W);
+    const int RP = h->RP;
+    for (int32_t t = 0; t < nseg; ++t) {
+        const int64_t off = seg_offset[t], n = seg_numel[t], rows = seg_rows[t];
+        if (off < 0 || n < 0 || off + n > bucket_numel)
+            return reject(fail(DDP_E_INVAL, "%s: segment %d [%lld, +%lld) outside the bucket of %lld", fn, t,
+                               static_cast<long long>(off), static_cast<long long>(n),
+                               static_cast<long long>(bucket_numel)));
+        if (rows < 0) return reject(fail(DDP_E_INVAL, "%s: segment %d has %lld rows", fn, t, static_cast<long long>(rows)));
+        if (rows == 0) {
+            for (int64_t i = 0; i < n; i += kVecPiece)   // pieces of at most kVecPiece elements, one block each
+                h->vecs.push_back(PsgdVec{off + i, h->nvec + i, std::min<int64_t>(kVecPiece, n - i)});
+            h->nvec += n;
+            continue;
+        }
+        if (n % rows != 0 || n == 0)
+            return reject(fail(DDP_E_INVAL, "%s: segment %d: %lld elements are not %lld rows", fn, t,
+                               static_cast<long long>(n), static_cast<long long>(rows)));
+        const int64_t cols = n / rows;
+        if (rows > (1LL << 30) || cols * RP > (1LL << 30))
+            return reject(fail(DDP_E_INVAL, "%s: segment %d: %lld x %lld too large", fn, t, static_cast<long long>(rows),
+                               static_cast<long long>(cols)));
+        PsgdMat m{};
+        m.off = off;
+        m.M = static_cast<int32_t>(rows);
+        m.N = static_cast<int32_t>(cols);
+        m.r = static_cast<int32_t>(std::min<int64_t>({rank, rows, cols}));
+        m.vec = (off % 4 == 0) && (cols % 4 == 0);
+        m.cbw = m.vec ? 128 : 32;
+        m.S = static_cast<int32_t>((rows + kRowsPerSplit - 1) / kRowsPerSplit);
+        m.p_off = h->p_elems;
+        h->p_elems += align4(rows * RP);
+        m.q_off = h->q_elems;
+        h->q_elems += align4(cols * RP);
+        m.qp_off = h->qp_elems;
+        h->qp_elems += align4(static_cast<int64_t>(m.S) * W * cols * RP);
+        const int32_t mi = static_cast<int32_t>(h->mats.size());
+        h->seg_mat[t] = mi;
+        h->mats.push_back(m);
+        for (int32_t r0 = 0; r0 < m.M; r0 += h->rows_p)
+            h->t_p.push_back(make_int4(mi, r0, std::min(h->rows_p, m.M - r0), 0));
+        for (int32_t r0 = 0; r0 < m.M; r0 += kRowsOut)
+            h->t_o.push_back(make_int4(mi, r0, std::min(kRowsOut, m.M - r0), 0));
+        const int32_t ncb = (m.N + m.cbw - 1) / m.cbw, units = m.S * W;
+        for (int32_t cb = 0; cb < ncb; ++cb)
+            for (int32_t u0 = 0; u0 < units; u0 += kWarps)
+                h->t_q.push_back(make_int4(mi, cb, u0, std::min(kWarps, units - u0)));
+        const int64_t qe = static_cast<int64_t>(m.N) * RP;
+        for (int64_t e0 = 0; e0 < qe; e0 += kFinalPerTile)
+            h->t_f.push_back(make_int4(mi, static_cast<int32_t>(e0), static_cast<int32_t>(std::min<int64_t>(kFinalPerTile, qe - e0)), 0));
+    }
+    size_t o = 0;
+    h->off_mats = o;
+    o = align256(o + h->mats.size() * sizeof(PsgdMat));
+    h->off_tp = o;
+    o = align256(o + h->t_p.size() * sizeof(int4));
+    h->off_tq = o;
+    o = align256(o + h->t_q.size() * sizeof(int4));
+    h->off_tf = o;
+    o = align256(o + h->t_f.size() * sizeof(int4));
+    h->off_to = o;
+    o = align256(o + h->t_o.size() * sizeof(int4));
+    h->off_vecs = o;
+    o = align256(o + h->vecs.size() * sizeof(PsgdVec));
+    h->off_P = o;
+    o = align256(o + static_cast<size_t>(h->p_elems) * sizeof(float));
+    h->off_QP = o;
+    o = align256(o + static_cast<size_t>(h->qp_elems) * sizeof(float));
+    h->ws_bytes = std::max<size_t>(o, 256);
+    *out = h;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_powersgd_sizes(const ddp_powersgd* h, int64_t* workspace_bytes, int64_t* q_elems,
+                                         int32_t* nmatrices)
+{
+    if (!h) return ddp::fail(DDP_E_INVAL, "ddp_powersgd_sizes: handle is NULL");
+    if (workspace_bytes) *workspace_bytes = static_cast<int64_t>(h->ws_bytes);
+    if (q_elems) *q_elems = h->q_elems;
+    if (nmatrices) *nmatrices = static_cast<int32_t>(h->mats.size());
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_powersgd_matrix(const ddp_powersgd* h, int32_t seg, int64_t* q_offset, int32_t* rows,
+                                          int32_t* cols, int32_t* rank_eff, int32_t* rank_pad)
+{
+    const char* fn = "ddp_powersgd_matrix";
+    if (!h) return ddp::fail(DDP_E_INVAL, "%s: handle is NULL", fn);
+    if (seg < 0 || seg >= h->nseg) return ddp::fail(DDP_E_INVAL, "%s: segment %d outside [0, %d)", fn, seg, h->nseg);
+    const int32_t mi = h->seg_mat[seg];
+    if (mi < 0) return ddp::fail(DDP_E_INVAL, "%s: segment %d is a 1-D tensor", fn, seg);
+    const PsgdMat& m = h->mats[mi];
+    if (q_offset) *q_offset = m.q_off;
+    if (rows) *rows = m.M;
+    if (cols) *cols = m.N;
+    if (rank_eff) *rank_eff = m.r;
+    if (rank_pad) *rank_pad = h->RP;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_powersgd_bind(ddp_powersgd* h, void* workspace, int64_t workspace_bytes, float* q_state,
+                                        float* error, int64_t error_stride, void* stream)
+{
+    using ddp::fail;
+    const char* fn = "ddp_powersgd_bind";
+    if (!h) return fail(DDP_E_INVAL, "%s: handle is NULL", fn);
+    if (!workspace || workspace_bytes < static_cast<int64_t>(h->ws_bytes))
+        return fail(DDP_E_INVAL, "%s: workspace of %lld bytes, %lld needed", fn, static_cast<long long>(workspace_bytes),
+                    static_cast<long long>(h->ws_bytes));
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return fail(DDP_E_INVAL, "%s: workspace not 256-byte aligned", fn);
+    if (h->q_elems > 0 && (!q_state || reinterpret_cast<uintptr_t>(q_state) % 16 != 0))
+        return fail(DDP_E_INVAL, "%s: q_state is NULL or not 16-byte aligned", fn);
+    if (h->ef && !h->mats.empty() && (!error || error_stride < h->bucket_numel))
+        return fail(DDP_E_INVAL, "%s: error feedback needs an error buffer with stride >= %lld", fn,
+                    static_cast<long long>(h->bucket_numel));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto put = [&](size_t off, const void* src, size_t bytes) {
+        return bytes == 0 ? cudaSuccess : cudaMemcpyAsync(ws + off, src, bytes, cudaMemcpyHostToDevice, s);
+    };
+    cudaError_t e = put(h->off_mats, h->mats.data(), h->mats.size() * sizeof(PsgdMat));
+    if (e == cudaSuccess) e = put(h->off_tp, h->t_p.data(), h->t_p.size() * sizeof(int4));
+    if (e == cudaSuccess) e = put(h->off_tq, h->t_q.data(), h->t_q.size() * sizeof(int4));
+    if (e == cudaSuccess) e = put(h->off_tf, h->t_f.data(), h->t_f.size() * sizeof(int4));
+    if (e == cudaSuccess) e = put(h->off_to, h->t_o.data(), h->t_o.size() * sizeof(int4));
+    if (e == cudaSuccess) e = put(h->off_vecs, h->vecs.data(), h->vecs.size() * sizeof(PsgdVec));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(DDP_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    h->ws = ws;
+    h->q = q_state;
+    h->err = h->ef ? error : nullptr;
+    h->estride = error_stride;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_powersgd_set_q(ddp_powersgd* h, int32_t seg, const float* q, void* stream)
+{
+    using ddp::fail;
+    const char* fn = "ddp_powersgd_set_q";
+    if (!h) return fail(DDP_E_INVAL, "%s: handle is NULL", fn);
+    if (!h->q) return fail(DDP_E_STATE, "%s: call ddp_powersgd_bind first", fn);
+    if (seg < 0 || seg >= h->nseg || h->seg_mat[seg] < 0)
+        return fail(DDP_E_INVAL, "%s: segment %d is not a matrix of this bucket", fn, seg);
+    if (!q) return fail(DDP_E_INVAL, "%s: q is NULL", fn);
+    const PsgdMat& m = h->mats[h->seg_mat[seg]];
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* dst = h->q + m.q_off;
+    const size_t pitch = static_cast<size_t>(h->RP) * sizeof(float);
+    cudaError_t e = cudaMemsetAsync(dst, 0, static_cast<size_t>(m.N) * pitch, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(dst, pitch, q, static_cast<size_t>(m.r) * sizeof(float), static_cast<size_t>(m.r) * sizeof(float),
+                              static_cast<size_t>(m.N), cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return fail(DDP_E_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replica_stride, void* stream)
+{
+    using ddp::fail;
+    const char* fn = "ddp_powersgd_reduce";
+    if (!h) return fail(DDP_E_INVAL, "%s: handle is NULL", fn);
+    if (!main_grad) return fail(DDP_E_INVAL, "%s: main_grad is NULL", fn);
+    if (h->W > 1 && replica_stride < h->bucket_numel)
+        return fail(DDP_E_INVAL, "%s: replica_stride %lld < bucket numel %lld", fn, static_cast<long long>(replica_stride),
+                    static_cast<long long>(h->bucket_numel));
+    if (h->iter < h->start_iter) {
+        const ddp_status st = ddp::launch_allreduce(main_grad, replica_stride, h->bucket_numel, h->W, DDP_ALLREDUCE, stream);
+        if (st == DDP_OK) ++h->iter;
+        return st;
+    }
+    if (!h->ws) return fail(DDP_E_STATE, "%s: call ddp_powersgd_bind first", fn);
+    PsgdArgs a{};
+    a.mg = main_grad;
+    a.stride = replica_stride;
+    a.err = h->err;
+    a.estride = h->estride;
+    a.P = reinterpret_cast<float*>(h->ws + h->off_P);
+    a.Q = h->q;
+    a.QP = reinterpret_cast<float*>(h->ws + h->off_QP);
+    a.mats = reinterpret_cast<const PsgdMat*>(h->ws + h->off_mats);
+    a.W = h->W;
+    a.ef = h->ef && h->err;
+    auto al16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    a.vec_ok = al16(main_grad) && replica_stride % 4 == 0 && (!a.ef || (al16(h->err) && h->estride % 4 == 0));
+    a.rows_p = h->rows_p;
+    a.inv_w = 1.0f / static_cast<float>(h->W);
+    a.nvec = h->nvec;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ddp_status st;
+    switch (h->RP) {
+    case 1: st = launch_all<1>(*h, a, s); break;
+    case 2: st = launch_all<2>(*h, a, s); break;
+    case 4: st = launch_all<4>(*h, a, s); break;
+    default: st = launch_all<8>(*h, a, s); break;
+    }
+    if (st != DDP_OK) return st;
+    ++h->iter;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_powersgd_iter(const ddp_powersgd* h, int32_t* iter)
+{
+    if (!h || !iter) return ddp::fail(DDP_E_INVAL, "ddp_powersgd_iter: NULL argument");
+    *iter = h->iter;
+    return ddp::ok();
+}
+
+extern "C" void ddp_powersgd_destroy(ddp_powersgd* h) { delete h; }
+
+int32_t ddp::powersgd_replicas(const ddp_powersgd* h) { return h->W; }
+int64_t ddp::powersgd_numel(const ddp_powersgd* h) { return h->bucket_numel; }

@@ -92,6 +92,8 @@ struct ddp_reducer {
     cudaEvent_t fu_copied = nullptr; // the last host-to-device copy of the bitmap has been read
     bool fu_copy_pending = false;
 
+    std::vector<ddp_powersgd*> hooks;  // per bucket: the PowerSGD hook, or null
+
     bool dry() const { return flags & DDP_R_DRY_RUN; }
     uint8_t* host_bitmap() { return dry() ? fu_host_dry.data() : fu_host; }
     // flags the packs read (replica w used p) and the ones unpack reads (anyone used p)
@@ -125,6 +127,13 @@ struct ddp_reducer {
         float* mgb = mg ? mg + start[b] : nullptr;
         void* st = static_cast<void*>(side);
         const bool copy_back = flags & DDP_R_COPY_BACK;
+        if (hooks[b]) {   // communication hook: pack, the hook's reduction, copy-back
+            ddp_status s = ddp::launch_pack(d, grads, pack_used(), ld, W, mgb, stride, accumulate, st);
+            if (s == DDP_OK) s = ddp_powersgd_reduce(hooks[b], mgb, stride, st);
+            if (s == DDP_OK && copy_back)
+                s = ddp::launch_unpack(d, mgb, stride, W, mode, grads_out, ld, unpack_used(), st);
+            return s;
+        }
         if (flags & DDP_R_FUSED)
             return ddp::launch_fused(d, grads, pack_used(), ld, W, mode, accumulate, mgb, stride,
                                      copy_back ? grads_out : nullptr, unpack_used(), st, wire());
@@ -154,6 +163,17 @@ struct ddp_reducer {
             }
         }
         const bool timing = flags & DDP_R_TIMING;
+        bool hooked = false;
+        for (int32_t i = 0; i < count; ++i) hooked = hooked || hooks[order[pos + i]];
+        if (hooked && count > 1) {   // hooked buckets go out one by one
+            for (int32_t i = 0; i < count; ++i) {
+                const int32_t b = order[pos + i];
+                if (timing && !cuda_ok(cudaEventRecord(t_begin[b], side), "cudaEventRecord", &st)) return st;
+                if ((st = launch_bucket(b)) != DDP_OK) return st;
+                if (timing && !cuda_ok(cudaEventRecord(t_end[b], side), "cudaEventRecord", &st)) return st;
+            }
+            return DDP_OK;
+        }
         if (count > 1) {
             if (timing)
                 for (int32_t i = 0; i < count; ++i)
@@ -362,6 +382,7 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
     r->producers.resize(nbuckets);
     r->ready.resize(nbuckets);
     r->gates.resize(nbuckets);
+    r->hooks.assign(nbuckets, nullptr);
 
     if (!dry) {
         ddp_status st = DDP_OK;
@@ -516,6 +537,27 @@ extern "C" ddp_status ddp_reducer_find_unused(ddp_reducer* r, uint8_t* local_use
     r->fu_global = global_used;
     r->fu_count = global_count;
     r->find_unused = true;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_register_powersgd(ddp_reducer* r, int32_t bucket, ddp_powersgd* h)
+{
+    using ddp::fail;
+    const char* fn = "ddp_reducer_register_powersgd";
+    if (!r) return fail(DDP_E_INVAL, "%s: reducer is NULL", fn);
+    if (bucket < 0 || bucket >= r->nbuckets) return fail(DDP_E_INVAL, "%s: bucket %d outside [0, %d)", fn, bucket, r->nbuckets);
+    if (r->phase == Phase::Backward) return fail(DDP_E_STATE, "%s: called inside an iteration", fn);
+    if (h) {
+        if (r->mode != DDP_ALLREDUCE) return fail(DDP_E_INVAL, "%s: the hook replaces an allreduce, not a reduce_scatter", fn);
+        if (!r->mg && !r->dry()) return fail(DDP_E_INVAL, "%s: the hook works on main_grad; the reducer has none", fn);
+        if (ddp::powersgd_replicas(h) != r->W)
+            return fail(DDP_E_INVAL, "%s: state planned for W = %d, reducer has W = %d", fn, ddp::powersgd_replicas(h), r->W);
+        if (ddp::powersgd_numel(h) != r->buckets[bucket].numel)
+            return fail(DDP_E_INVAL, "%s: state planned for %lld elements, bucket %d has %lld", fn,
+                        static_cast<long long>(ddp::powersgd_numel(h)), bucket,
+                        static_cast<long long>(r->buckets[bucket].numel));
+    }
+    r->hooks[bucket] = h;
     return ddp::ok();
 }
 

@@ -14,7 +14,7 @@ from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, 
                ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
                ddp_reducer_find_unused, ddp_reducer_mark_ready_many, ddp_reducer_prepare,
-               ddp_reducer_set_local_used)
+               ddp_reducer_register_powersgd, ddp_reducer_set_local_used)
 
 
 class BucketReducer:
@@ -29,7 +29,10 @@ class BucketReducer:
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads, used=None,
                  grads_out=None, fused=True, timing=False, side_stream=None, main_grad=True, grad_reduce_in_fp32=1,
-                 coalesce=False, wire=None):
+                 coalesce=False, wire=None, powersgd=None):
+        """powersgd: dict(rank, shapes, q0, error_feedback=True, start_iter=0) registers the
+        PowerSGD hook on every bucket; shapes[p] is parameter p's shape and q0(p, n, r)
+        its initial Q (n x r), the hook's random draw."""
         import torch
 
         self.W, self.mode = int(W), int(mode)
@@ -51,6 +54,22 @@ class BucketReducer:
                                          None, P, self.main_grad, self.plan.replica_stride, self.out_tab,
                                          None, self.side)
         self.ready_order = np.arange(P - 1, -1, -1, dtype=np.int32)
+        self.hooks = []
+        if powersgd is not None:
+            from .powersgd import PowerSGDBucket
+
+            cfg = dict(error_feedback=True, start_iter=0)
+            cfg.update(powersgd)
+            for b in range(self.plan.nbuckets):
+                mem = self.plan.members[b]
+                hook = PowerSGDBucket(self.W, cfg["rank"], [int(self.plan.offset_of[p]) for p in mem],
+                                      [int(self.plan.numels[p]) for p in mem], [cfg["shapes"][p] for p in mem],
+                                      int(self.plan.bucket_numel[b]),
+                                      lambda k, n, r, mem=mem: cfg["q0"](mem[k], n, r),
+                                      error_feedback=cfg["error_feedback"], start_iter=cfg["start_iter"],
+                                      device=self.plan.device, stream=self.side)
+                ddp_reducer_register_powersgd(self.handle, b, hook.handle)
+                self.hooks.append(hook)
         if used is not None:
             # find_unused_parameters: the reducer uploads the host bitmap at every prepare,
             # all-reduces it on the side stream and marks the parameters nobody used
@@ -114,6 +133,9 @@ class BucketReducer:
         if self.handle:
             ddp_reducer_destroy(self.handle)
             self.handle = None
+        for h in getattr(self, "hooks", []):
+            h.close()
+        self.hooks = []
 
     def __del__(self):
         try:

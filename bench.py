@@ -674,6 +674,105 @@ def run_bitmap(args):
     return line
 
 
+def powersgd_bytes(wl, plan, b, rank, ef=True):
+    """Algorithmic HBM bytes of one compressed hook call on bucket b, and the elements
+    a rank would all-reduce (P and Q of every matrix, the 1-D tensors whole).
+    Per matrix element and replica: P pass reads G (and E, writing M back to E),
+    the Q pass reads M, the output pass writes the result (and reads M, writes E):
+    12 + 4 + 12 bytes with error feedback, 4 + 4 + 4 without.  1-D tensors: W
+    reads and W writes of 4 bytes."""
+    W = wl.W
+    nbytes, comm, elems = 0, 0, 0
+    for p in plan.members[b]:
+        shape, n = wl.shapes[p], wl.numels[p]
+        elems += n
+        if len(shape) >= 2:
+            m, k = shape[0], n // shape[0]
+            nbytes += W * n * (28 if ef else 12)
+            comm += (m + k) * min(rank, m, k)
+        else:
+            nbytes += 2 * W * n * 4
+            comm += n
+    return nbytes, comm, elems
+
+
+def run_powersgd(args):
+    """The PowerSGD hook (DDP chapter 17.27) on ResNet-50's buckets, W = 8, error
+    feedback, rank --psgd-rank: (1) ddp_powersgd_reduce alone per bucket against
+    ddp_bucket_allreduce on the same packed bucket; (2) the reducer's step with every
+    bucket hooked against the plain fused step.  CUDA events on the launching
+    stream, inputs resident and larger than L2.  One JSON line."""
+    import torch
+
+    import allreduce_ddp_assign_gb300 as D
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    dev = torch.device("cuda", 0)
+    D.lib()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    rank = args.psgd_rank
+    wl = WL.c7_resnet50_powersgd(rank)
+    grads = [[WL.grad_torch(wl, p, w, 0, dev) for p in range(wl.nparams)] for w in range(wl.W)]
+    cfg = dict(rank=rank, shapes=wl.shapes, q0=lambda p, n, r: WL.powersgd_q0_np(wl.seed, p, n, r))
+    sess = BucketReducer(wl.numels, None, wl.W, wl.mode, wl.order, wl.cap_bytes, wl.first_cap_bytes,
+                         wl.pad_multiple, grads, powersgd=cfg)
+    plain = BucketReducer(wl.numels, None, wl.W, wl.mode, wl.order, wl.cap_bytes, wl.first_cap_bytes,
+                          wl.pad_multiple, grads, coalesce=True)
+    plan = sess.plan
+    comp = torch.cuda.current_stream()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(comp)
+        for _ in range(reps):
+            fn()
+        b.record(comp)
+        b.synchronize()
+        return a.elapsed_time(b) / reps
+
+    sess.step(comp, comp)   # packs the buckets once
+    torch.cuda.synchronize()
+    per_bucket = []
+    tot_bytes = tot_comm = tot_elems = 0
+    t_hook = t_ring = 0.0
+    for b in range(plan.nbuckets):
+        mg = plan.main_grad_at(sess.main_grad, b)
+        nb, cm, el = powersgd_bytes(wl, plan, b, rank)
+        th = timed(lambda: sess.hooks[b].reduce(mg, plan.replica_stride, comp), args.steps)
+        tr = timed(lambda: D.ddp_bucket_allreduce(mg, plan.replica_stride, int(plan.bucket_numel[b]), wl.W,
+                                                  D.DDP_ALLREDUCE, comp), args.steps)
+        per_bucket.append({"bucket": b, "elements": el, "hook_us": round(th * 1e3, 2), "ring_us": round(tr * 1e3, 2),
+                           "hook_GBps": round(nb / (th * 1e-3) / 1e9, 1), "compression": round(el / cm, 1)})
+        tot_bytes += nb
+        tot_comm += cm
+        tot_elems += el
+        t_hook += th
+        t_ring += tr
+    step_hook = timed(lambda: sess.step(comp, comp), max(args.steps // 4, 10))
+    step_plain = timed(lambda: plain.step(comp, comp), max(args.steps // 4, 10))
+    achieved = tot_bytes / (t_hook * 1e-3) / 1e9
+    line = {"powersgd": True, "workload": wl.name, "rank": rank, "W": wl.W, "error_feedback": True,
+            "hook_ms_per_step": round(t_hook, 4), "ring_allreduce_ms_per_step": round(t_ring, 4),
+            "reducer_step_ms": {"powersgd": round(step_hook, 4), "plain_fused_coalesced": round(step_plain, 4)},
+            "compression_ratio": round(tot_elems / tot_comm, 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "bytes_per_step": tot_bytes,
+                         "kernel": "the hook's six launches per bucket, summed"},
+            "per_bucket": per_bucket, "steps": args.steps}
+    print(json.dumps(line), flush=True)
+    sess.close()
+    plain.close()
+    return line
+
+
 def run_overlap(args, wl=None):
     """The reducer's overlap with a synthetic backward ("Lecture 15: PyTorch DDP" 3.1):
     the compute stream runs one bounded spin kernel per parameter, in reverse order,
@@ -795,6 +894,8 @@ def main(argv=None):
     ap.add_argument("--sweep-max-bytes", type=int, default=0)
     ap.add_argument("--overlap", action="store_true", help="overlap with a synthetic backward (JSON line)")
     ap.add_argument("--bitmap", action="store_true", help="find_unused bitmap all-reduce (JSON line)")
+    ap.add_argument("--powersgd", action="store_true", help="PowerSGD hook on ResNet-50 (JSON line)")
+    ap.add_argument("--psgd-rank", type=int, default=4)
     ap.add_argument("--backward-ms", type=float, default=3.0)
     args = ap.parse_args(argv)
     if args.sweep:
@@ -803,6 +904,8 @@ def main(argv=None):
         return run_overlap(args)
     if args.bitmap:
         return run_bitmap(args)
+    if args.powersgd:
+        return run_powersgd(args)
     wl = WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, wl)

@@ -367,6 +367,101 @@ ddp_status ddp_used_allreduce(const uint8_t* local_used, int32_t ld, int32_t W, 
                               int32_t* global_count, uint8_t* global_used, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* The PowerSGD communication hook (device)                                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * A PowerSGD state object for one bucket: the hook of DDP chapter 17.27
+ * (Vogels et al., PowerSGD), applied in place to the W replicas of the
+ * bucket's fp32 main_grad in place of ddp_bucket_allreduce.
+ *
+ * Per iteration, after start_iter plain all-reduces of the whole bucket:
+ *   - every 1-D tensor (seg_rows == 0) gets the ring mean of the concatenation
+ *     of the bucket's 1-D tensors (same arithmetic as ddp_bucket_allreduce);
+ *   - every tensor with seg_rows = M > 0, viewed as M x N (N = numel / M, the
+ *     tensor's shape[0] x the rest), rank R' = min(rank, M, N):
+ *       M_w = G_w + E_w              (error feedback; E_w = 0 without it)
+ *       P   = sum_w M_w Q            (Q: N x R', the warm-started state)
+ *       P   = orthonormal columns of P (Gram-Schmidt; a zero column stays 0)
+ *       Q   = (sum_w M_w^T P) / W    (kept as the next iteration's Q)
+ *       every replica's tensor = P Q^T;  E_w = M_w - P Q^T
+ * The bucket's padding is left alone once compression starts.  Sums over
+ * replicas are taken in replica order; P and Q products accumulate in fp32
+ * with fused multiply-adds (the orthonormalisation's dot products in fp64), so
+ * results match an exact evaluation to within rounding, not bit for bit.
+ *
+ * Memory (all the caller's; the library allocates none):
+ *   workspace  DEVICE, ddp_powersgd_sizes bytes, 256-byte aligned: tile
+ *              tables (written by ddp_powersgd_bind) and the scratch P and
+ *              partial sums of Q (overwritten by every reduce).
+ *   q_state    DEVICE fp32, q_elems: every matrix's Q as N rows of rank_pad
+ *              floats (ddp_powersgd_matrix gives the offset); columns past
+ *              the effective rank must be 0.  ddp_powersgd_set_q writes one
+ *              matrix's initial Q (the hook's random draw is the caller's).
+ *   error      DEVICE fp32, W replicas of the bucket layout with stride
+ *              error_stride >= bucket_numel; must start at 0; only the
+ *              matrices' elements are used.  NULL without error feedback.
+ */
+typedef struct ddp_powersgd ddp_powersgd;
+
+/*
+ * ddp_powersgd_create -- plan the hook for one bucket (HOST only).
+ *   W                 replicas, 1..64.
+ *   rank              1..8 (padded internally to 1, 2, 4 or 8).
+ *   nseg              tensors in the bucket.
+ *   seg_offset, seg_numel  HOST int64[nseg]: element offset and size of each
+ *                     tensor in the bucket (as from ddp_assign_buckets).
+ *   seg_rows          HOST int64[nseg]: the matrix view's rows (shape[0]) of a
+ *                     tensor of two or more dimensions, 0 for a 1-D tensor.
+ *   bucket_numel      elements of the bucket, padding included.
+ *   error_feedback    0/1.   start_iter  plain all-reduce iterations first.
+ * Errors: DDP_E_INVAL (ranges; a segment outside the bucket; numel not a
+ * multiple of rows; N x rank_pad above 2^30).
+ */
+ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg, const int64_t* seg_offset,
+                               const int64_t* seg_numel, const int64_t* seg_rows, int64_t bucket_numel,
+                               int32_t error_feedback, int32_t start_iter, ddp_powersgd** out);
+
+/* Sizes of the caller's buffers (any output may be NULL); nmatrices = tensors compressed. */
+ddp_status ddp_powersgd_sizes(const ddp_powersgd* h, int64_t* workspace_bytes, int64_t* q_elems,
+                              int32_t* nmatrices);
+
+/* Layout of segment seg's Q inside q_state.  DDP_E_INVAL for a 1-D segment. */
+ddp_status ddp_powersgd_matrix(const ddp_powersgd* h, int32_t seg, int64_t* q_offset, int32_t* rows,
+                               int32_t* cols, int32_t* rank_eff, int32_t* rank_pad);
+
+/*
+ * ddp_powersgd_bind -- attach the caller's buffers and copy the tile tables
+ * into the workspace on `stream` (waits for the copy).  The buffers must stay
+ * valid while reductions use them.
+ * Errors: DDP_E_INVAL (workspace too small or unaligned, q_state NULL or not
+ * 16-byte aligned, error buffer missing with error feedback); DDP_E_CUDA.
+ */
+ddp_status ddp_powersgd_bind(ddp_powersgd* h, void* workspace, int64_t workspace_bytes, float* q_state,
+                             float* error, int64_t error_stride, void* stream);
+
+/*
+ * ddp_powersgd_set_q -- write segment seg's initial Q from HOST q[N x R']
+ * (row-major), zeroing the padding columns; waits for the copy on `stream`.
+ * Errors: DDP_E_INVAL (not a matrix segment, q NULL); DDP_E_STATE (not bound).
+ */
+ddp_status ddp_powersgd_set_q(ddp_powersgd* h, int32_t seg, const float* q, void* stream);
+
+/*
+ * ddp_powersgd_reduce -- one iteration of the hook on the bucket's W replicas:
+ * main_grad (DEVICE) is replica 0's bucket, replica w starts replica_stride
+ * elements later.  Asynchronous on `stream`; advances the iteration count.
+ * Two reductions with the same state must not overlap.
+ * Errors: DDP_E_INVAL (NULL main_grad, stride < bucket_numel); DDP_E_STATE
+ * (compressing before ddp_powersgd_bind); DDP_E_CUDA.
+ */
+ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replica_stride, void* stream);
+
+/* Iterations done so far (plain and compressed). */
+ddp_status ddp_powersgd_iter(const ddp_powersgd* h, int32_t* iter);
+
+void ddp_powersgd_destroy(ddp_powersgd* h);
+
+/* ------------------------------------------------------------------------ */
 /* Steps 2-4 fused (device)                                                  */
 /* ------------------------------------------------------------------------ */
 /*
@@ -536,6 +631,17 @@ ddp_status ddp_reducer_find_unused(ddp_reducer* r, uint8_t* local_used, uint8_t*
  * (find_unused is off, or inside an iteration); DDP_E_CUDA.
  */
 ddp_status ddp_reducer_set_local_used(ddp_reducer* r, const uint8_t* flags, int32_t ld);
+
+/*
+ * ddp_reducer_register_powersgd -- register the PowerSGD hook (DDP chapter
+ * 17.27, register_comm_hook) for bucket `bucket`: from then on its issue is
+ * pack, ddp_powersgd_reduce on the side stream, and the copy-back when
+ * DDP_R_COPY_BACK is set (never coalesced with other buckets).  NULL removes
+ * the hook.  The state object stays the caller's and must be bound.
+ * Errors: DDP_E_INVAL (bucket out of range, a reduce_scatter reducer, no
+ * main_grad, a state planned for another W); DDP_E_STATE (inside an iteration).
+ */
+ddp_status ddp_reducer_register_powersgd(ddp_reducer* r, int32_t bucket, ddp_powersgd* h);
 
 /*
  * ddp_reducer_mark_ready -- the autograd hook of parameter `param` fired: its

@@ -76,6 +76,7 @@ class State:
     start_iter: int = 0
     iter: int = 0
     error: list = field(default_factory=list)   # error[w][t]: M x N float64 (None for 1-D)
+    cond: dict = field(default_factory=dict)    # per tensor: 2-norm condition number of the last P (for tolerances)
 
     def __post_init__(self):
         if not self.error:
@@ -137,6 +138,8 @@ def step(state: State, bucket: np.ndarray, seg_offset, orc) -> np.ndarray:
             mw.append(g + state.error[w][t] if state.error_feedback else g)
         q = state.q[t]
         p = sum(mw[w] @ q for w in range(W))
+        sv = np.linalg.svd(p, compute_uv=False)
+        state.cond[t] = float(sv[0] / sv[-1]) if sv[-1] > 0 else float("inf")
         p = _orthonormal(p)
         qn = sum(mw[w].T @ p for w in range(W)) / W
         approx = p @ qn.T

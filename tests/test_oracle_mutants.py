@@ -86,7 +86,7 @@ def test_mutant_is_caught(name, tmp_path):
 # the PowerSGD oracle (Python): each mutant is a patched copy of the module
 # ---------------------------------------------------------------------------
 PSGD_MUTANTS = {
-    "p_not_all_reduced": [("p = sum(mw[w] @ q for w in range(W))", "p = mw[0] @ q")],
+    "p_not_all_reduced": [("p = sum(mw[w] @ q for w in range(W))\n", "p = mw[0] @ q\n")],
     "p_not_orthogonalised": [("        p = _orthonormal(p)\n", "")],
     "q_not_divided_by_world": [("qn = sum(mw[w].T @ p for w in range(W)) / W", "qn = sum(mw[w].T @ p for w in range(W))")],
     "error_not_fed_back": [("mw.append(g + state.error[w][t] if state.error_feedback else g)", "mw.append(g)")],
