@@ -84,6 +84,7 @@ _SIGS = {
     "ddp_powersgd_bind": (C.c_int32, [_vp, _vp, C.c_int64, _vp, _vp, C.c_int64, _vp]),
     "ddp_powersgd_set_q": (C.c_int32, [_vp, C.c_int32, _vp, _vp]),
     "ddp_powersgd_reduce": (C.c_int32, [_vp, _vp, C.c_int64, _vp]),
+    "ddp_powersgd_reduce_static": (C.c_int32, [_vp, _vp, C.c_int64, _vp]),
     "ddp_powersgd_iter": (C.c_int32, [_vp, _i32p]),
     "ddp_powersgd_destroy": (None, [_vp]),
     "ddp_reducer_set_local_used": (C.c_int32, [_vp, _vp, C.c_int32]),
@@ -373,6 +374,10 @@ def ddp_powersgd_set_q(h, seg, q, stream=None) -> None:
 
 def ddp_powersgd_reduce(h, main_grad, replica_stride, stream=None) -> None:
     _check(lib().ddp_powersgd_reduce(h, _ptr(main_grad), int(replica_stride), _stream(stream)))
+
+
+def ddp_powersgd_reduce_static(h, main_grad, replica_stride, stream=None) -> None:
+    _check(lib().ddp_powersgd_reduce_static(h, _ptr(main_grad), int(replica_stride), _stream(stream)))
 
 
 def ddp_powersgd_iter(h) -> int:

@@ -29,6 +29,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "common.h"
@@ -684,3 +685,96 @@ extern "C" void ddp_powersgd_destroy(ddp_powersgd* h) { delete h; }
 
 int32_t ddp::powersgd_replicas(const ddp_powersgd* h) { return h->W; }
 int64_t ddp::powersgd_numel(const ddp_powersgd* h) { return h->bucket_numel; }
+
+// ---------------------------------------------------------------------------
+// ddp_powersgd_reduce_static: the same kernels with their scratch (the summed
+// P and the partial sums of Q) in a fixed device array of this library instead
+// of the caller's workspace.  Nothing of that scratch is read before the same
+// call has written it, so nothing needs clearing.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int64_t kStaticScratchBytes = DDP_POWERSGD_STATIC_SCRATCH_BYTES;
+constexpr int64_t kStaticScratchFloats = kStaticScratchBytes / static_cast<int64_t>(sizeof(float));
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) float g_psgd_static_scratch[kStaticScratchFloats];
+
+std::mutex g_static_mu;
+float* g_static_ptr[kMaxDevices] = {};
+
+// The array's address on the current device, looked up once per device.
+ddp_status static_scratch(float** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_powersgd_reduce_static: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return ddp::fail(DDP_E_INVAL, "ddp_powersgd_reduce_static: device %d beyond the %d supported", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_psgd_static_scratch);
+        if (e != cudaSuccess)
+            return ddp::fail(DDP_E_CUDA, "ddp_powersgd_reduce_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        g_static_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_static_ptr[dev];
+    return DDP_OK;
+}
+
+}  // namespace
+
+extern "C" ddp_status ddp_powersgd_reduce_static(ddp_powersgd* h, float* main_grad, int64_t replica_stride,
+                                                 void* stream)
+{
+    using ddp::fail;
+    const char* fn = "ddp_powersgd_reduce_static";
+    if (!h) return fail(DDP_E_INVAL, "%s: handle is NULL", fn);
+    if (!main_grad) return fail(DDP_E_INVAL, "%s: main_grad is NULL", fn);
+    if (h->W > 1 && replica_stride < h->bucket_numel)
+        return fail(DDP_E_INVAL, "%s: replica_stride %lld < bucket numel %lld", fn, static_cast<long long>(replica_stride),
+                    static_cast<long long>(h->bucket_numel));
+    const int64_t p_floats = (h->p_elems + 63) & ~static_cast<int64_t>(63);   // QP starts 256-byte aligned
+    const int64_t need = p_floats + h->qp_elems;
+    if (need > kStaticScratchFloats)
+        return fail(DDP_E_CAPACITY, "%s: this bucket needs %lld bytes of scratch, the static array holds %lld "
+                    "(use ddp_powersgd_reduce with a workspace)", fn, static_cast<long long>(need * 4),
+                    static_cast<long long>(kStaticScratchBytes));
+    if (h->iter < h->start_iter) {
+        const ddp_status st = ddp::launch_allreduce(main_grad, replica_stride, h->bucket_numel, h->W, DDP_ALLREDUCE, stream);
+        if (st == DDP_OK) ++h->iter;
+        return st;
+    }
+    if (!h->ws) return fail(DDP_E_STATE, "%s: call ddp_powersgd_bind first", fn);
+    float* scratch = nullptr;
+    const ddp_status sst = static_scratch(&scratch);
+    if (sst != DDP_OK) return sst;
+    PsgdArgs a{};
+    a.mg = main_grad;
+    a.stride = replica_stride;
+    a.err = h->err;
+    a.estride = h->estride;
+    a.P = scratch;
+    a.Q = h->q;
+    a.QP = scratch + p_floats;
+    a.mats = reinterpret_cast<const PsgdMat*>(h->ws + h->off_mats);
+    a.W = h->W;
+    a.ef = h->ef && h->err;
+    auto al16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    a.vec_ok = al16(main_grad) && replica_stride % 4 == 0 && (!a.ef || (al16(h->err) && h->estride % 4 == 0));
+    a.rows_p = h->rows_p;
+    a.inv_w = 1.0f / static_cast<float>(h->W);
+    a.nvec = h->nvec;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ddp_status st;
+    switch (h->RP) {
+    case 1: st = launch_all<1>(*h, a, s); break;
+    case 2: st = launch_all<2>(*h, a, s); break;
+    case 4: st = launch_all<4>(*h, a, s); break;
+    default: st = launch_all<8>(*h, a, s); break;
+    }
+    if (st != DDP_OK) return st;
+    ++h->iter;
+    return ddp::ok();
+}

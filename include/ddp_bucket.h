@@ -456,6 +456,28 @@ ddp_status ddp_powersgd_set_q(ddp_powersgd* h, int32_t seg, const float* q, void
  */
 ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replica_stride, void* stream);
 
+/*
+ * ddp_powersgd_reduce_static -- ddp_powersgd_reduce, allocating nothing and
+ * using no caller scratch: the kernels' scratch (the summed P and the partial
+ * sums of Q) lives in a fixed device array of DDP_POWERSGD_STATIC_SCRATCH_BYTES
+ * (8 MiB) inside the library.  The pages have no counterpart: this is an
+ * entry point of this library for callers that want no scratch allocation at
+ * all.  The workspace bound by ddp_powersgd_bind still supplies the tile
+ * tables; its scratch part is not used.
+ *
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's address (cudaGetSymbolAddress) and keeps it; make that first
+ * call before any stream capture.  Nothing of the scratch is read before the
+ * same call writes it, so nothing needs clearing.  Calls that overlap in time
+ * (any state objects, any streams, on one device) share the array and race:
+ * serialise them.  Results are identical to ddp_powersgd_reduce's.
+ * Errors: as ddp_powersgd_reduce; DDP_E_CAPACITY when the bucket's scratch
+ * (ddp_powersgd_sizes minus the tables) exceeds the array; DDP_E_CUDA if the
+ * address lookup fails.
+ */
+#define DDP_POWERSGD_STATIC_SCRATCH_BYTES (8ll << 20)
+ddp_status ddp_powersgd_reduce_static(ddp_powersgd* h, float* main_grad, int64_t replica_stride, void* stream);
+
 /* Iterations done so far (plain and compressed). */
 ddp_status ddp_powersgd_iter(const ddp_powersgd* h, int32_t* iter);
 
