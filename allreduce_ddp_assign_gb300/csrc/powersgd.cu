@@ -13,15 +13,16 @@
 //   psgd_vec_kernel     1-D tensors: ring-ordered mean over their concatenation
 //   psgd_p_kernel       per (row, replica): M = G + E (stored back into E),
 //                       P_w[row] = M[row, :] Q; then the sum over replicas
-//   psgd_orth_kernel    per tensor: modified Gram-Schmidt on P's columns
-//   psgd_qpart_kernel   per (column block, row split, replica): partial M^T P
+//   psgd_orth_kernel    per tensor: P <- P R^-1, R the Cholesky factor of P^T P
+//   psgd_qpart_kernel   per (column block, row split, replica): partial M^T P,
+//                       the split's rows shared by the block's warps
 //   psgd_qfinal_kernel  Q = (sum over replicas of the sum over splits) / W
 //   psgd_out_kernel     per row: G^ = P Q^T written to every replica, E = M - G^
 // Every kernel streams its matrix once: the contraction is rank R (1..8)
 // against a row or column of M, R fused multiply-adds per element and 4 to 12
 // bytes per element, far below the CUDA cores' arithmetic ridge, so the work is
 // HBM-bound and stays on the CUDA cores in fp32.  The orthonormalisation
-// accumulates its dot products in fp64 (M x R values, negligible time).
+// forms P^T P in fp64 (M x R values, negligible time).
 //
 // Rank is padded to RP in {1, 2, 4, 8}: Q and P carry RP columns, those past a
 // tensor's effective rank min(R, M, N) are zero and stay zero.
@@ -40,8 +41,10 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsOut = kWarps;       // rows per output tile: one per warp
 constexpr int kRowsPerSplit = 256;     // rows of one partial M^T P
-constexpr int kFinalPerTile = 1024;    // Q elements per finalising tile
+constexpr int kFinalPerTile = 256;     // Q elements per finalising tile
 constexpr int kMaxPairs = 256;         // (row, replica) pairs per P tile
+constexpr int kGW = 4;                 // replicas a warp carries at once in the P pass
+constexpr int kOutBatch = 4;           // replicas whose error loads the output pass issues together
 constexpr int64_t kVecPiece = 16384;   // elements of a 1-D tensor per block
 
 struct PsgdMat {
@@ -80,9 +83,6 @@ struct PsgdArgs {
     float inv_w;
     int64_t nvec;     // length of the concatenation of the 1-D tensors
 };
-
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
 template <int RP>
 __device__ __forceinline__ void load_row(const float* __restrict__ src, float (&v)[RP])
@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(kThreads) psgd_vec_kernel(const PsgdArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// P = sum_w (G_w + E_w) Q  (tile: {mat, row0, nrows}; one warp per (row, replica))
+// P = sum_w (G_w + E_w) Q  (tile: {mat, row0, nrows}; one warp per row and
+// group of up to kGW replicas, which share the loads of Q)
 // ---------------------------------------------------------------------------
 template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
@@ -140,53 +141,89 @@ __global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
     const int4 t = a.tiles[blockIdx.x];
     const PsgdMat m = a.mats[t.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pairs = t.z * a.W;
+    const int ngroups = (a.W + kGW - 1) / kGW;
+    const int units = t.z * ngroups;
     const bool vec = m.vec && a.vec_ok;
     const float* q = a.Q + m.q_off;
-    for (int u = warp; u < pairs; u += kWarps) {
-        const int row = t.y + u / a.W, w = u % a.W;
-        float* g = a.mg + w * a.stride + m.off + static_cast<int64_t>(row) * m.N;
-        float* e = a.ef ? a.err + w * a.estride + m.off + static_cast<int64_t>(row) * m.N : nullptr;
-        float acc[RP];
+    for (int u = warp; u < units; u += kWarps) {
+        const int rl = u / ngroups, w0 = (u % ngroups) * kGW;
+        const int gw = min(kGW, a.W - w0);
+        const int64_t rowoff = m.off + static_cast<int64_t>(t.y + rl) * m.N;
+        float* g[kGW];
+        float* e[kGW];
 #pragma unroll
-        for (int r = 0; r < RP; ++r) acc[r] = 0.f;
+        for (int k = 0; k < kGW; ++k) {
+            const int w = w0 + (k < gw ? k : 0);
+            g[k] = a.mg + w * a.stride + rowoff;
+            e[k] = a.ef ? a.err + w * a.estride + rowoff : nullptr;
+        }
+        float acc[kGW][RP];
+#pragma unroll
+        for (int k = 0; k < kGW; ++k)
+#pragma unroll
+            for (int r = 0; r < RP; ++r) acc[k][r] = 0.f;
         if (vec) {
             for (int j = 4 * lane; j < m.N; j += 128) {
-                float4 x = ld4(g + j);
-                if (e) {
-                    const float4 y = ld4(e + j);
-                    x = make_float4(__fadd_rn(x.x, y.x), __fadd_rn(x.y, y.y), __fadd_rn(x.z, y.z), __fadd_rn(x.w, y.w));
-                    st4(e + j, x);
+                // every load of the step first (stores to E would otherwise keep the
+                // next replica's loads from being issued early), then the sums
+                float4 x[kGW], y[kGW];
+#pragma unroll
+                for (int k = 0; k < kGW; ++k) {
+                    if (k >= gw) continue;
+                    x[k] = __ldcs(reinterpret_cast<const float4*>(g[k] + j));
+                    if (a.ef) y[k] = __ldcs(reinterpret_cast<const float4*>(e[k] + j));
+                }
+                if (a.ef) {
+#pragma unroll
+                    for (int k = 0; k < kGW; ++k) {
+                        if (k >= gw) continue;
+                        x[k] = make_float4(__fadd_rn(x[k].x, y[k].x), __fadd_rn(x[k].y, y[k].y), __fadd_rn(x[k].z, y[k].z),
+                                           __fadd_rn(x[k].w, y[k].w));
+                        __stcs(reinterpret_cast<float4*>(e[k] + j), x[k]);
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     float qv[RP];
                     load_row<RP>(q + static_cast<int64_t>(j + c) * RP, qv);
-                    const float xc = comp(x, c);
 #pragma unroll
-                    for (int r = 0; r < RP; ++r) acc[r] = fmaf(xc, qv[r], acc[r]);
+                    for (int k = 0; k < kGW; ++k) {
+                        if (k >= gw) continue;
+                        const float xc = comp(x[k], c);
+#pragma unroll
+                        for (int r = 0; r < RP; ++r) acc[k][r] = fmaf(xc, qv[r], acc[k][r]);
+                    }
                 }
             }
         } else {
             for (int j = lane; j < m.N; j += 32) {
-                float x = g[j];
-                if (e) {
-                    x = __fadd_rn(x, e[j]);
-                    e[j] = x;
-                }
                 float qv[RP];
                 load_row<RP>(q + static_cast<int64_t>(j) * RP, qv);
 #pragma unroll
-                for (int r = 0; r < RP; ++r) acc[r] = fmaf(x, qv[r], acc[r]);
+                for (int k = 0; k < kGW; ++k) {
+                    if (k >= gw) continue;
+                    float x = g[k][j];
+                    if (a.ef) {
+                        x = __fadd_rn(x, e[k][j]);
+                        e[k][j] = x;
+                    }
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) acc[k][r] = fmaf(x, qv[r], acc[k][r]);
+                }
             }
         }
 #pragma unroll
-        for (int r = 0; r < RP; ++r)
+        for (int k = 0; k < kGW; ++k)
 #pragma unroll
-            for (int o = 16; o; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+            for (int r = 0; r < RP; ++r)
+#pragma unroll
+                for (int o = 16; o; o >>= 1) acc[k][r] += __shfl_xor_sync(0xffffffffu, acc[k][r], o);
         if (lane == 0)
 #pragma unroll
-            for (int r = 0; r < RP; ++r) part[u][r] = acc[r];
+            for (int k = 0; k < kGW; ++k)
+                if (k < gw)
+#pragma unroll
+                    for (int r = 0; r < RP; ++r) part[rl * a.W + w0 + k][r] = acc[k][r];
     }
     __syncthreads();
     // the all-reduce of P: replicas summed in order 0 .. W-1
@@ -199,117 +236,176 @@ __global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// orthonormal columns of P (one block per tensor): modified Gram-Schmidt with
-// fp64 dot products; a column whose norm is 0 becomes 0
+// orthonormal columns of P (one block per tensor): the Gram matrix P^T P in
+// fp64 (one pass; products of fp32 values are exact in fp64), its Cholesky
+// factor R (upper triangular, positive diagonal) and R^-1 on one thread, then
+// P <- P R^-1 (a second pass) -- the orthonormal basis whose triangle has a
+// positive diagonal.  A column whose pivot is not positive (zero, or in the
+// span of the earlier columns) becomes 0.
 // ---------------------------------------------------------------------------
-__device__ double block_sum(double v, double* red)
-{
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    double s = 0.0;
-    for (int k = 0; k < kWarps; ++k) s += red[k];
-    return s;
-}
-
 template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
 {
-    __shared__ double red[kWarps];
+    constexpr int NG = RP * (RP + 1) / 2;
+    __shared__ double red[kWarps][NG];
+    __shared__ float rinv[RP][RP];
     const PsgdMat m = a.mats[blockIdx.x];
     float* p = a.P + m.p_off;
-    for (int r = 0; r < m.r; ++r) {
-        for (int k = 0; k < r; ++k) {
-            double d = 0.0;
-            for (int i = threadIdx.x; i < m.M; i += kThreads)
-                d += static_cast<double>(p[static_cast<int64_t>(i) * RP + k]) * p[static_cast<int64_t>(i) * RP + r];
-            const float df = static_cast<float>(block_sum(d, red));
-            for (int i = threadIdx.x; i < m.M; i += kThreads) {
-                float* x = p + static_cast<int64_t>(i) * RP;
-                x[r] = fmaf(-df, x[k], x[r]);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    double g[NG];
+#pragma unroll
+    for (int k = 0; k < NG; ++k) g[k] = 0.0;
+    for (int i = threadIdx.x; i < m.M; i += kThreads) {
+        const float* row = p + static_cast<int64_t>(i) * RP;
+        double x[RP];
+#pragma unroll
+        for (int c = 0; c < RP; ++c) x[c] = row[c];
+        int k = 0;
+#pragma unroll
+        for (int c = 0; c < RP; ++c)
+#pragma unroll
+            for (int d = c; d < RP; ++d) g[k++] += x[c] * x[d];
+    }
+#pragma unroll
+    for (int k = 0; k < NG; ++k) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) g[k] += __shfl_xor_sync(0xffffffffu, g[k], o);
+        if (lane == 0) red[warp][k] = g[k];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double G[RP][RP], R[RP][RP], X[RP][RP];
+        bool ok[RP];
+        int k = 0;
+        for (int c = 0; c < RP; ++c)
+            for (int d = c; d < RP; ++d) {
+                double s = 0.0;
+                for (int w = 0; w < kWarps; ++w) s += red[w][k];
+                G[c][d] = G[d][c] = s;
+                ++k;
             }
-            __syncthreads();
+        for (int c = 0; c < RP; ++c)
+            for (int d = 0; d < RP; ++d) R[c][d] = X[c][d] = 0.0;
+        for (int c = 0; c < RP; ++c) {
+            ok[c] = false;
+            if (c >= m.r) continue;
+            double d = G[c][c];
+            for (int q = 0; q < c; ++q)
+                if (ok[q]) d -= R[q][c] * R[q][c];
+            if (!(d > 0.0)) continue;
+            ok[c] = true;
+            R[c][c] = sqrt(d);
+            for (int e = c + 1; e < RP; ++e) {
+                double s = G[c][e];
+                for (int q = 0; q < c; ++q)
+                    if (ok[q]) s -= R[q][c] * R[q][e];
+                R[c][e] = s / R[c][c];
+            }
         }
-        double nn = 0.0;
-        for (int i = threadIdx.x; i < m.M; i += kThreads) {
-            const double x = p[static_cast<int64_t>(i) * RP + r];
-            nn += x * x;
+        for (int c = 0; c < RP; ++c) {   // column c of R^-1 (zero for a dropped column)
+            if (!ok[c]) continue;
+            X[c][c] = 1.0 / R[c][c];
+            for (int r = c - 1; r >= 0; --r) {
+                if (!ok[r]) continue;
+                double s = 0.0;
+                for (int q = r + 1; q <= c; ++q)
+                    if (ok[q]) s += R[r][q] * X[q][c];
+                X[r][c] = -s / R[r][r];
+            }
         }
-        nn = block_sum(nn, red);
-        const float inv = nn > 0.0 ? static_cast<float>(1.0 / sqrt(nn)) : 0.f;
-        for (int i = threadIdx.x; i < m.M; i += kThreads) {
-            float* x = p + static_cast<int64_t>(i) * RP + r;
-            *x = nn > 0.0 ? __fmul_rn(*x, inv) : 0.f;
+        for (int c = 0; c < RP; ++c)
+            for (int d = 0; d < RP; ++d) rinv[c][d] = static_cast<float>(X[c][d]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < m.M; i += kThreads) {
+        float* row = p + static_cast<int64_t>(i) * RP;
+        float x[RP], y[RP];
+#pragma unroll
+        for (int c = 0; c < RP; ++c) x[c] = row[c];
+#pragma unroll
+        for (int c = 0; c < RP; ++c) {
+            float s = 0.f;
+#pragma unroll
+            for (int q = 0; q <= c; ++q) s = fmaf(x[q], rinv[q][c], s);
+            y[c] = s;
         }
-        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < RP; ++c) row[c] = y[c];
     }
 }
 
 // ---------------------------------------------------------------------------
 // partial Q_w = M_w^T P over one row split and one column block (tile: {mat,
-// column block, first unit, units}; unit = split * W + replica, one per warp)
+// column block, unit}; unit = split * W + replica): the 8 warps take every 8th
+// row of the split and their sums are added in warp order in shared memory
 // ---------------------------------------------------------------------------
 template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_qpart_kernel(const PsgdArgs a)
 {
+    __shared__ float red[kWarps][128 * RP];
     const int4 t = a.tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp >= t.w) return;
     const PsgdMat m = a.mats[t.x];
-    const int u = t.z + warp;
+    const int u = t.z;
     const int s = u / a.W, w = u % a.W;
     const int i0 = s * kRowsPerSplit, i1 = min(m.M, i0 + kRowsPerSplit);
     const float* src = (a.ef ? a.err + w * a.estride : a.mg + w * a.stride) + m.off;
     const float* p = a.P + m.p_off;
     float* out = a.QP + m.qp_off + static_cast<int64_t>(u) * m.N * RP;
+    const int c0 = t.y * m.cbw;
+    const int ncol = min(m.cbw, m.N - c0);
     const bool vec = m.vec && a.vec_ok;
     if (vec) {
-        const int c = t.y * m.cbw + 4 * lane;
-        if (c >= m.N) return;
+        const int c = 4 * lane;
         float acc[4][RP];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int r = 0; r < RP; ++r) acc[k][r] = 0.f;
+        if (c < ncol) {
 #pragma unroll 4
-        for (int i = i0; i < i1; ++i) {
-            const float4 x = ld4(src + static_cast<int64_t>(i) * m.N + c);
-            float pv[RP];
-            load_row<RP>(p + static_cast<int64_t>(i) * RP, pv);
+            for (int i = i0 + warp; i < i1; i += kWarps) {
+                const float4 x = __ldcs(reinterpret_cast<const float4*>(src + static_cast<int64_t>(i) * m.N + c0 + c));
+                float pv[RP];
+                load_row<RP>(p + static_cast<int64_t>(i) * RP, pv);
 #pragma unroll
-            for (int r = 0; r < RP; ++r) {
-                acc[0][r] = fmaf(x.x, pv[r], acc[0][r]);
-                acc[1][r] = fmaf(x.y, pv[r], acc[1][r]);
-                acc[2][r] = fmaf(x.z, pv[r], acc[2][r]);
-                acc[3][r] = fmaf(x.w, pv[r], acc[3][r]);
+                for (int r = 0; r < RP; ++r) {
+                    acc[0][r] = fmaf(x.x, pv[r], acc[0][r]);
+                    acc[1][r] = fmaf(x.y, pv[r], acc[1][r]);
+                    acc[2][r] = fmaf(x.z, pv[r], acc[2][r]);
+                    acc[3][r] = fmaf(x.w, pv[r], acc[3][r]);
+                }
             }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int r = 0; r < RP; ++r) out[static_cast<int64_t>(c + k) * RP + r] = acc[k][r];
+            for (int r = 0; r < RP; ++r) red[warp][(c + k) * RP + r] = acc[k][r];
     } else {
-        // the block's columns 32 at a time (the block is 128 wide when the plan
-        // allowed 16-byte rows but the buffers are not aligned)
-        const int c1 = min(m.N, (t.y + 1) * m.cbw);
-        for (int c = t.y * m.cbw + lane; c < c1; c += 32) {
+        for (int c = lane; c < m.cbw; c += 32) {
             float acc[RP];
 #pragma unroll
             for (int r = 0; r < RP; ++r) acc[r] = 0.f;
+            if (c < ncol) {
 #pragma unroll 4
-            for (int i = i0; i < i1; ++i) {
-                const float x = src[static_cast<int64_t>(i) * m.N + c];
-                float pv[RP];
-                load_row<RP>(p + static_cast<int64_t>(i) * RP, pv);
+                for (int i = i0 + warp; i < i1; i += kWarps) {
+                    const float x = src[static_cast<int64_t>(i) * m.N + c0 + c];
+                    float pv[RP];
+                    load_row<RP>(p + static_cast<int64_t>(i) * RP, pv);
 #pragma unroll
-                for (int r = 0; r < RP; ++r) acc[r] = fmaf(x, pv[r], acc[r]);
+                    for (int r = 0; r < RP; ++r) acc[r] = fmaf(x, pv[r], acc[r]);
+                }
             }
 #pragma unroll
-            for (int r = 0; r < RP; ++r) out[static_cast<int64_t>(c) * RP + r] = acc[r];
+            for (int r = 0; r < RP; ++r) red[warp][c * RP + r] = acc[r];
         }
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < ncol * RP; k += kThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < kWarps; ++q) v = __fadd_rn(v, red[q][k]);
+        out[static_cast<int64_t>(c0) * RP + k] = v;
     }
 }
 
@@ -328,6 +424,7 @@ __global__ void __launch_bounds__(kThreads) psgd_qfinal_kernel(const PsgdArgs a)
         float tot = 0.f;
         for (int w = 0; w < a.W; ++w) {
             float qw = 0.f;
+#pragma unroll 4
             for (int s = 0; s < m.S; ++s) qw = __fadd_rn(qw, a.QP[m.qp_off + (static_cast<int64_t>(s) * a.W + w) * plane + el]);
             tot = __fadd_rn(tot, qw);
         }
@@ -364,14 +461,23 @@ __global__ void __launch_bounds__(kThreads) psgd_out_kernel(const PsgdArgs a)
                 h[c] = s;
             }
             const float4 hv = make_float4(h[0], h[1], h[2], h[3]);
-            for (int w = 0; w < a.W; ++w) {
-                if (a.ef) {
-                    float* e = a.err + w * a.estride + base + j;
-                    const float4 x = ld4(e);
-                    st4(e, make_float4(__fsub_rn(x.x, h[0]), __fsub_rn(x.y, h[1]), __fsub_rn(x.z, h[2]),
-                                       __fsub_rn(x.w, h[3])));
+            for (int w0 = 0; w0 < a.W; w0 += kOutBatch) {
+                const int nb = min(kOutBatch, a.W - w0);
+                if (a.ef) {   // the batch's loads first, then its stores
+                    float4 x[kOutBatch];
+#pragma unroll
+                    for (int k = 0; k < kOutBatch; ++k)
+                        if (k < nb) x[k] = __ldcs(reinterpret_cast<const float4*>(a.err + (w0 + k) * a.estride + base + j));
+#pragma unroll
+                    for (int k = 0; k < kOutBatch; ++k)
+                        if (k < nb)
+                            __stcs(reinterpret_cast<float4*>(a.err + (w0 + k) * a.estride + base + j),
+                                   make_float4(__fsub_rn(x[k].x, h[0]), __fsub_rn(x[k].y, h[1]), __fsub_rn(x[k].z, h[2]),
+                                               __fsub_rn(x[k].w, h[3])));
                 }
-                st4(a.mg + w * a.stride + base + j, hv);
+#pragma unroll
+                for (int k = 0; k < kOutBatch; ++k)
+                    if (k < nb) __stcs(reinterpret_cast<float4*>(a.mg + (w0 + k) * a.stride + base + j), hv);
             }
         }
     } else {
@@ -473,7 +579,10 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
     h->bucket_numel = bucket_numel;
     h->nseg = nseg;
     h->seg_mat.assign(nseg, -1);
-    h->rows_p = std::max(1, 32 / W);
+    {   // P tiles: about two warp units per warp, at most kMaxPairs (row, replica) pairs
+        const int ngroups = (W + kGW - 1) / kGW;
+        h->rows_p = std::max(1, std::min(kMaxPairs / W, 16 / ngroups));
+    }
     const int RP = h->RP;
     for (int32_t t = 0; t < nseg; ++t) {
         const int64_t off = seg_offset[t], n = seg_numel[t], rows = seg_rows[t];
@@ -518,8 +627,7 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
             h->t_o.push_back(make_int4(mi, r0, std::min(kRowsOut, m.M - r0), 0));
         const int32_t ncb = (m.N + m.cbw - 1) / m.cbw, units = m.S * W;
         for (int32_t cb = 0; cb < ncb; ++cb)
-            for (int32_t u0 = 0; u0 < units; u0 += kWarps)
-                h->t_q.push_back(make_int4(mi, cb, u0, std::min(kWarps, units - u0)));
+            for (int32_t u = 0; u < units; ++u) h->t_q.push_back(make_int4(mi, cb, u, 0));
         const int64_t qe = static_cast<int64_t>(m.N) * RP;
         for (int64_t e0 = 0; e0 < qe; e0 += kFinalPerTile)
             h->t_f.push_back(make_int4(mi, static_cast<int32_t>(e0), static_cast<int32_t>(std::min<int64_t>(kFinalPerTile, qe - e0)), 0));

@@ -381,12 +381,14 @@ ddp_status ddp_used_allreduce(const uint8_t* local_used, int32_t ld, int32_t W, 
  *     tensor's shape[0] x the rest), rank R' = min(rank, M, N):
  *       M_w = G_w + E_w              (error feedback; E_w = 0 without it)
  *       P   = sum_w M_w Q            (Q: N x R', the warm-started state)
- *       P   = orthonormal columns of P (Gram-Schmidt; a zero column stays 0)
+ *       P   = P R^-1, R the Cholesky factor of P^T P (the orthonormal
+ *             basis with a positive-diagonal triangle; a column with no
+ *             positive pivot becomes 0)
  *       Q   = (sum_w M_w^T P) / W    (kept as the next iteration's Q)
  *       every replica's tensor = P Q^T;  E_w = M_w - P Q^T
  * The bucket's padding is left alone once compression starts.  Sums over
  * replicas are taken in replica order; P and Q products accumulate in fp32
- * with fused multiply-adds (the orthonormalisation's dot products in fp64), so
+ * with fused multiply-adds (P^T P in fp64), so
  * results match an exact evaluation to within rounding, not bit for bit.
  *
  * Memory (all the caller's; the library allocates none):
