@@ -10,19 +10,21 @@
 //
 // Kernels per compressed iteration (one launch each, over every tensor of the
 // bucket through tile tables built on the host):
-//   psgd_vec_kernel     1-D tensors: ring-ordered mean over their concatenation
-//   psgd_p_kernel       per (row, replica): M = G + E (stored back into E),
-//                       P_w[row] = M[row, :] Q; then the sum over replicas
-//   psgd_orth_kernel    per tensor: P <- P R^-1, R the Cholesky factor of P^T P
+//   psgd_p_kernel       per (row, group of replicas): M = G + E (stored back into
+//                       E), P_w[row] = M[row, :] Q; the sum over replicas; the
+//                       tile's share of P^T P in fp64.  Extra blocks take the
+//                       1-D tensors: ring-ordered mean over their concatenation
+//   psgd_orth_kernel    per tensor: P^T P from the tiles' shares, its Cholesky
+//                       factor R, and P <- P R^-1
 //   psgd_qpart_kernel   per (column block, row split, replica): partial M^T P,
-//                       the split's rows shared by the block's warps
-//   psgd_qfinal_kernel  Q = (sum over replicas of the sum over splits) / W
+//                       the split's rows shared by the block's warps; the last
+//                       block of a column block sums the partials in a fixed
+//                       order into Q = (sum_w M_w^T P) / W
 //   psgd_out_kernel     per row: G^ = P Q^T written to every replica, E = M - G^
 // Every kernel streams its matrix once: the contraction is rank R (1..8)
 // against a row or column of M, R fused multiply-adds per element and 4 to 12
 // bytes per element, far below the CUDA cores' arithmetic ridge, so the work is
-// HBM-bound and stays on the CUDA cores in fp32.  The orthonormalisation
-// forms P^T P in fp64 (M x R values, negligible time).
+// HBM-bound and stays on the CUDA cores in fp32.
 //
 // Rank is padded to RP in {1, 2, 4, 8}: Q and P carry RP columns, those past a
 // tensor's effective rank min(R, M, N) are zero and stay zero.
@@ -41,8 +43,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsOut = kWarps;       // rows per output tile: one per warp
 constexpr int kRowsPerSplit = 256;     // rows of one partial M^T P
-constexpr int kFinalPerTile = 256;     // Q elements per finalising tile
 constexpr int kMaxPairs = 256;         // (row, replica) pairs per P tile
+constexpr int kMaxRowsP = 16;          // rows per P tile
 constexpr int kGW = 4;                 // replicas a warp carries at once in the P pass
 constexpr int kOutBatch = 4;           // replicas whose error loads the output pass issues together
 constexpr int64_t kVecPiece = 16384;   // elements of a 1-D tensor per block
@@ -57,6 +59,10 @@ struct PsgdMat {
     int32_t vec;     // offset and N are multiples of 4 (16-byte rows when the buffers are aligned)
     int32_t S;       // row splits of M^T P
     int32_t cbw;     // column block width of M^T P (128 on the 16-byte path, 32 otherwise)
+    int32_t pt0;     // first P tile of the tensor (its shares of P^T P follow in tile order)
+    int32_t ntp;     // P tiles of the tensor
+    int32_t cnt0;    // first completion counter (one per column block)
+    int32_t pad;
 };
 
 struct PsgdVec {
@@ -73,13 +79,16 @@ struct PsgdArgs {
     float* P;
     float* Q;
     float* QP;
+    double* GR;       // per P tile: its share of P^T P (upper triangle, row-major)
+    int* CNT;         // per column block: blocks of the Q pass finished
     const PsgdMat* mats;
     const int4* tiles;
     const PsgdVec* vecs;
+    int32_t n_ptiles; // blocks of the P launch past this take the 1-D tensors
+    int32_t ncnt;
     int32_t W;
     int32_t ef;
     int32_t vec_ok;
-    int32_t rows_p;   // rows per P tile
     float inv_w;
     int64_t nvec;     // length of the concatenation of the 1-D tensors
 };
@@ -111,9 +120,8 @@ __device__ __forceinline__ float comp(const float4& v, int c) { return c == 0 ? 
 // 1-D tensors: the ring mean over the concatenation (chunk c summed from
 // replica c+1 round to replica c, each term scaled by fp32(1/W))
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) psgd_vec_kernel(const PsgdArgs a)
+__device__ void vec_piece(const PsgdArgs& a, const PsgdVec v)
 {
-    const PsgdVec v = a.vecs[blockIdx.x];
     const int64_t L = (a.nvec + a.W - 1) / a.W;
     for (int64_t i = threadIdx.x; i < v.len; i += kThreads) {
         const int64_t e = v.off + i;
@@ -121,7 +129,6 @@ __global__ void __launch_bounds__(kThreads) psgd_vec_kernel(const PsgdArgs a)
         float acc = 0.f;
         for (int k = 0; k < a.W; ++k) {
             int w = c + 1 + k;
-            w -= (w >= a.W) ? a.W : 0;
             w -= (w >= a.W) ? a.W : 0;
             const float t = __fmul_rn(a.mg[w * a.stride + e], a.inv_w);
             acc = k == 0 ? t : __fadd_rn(acc, t);
@@ -137,7 +144,15 @@ __global__ void __launch_bounds__(kThreads) psgd_vec_kernel(const PsgdArgs a)
 template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
 {
+    constexpr int NG = RP * (RP + 1) / 2;
     __shared__ float part[kMaxPairs][RP];
+    __shared__ float prow[kMaxRowsP][RP];
+    if (static_cast<int>(blockIdx.x) >= a.n_ptiles) {
+        vec_piece(a, a.vecs[blockIdx.x - a.n_ptiles]);
+        return;
+    }
+    if (blockIdx.x == 0)   // the Q pass's completion counters start each call at zero
+        for (int k = threadIdx.x; k < a.ncnt; k += kThreads) a.CNT[k] = 0;
     const int4 t = a.tiles[blockIdx.x];
     const PsgdMat m = a.mats[t.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -232,45 +247,61 @@ __global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
         float s = 0.f;
         for (int w = 0; w < a.W; ++w) s = __fadd_rn(s, part[rl * a.W + w][r]);
         a.P[m.p_off + static_cast<int64_t>(t.y + rl) * RP + r] = s;
+        prow[rl][r] = s;
+    }
+    __syncthreads();
+    // this tile's share of P^T P (fp32 products are exact in fp64)
+    if (threadIdx.x < NG) {
+        int c = 0, k = threadIdx.x;
+        while (k >= RP - c) {
+            k -= RP - c;
+            ++c;
+        }
+        const int d = c + k;
+        double s = 0.0;
+        for (int rl = 0; rl < t.z; ++rl) s += static_cast<double>(prow[rl][c]) * prow[rl][d];
+        a.GR[static_cast<int64_t>(blockIdx.x) * NG + threadIdx.x] = s;
     }
 }
 
 // ---------------------------------------------------------------------------
-// orthonormal columns of P (one block per tensor): the Gram matrix P^T P in
-// fp64 (one pass; products of fp32 values are exact in fp64), its Cholesky
-// factor R (upper triangular, positive diagonal) and R^-1 on one thread, then
-// P <- P R^-1 (a second pass) -- the orthonormal basis whose triangle has a
-// positive diagonal.  A column whose pivot is not positive (zero, or in the
-// span of the earlier columns) becomes 0.
+// orthonormal columns of P (one block per tensor): P^T P summed from the P
+// tiles' shares in a fixed order, its Cholesky factor R (upper triangular,
+// positive diagonal) and R^-1 on one thread, then P <- P R^-1 -- the
+// orthonormal basis whose triangle has a positive diagonal.  A column whose
+// pivot is not positive (zero, or in the span of the earlier columns) becomes 0.
 // ---------------------------------------------------------------------------
 template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
 {
     constexpr int NG = RP * (RP + 1) / 2;
     __shared__ double red[kWarps][NG];
+    __shared__ double gsum[NG];
     __shared__ float rinv[RP][RP];
     const PsgdMat m = a.mats[blockIdx.x];
     float* p = a.P + m.p_off;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    double g[NG];
+    {   // the tiles' shares: thread i adds tiles i, i + 256, ...; then a fixed tree over the block
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        double g[NG];
 #pragma unroll
-    for (int k = 0; k < NG; ++k) g[k] = 0.0;
-    for (int i = threadIdx.x; i < m.M; i += kThreads) {
-        const float* row = p + static_cast<int64_t>(i) * RP;
-        double x[RP];
+        for (int k = 0; k < NG; ++k) g[k] = 0.0;
+        for (int t = threadIdx.x; t < m.ntp; t += kThreads) {
+            const double* src = a.GR + static_cast<int64_t>(m.pt0 + t) * NG;
 #pragma unroll
-        for (int c = 0; c < RP; ++c) x[c] = row[c];
-        int k = 0;
+            for (int k = 0; k < NG; ++k) g[k] += src[k];
+        }
 #pragma unroll
-        for (int c = 0; c < RP; ++c)
+        for (int k = 0; k < NG; ++k) {
 #pragma unroll
-            for (int d = c; d < RP; ++d) g[k++] += x[c] * x[d];
-    }
-#pragma unroll
-    for (int k = 0; k < NG; ++k) {
-#pragma unroll
-        for (int o = 16; o; o >>= 1) g[k] += __shfl_xor_sync(0xffffffffu, g[k], o);
-        if (lane == 0) red[warp][k] = g[k];
+            for (int o = 16; o; o >>= 1) g[k] += __shfl_xor_sync(0xffffffffu, g[k], o);
+            if (lane == 0) red[warp][k] = g[k];
+        }
+        __syncthreads();
+        if (threadIdx.x < NG) {
+            double s = 0.0;
+            for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
+            gsum[threadIdx.x] = s;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -279,9 +310,7 @@ __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
         int k = 0;
         for (int c = 0; c < RP; ++c)
             for (int d = c; d < RP; ++d) {
-                double s = 0.0;
-                for (int w = 0; w < kWarps; ++w) s += red[w][k];
-                G[c][d] = G[d][c] = s;
+                G[c][d] = G[d][c] = gsum[k];
                 ++k;
             }
         for (int c = 0; c < RP; ++c)
@@ -337,12 +366,15 @@ __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
 // ---------------------------------------------------------------------------
 // partial Q_w = M_w^T P over one row split and one column block (tile: {mat,
 // column block, unit}; unit = split * W + replica): the 8 warps take every 8th
-// row of the split and their sums are added in warp order in shared memory
+// row of the split and their sums are added in warp order in shared memory.
+// The last block of a column block to finish (a completion counter) adds the
+// partials in the order (replica, split) and writes Q = sum / W.
 // ---------------------------------------------------------------------------
 template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_qpart_kernel(const PsgdArgs a)
 {
     __shared__ float red[kWarps][128 * RP];
+    __shared__ int last;
     const int4 t = a.tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const PsgdMat m = a.mats[t.x];
@@ -407,25 +439,29 @@ __global__ void __launch_bounds__(kThreads) psgd_qpart_kernel(const PsgdArgs a)
         for (int q = 0; q < kWarps; ++q) v = __fadd_rn(v, red[q][k]);
         out[static_cast<int64_t>(c0) * RP + k] = v;
     }
-}
-
-// ---------------------------------------------------------------------------
-// Q = (sum_w sum_s partial[s][w]) / W  (tile: {mat, first element, count})
-// ---------------------------------------------------------------------------
-template <int RP>
-__global__ void __launch_bounds__(kThreads) psgd_qfinal_kernel(const PsgdArgs a)
-{
-    const int4 t = a.tiles[blockIdx.x];
-    const PsgdMat m = a.mats[t.x];
+    // completion: the partial is published before the count (threadFenceReduction pattern)
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(a.CNT + m.cnt0 + t.y, 1) == m.S * a.W - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
     const int64_t plane = static_cast<int64_t>(m.N) * RP;
     const float wf = static_cast<float>(a.W);
-    for (int k = threadIdx.x; k < t.z; k += kThreads) {
-        const int64_t el = t.y + k;
+    for (int k = threadIdx.x; k < ncol * RP; k += kThreads) {
+        const int64_t el = static_cast<int64_t>(c0) * RP + k;
         float tot = 0.f;
-        for (int w = 0; w < a.W; ++w) {
+        for (int ww = 0; ww < a.W; ++ww) {
             float qw = 0.f;
-#pragma unroll 4
-            for (int s = 0; s < m.S; ++s) qw = __fadd_rn(qw, a.QP[m.qp_off + (static_cast<int64_t>(s) * a.W + w) * plane + el]);
+            for (int s0 = 0; s0 < m.S; s0 += 8) {   // eight loads in flight, added in split order
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    v[j] = s0 + j < m.S ? __ldcg(a.QP + m.qp_off + (static_cast<int64_t>(s0 + j) * a.W + ww) * plane + el) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (s0 + j < m.S) qw = __fadd_rn(qw, v[j]);
+            }
             tot = __fadd_rn(tot, qw);
         }
         a.Q[m.q_off + el] = __fdiv_rn(tot, wf);
@@ -514,10 +550,12 @@ struct ddp_powersgd {
     std::vector<PsgdMat> mats;
     std::vector<PsgdVec> vecs;
     int64_t nvec = 0;
-    std::vector<int4> t_p, t_q, t_f, t_o;
-    int32_t rows_p = 1;
+    std::vector<int4> t_p, t_q, t_o;
+    int32_t rows_p = 1, ncnt = 0;
     int64_t q_elems = 0, p_elems = 0, qp_elems = 0;
-    size_t off_mats = 0, off_tp = 0, off_tq = 0, off_tf = 0, off_to = 0, off_vecs = 0, off_P = 0, off_QP = 0;
+    // workspace: the tables, then the scratch (offsets from the scratch's start)
+    size_t off_mats = 0, off_tp = 0, off_tq = 0, off_to = 0, off_vecs = 0, off_scratch = 0;
+    size_t s_P = 0, s_QP = 0, s_GR = 0, s_CNT = 0, scratch_bytes = 0;
     size_t ws_bytes = 0;
     // bound buffers
     uint8_t* ws = nullptr;
@@ -528,28 +566,61 @@ struct ddp_powersgd {
 
 namespace {
 
+// The kernels' arguments over the bound buffers, with the scratch at `scratch`.
+PsgdArgs make_args(const ddp_powersgd& h, uint8_t* scratch, float* main_grad, int64_t replica_stride)
+{
+    PsgdArgs a{};
+    a.mg = main_grad;
+    a.stride = replica_stride;
+    a.err = h.err;
+    a.estride = h.estride;
+    a.P = reinterpret_cast<float*>(scratch + h.s_P);
+    a.QP = reinterpret_cast<float*>(scratch + h.s_QP);
+    a.GR = reinterpret_cast<double*>(scratch + h.s_GR);
+    a.CNT = reinterpret_cast<int*>(scratch + h.s_CNT);
+    a.Q = h.q;
+    a.mats = reinterpret_cast<const PsgdMat*>(h.ws + h.off_mats);
+    a.vecs = reinterpret_cast<const PsgdVec*>(h.ws + h.off_vecs);
+    a.n_ptiles = static_cast<int32_t>(h.t_p.size());
+    a.ncnt = h.ncnt;
+    a.W = h.W;
+    a.ef = h.ef && h.err;
+    auto al16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+    a.vec_ok = al16(main_grad) && replica_stride % 4 == 0 && (!a.ef || (al16(h.err) && h.estride % 4 == 0));
+    a.inv_w = 1.0f / static_cast<float>(h.W);
+    a.nvec = h.nvec;
+    return a;
+}
+
 template <int RP>
 ddp_status launch_all(const ddp_powersgd& h, const PsgdArgs& base, cudaStream_t s)
 {
     PsgdArgs a = base;
-    if (!h.vecs.empty()) {
-        a.vecs = reinterpret_cast<const PsgdVec*>(h.ws + h.off_vecs);
-        psgd_vec_kernel<<<static_cast<unsigned>(h.vecs.size()), kThreads, 0, s>>>(a);
+    const unsigned nblocks_p = static_cast<unsigned>(h.t_p.size() + h.vecs.size());
+    if (nblocks_p > 0) {
+        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tp);
+        psgd_p_kernel<RP><<<nblocks_p, kThreads, 0, s>>>(a);
     }
     if (!h.mats.empty()) {
-        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tp);
-        psgd_p_kernel<RP><<<static_cast<unsigned>(h.t_p.size()), kThreads, 0, s>>>(a);
         psgd_orth_kernel<RP><<<static_cast<unsigned>(h.mats.size()), kThreads, 0, s>>>(a);
         a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tq);
         psgd_qpart_kernel<RP><<<static_cast<unsigned>(h.t_q.size()), kThreads, 0, s>>>(a);
-        a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tf);
-        psgd_qfinal_kernel<RP><<<static_cast<unsigned>(h.t_f.size()), kThreads, 0, s>>>(a);
         a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_to);
         psgd_out_kernel<RP><<<static_cast<unsigned>(h.t_o.size()), kThreads, 0, s>>>(a);
     }
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_powersgd_reduce: kernel launch failed: %s", cudaGetErrorString(err));
     return DDP_OK;
+}
+
+ddp_status launch_rank(const ddp_powersgd& h, const PsgdArgs& a, cudaStream_t s)
+{
+    switch (h.RP) {
+    case 1: return launch_all<1>(h, a, s);
+    case 2: return launch_all<2>(h, a, s);
+    case 4: return launch_all<4>(h, a, s);
+    default: return launch_all<8>(h, a, s);
+    }
 }
 
 }  // namespace
@@ -581,7 +652,7 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
     h->seg_mat.assign(nseg, -1);
     {   // P tiles: about two warp units per warp, at most kMaxPairs (row, replica) pairs
         const int ngroups = (W + kGW - 1) / kGW;
-        h->rows_p = std::max(1, std::min(kMaxPairs / W, 16 / ngroups));
+        h->rows_p = std::max(1, std::min({kMaxPairs / W, 16 / ngroups, kMaxRowsP}));
     }
     const int RP = h->RP;
     for (int32_t t = 0; t < nseg; ++t) {
@@ -619,19 +690,21 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
         m.qp_off = h->qp_elems;
         h->qp_elems += align4(static_cast<int64_t>(m.S) * W * cols * RP);
         const int32_t mi = static_cast<int32_t>(h->mats.size());
-        h->seg_mat[t] = mi;
-        h->mats.push_back(m);
+        m.pt0 = static_cast<int32_t>(h->t_p.size());
         for (int32_t r0 = 0; r0 < m.M; r0 += h->rows_p)
             h->t_p.push_back(make_int4(mi, r0, std::min(h->rows_p, m.M - r0), 0));
+        m.ntp = static_cast<int32_t>(h->t_p.size()) - m.pt0;
         for (int32_t r0 = 0; r0 < m.M; r0 += kRowsOut)
             h->t_o.push_back(make_int4(mi, r0, std::min(kRowsOut, m.M - r0), 0));
         const int32_t ncb = (m.N + m.cbw - 1) / m.cbw, units = m.S * W;
+        m.cnt0 = h->ncnt;
+        h->ncnt += ncb;
         for (int32_t cb = 0; cb < ncb; ++cb)
             for (int32_t u = 0; u < units; ++u) h->t_q.push_back(make_int4(mi, cb, u, 0));
-        const int64_t qe = static_cast<int64_t>(m.N) * RP;
-        for (int64_t e0 = 0; e0 < qe; e0 += kFinalPerTile)
-            h->t_f.push_back(make_int4(mi, static_cast<int32_t>(e0), static_cast<int32_t>(std::min<int64_t>(kFinalPerTile, qe - e0)), 0));
+        h->seg_mat[t] = mi;
+        h->mats.push_back(m);
     }
+    const size_t ng = static_cast<size_t>(RP * (RP + 1) / 2);
     size_t o = 0;
     h->off_mats = o;
     o = align256(o + h->mats.size() * sizeof(PsgdMat));
@@ -639,17 +712,22 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
     o = align256(o + h->t_p.size() * sizeof(int4));
     h->off_tq = o;
     o = align256(o + h->t_q.size() * sizeof(int4));
-    h->off_tf = o;
-    o = align256(o + h->t_f.size() * sizeof(int4));
     h->off_to = o;
     o = align256(o + h->t_o.size() * sizeof(int4));
     h->off_vecs = o;
     o = align256(o + h->vecs.size() * sizeof(PsgdVec));
-    h->off_P = o;
-    o = align256(o + static_cast<size_t>(h->p_elems) * sizeof(float));
-    h->off_QP = o;
-    o = align256(o + static_cast<size_t>(h->qp_elems) * sizeof(float));
-    h->ws_bytes = std::max<size_t>(o, 256);
+    h->off_scratch = o;
+    size_t sc = 0;
+    h->s_P = sc;
+    sc = align256(sc + static_cast<size_t>(h->p_elems) * sizeof(float));
+    h->s_QP = sc;
+    sc = align256(sc + static_cast<size_t>(h->qp_elems) * sizeof(float));
+    h->s_GR = sc;
+    sc = align256(sc + h->t_p.size() * ng * sizeof(double));
+    h->s_CNT = sc;
+    sc = align256(sc + static_cast<size_t>(h->ncnt) * sizeof(int));
+    h->scratch_bytes = sc;
+    h->ws_bytes = std::max<size_t>(o + sc, 256);
     *out = h;
     return ddp::ok();
 }
@@ -704,7 +782,6 @@ extern "C" ddp_status ddp_powersgd_bind(ddp_powersgd* h, void* workspace, int64_
     cudaError_t e = put(h->off_mats, h->mats.data(), h->mats.size() * sizeof(PsgdMat));
     if (e == cudaSuccess) e = put(h->off_tp, h->t_p.data(), h->t_p.size() * sizeof(int4));
     if (e == cudaSuccess) e = put(h->off_tq, h->t_q.data(), h->t_q.size() * sizeof(int4));
-    if (e == cudaSuccess) e = put(h->off_tf, h->t_f.data(), h->t_f.size() * sizeof(int4));
     if (e == cudaSuccess) e = put(h->off_to, h->t_o.data(), h->t_o.size() * sizeof(int4));
     if (e == cudaSuccess) e = put(h->off_vecs, h->vecs.data(), h->vecs.size() * sizeof(PsgdVec));
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -753,30 +830,8 @@ extern "C" ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int
         return st;
     }
     if (!h->ws) return fail(DDP_E_STATE, "%s: call ddp_powersgd_bind first", fn);
-    PsgdArgs a{};
-    a.mg = main_grad;
-    a.stride = replica_stride;
-    a.err = h->err;
-    a.estride = h->estride;
-    a.P = reinterpret_cast<float*>(h->ws + h->off_P);
-    a.Q = h->q;
-    a.QP = reinterpret_cast<float*>(h->ws + h->off_QP);
-    a.mats = reinterpret_cast<const PsgdMat*>(h->ws + h->off_mats);
-    a.W = h->W;
-    a.ef = h->ef && h->err;
-    auto al16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
-    a.vec_ok = al16(main_grad) && replica_stride % 4 == 0 && (!a.ef || (al16(h->err) && h->estride % 4 == 0));
-    a.rows_p = h->rows_p;
-    a.inv_w = 1.0f / static_cast<float>(h->W);
-    a.nvec = h->nvec;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    ddp_status st;
-    switch (h->RP) {
-    case 1: st = launch_all<1>(*h, a, s); break;
-    case 2: st = launch_all<2>(*h, a, s); break;
-    case 4: st = launch_all<4>(*h, a, s); break;
-    default: st = launch_all<8>(*h, a, s); break;
-    }
+    const ddp_status st = launch_rank(*h, make_args(*h, h->ws + h->off_scratch, main_grad, replica_stride),
+                                      static_cast<cudaStream_t>(stream));
     if (st != DDP_OK) return st;
     ++h->iter;
     return ddp::ok();
@@ -796,23 +851,23 @@ int64_t ddp::powersgd_numel(const ddp_powersgd* h) { return h->bucket_numel; }
 
 // ---------------------------------------------------------------------------
 // ddp_powersgd_reduce_static: the same kernels with their scratch (the summed
-// P and the partial sums of Q) in a fixed device array of this library instead
-// of the caller's workspace.  Nothing of that scratch is read before the same
-// call has written it, so nothing needs clearing.
+// P, the partial sums of Q, the shares of P^T P and the completion counters)
+// in a fixed device array of this library instead of the caller's workspace.
+// Within one call every part of that scratch is written before it is read
+// (the counters are zeroed by the first kernel), so nothing needs clearing.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr int64_t kStaticScratchBytes = DDP_POWERSGD_STATIC_SCRATCH_BYTES;
-constexpr int64_t kStaticScratchFloats = kStaticScratchBytes / static_cast<int64_t>(sizeof(float));
 constexpr int kMaxDevices = 64;
 
-__device__ __align__(256) float g_psgd_static_scratch[kStaticScratchFloats];
+__device__ __align__(256) uint8_t g_psgd_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mu;
-float* g_static_ptr[kMaxDevices] = {};
+uint8_t* g_static_ptr[kMaxDevices] = {};
 
 // The array's address on the current device, looked up once per device.
-ddp_status static_scratch(float** out)
+ddp_status static_scratch(uint8_t** out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -825,7 +880,7 @@ ddp_status static_scratch(float** out)
         e = cudaGetSymbolAddress(&p, g_psgd_static_scratch);
         if (e != cudaSuccess)
             return ddp::fail(DDP_E_CUDA, "ddp_powersgd_reduce_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        g_static_ptr[dev] = static_cast<float*>(p);
+        g_static_ptr[dev] = static_cast<uint8_t*>(p);
     }
     *out = g_static_ptr[dev];
     return DDP_OK;
@@ -843,11 +898,9 @@ extern "C" ddp_status ddp_powersgd_reduce_static(ddp_powersgd* h, float* main_gr
     if (h->W > 1 && replica_stride < h->bucket_numel)
         return fail(DDP_E_INVAL, "%s: replica_stride %lld < bucket numel %lld", fn, static_cast<long long>(replica_stride),
                     static_cast<long long>(h->bucket_numel));
-    const int64_t p_floats = (h->p_elems + 63) & ~static_cast<int64_t>(63);   // QP starts 256-byte aligned
-    const int64_t need = p_floats + h->qp_elems;
-    if (need > kStaticScratchFloats)
+    if (static_cast<int64_t>(h->scratch_bytes) > kStaticScratchBytes)
         return fail(DDP_E_CAPACITY, "%s: this bucket needs %lld bytes of scratch, the static array holds %lld "
-                    "(use ddp_powersgd_reduce with a workspace)", fn, static_cast<long long>(need * 4),
+                    "(use ddp_powersgd_reduce with a workspace)", fn, static_cast<long long>(h->scratch_bytes),
                     static_cast<long long>(kStaticScratchBytes));
     if (h->iter < h->start_iter) {
         const ddp_status st = ddp::launch_allreduce(main_grad, replica_stride, h->bucket_numel, h->W, DDP_ALLREDUCE, stream);
@@ -855,33 +908,10 @@ extern "C" ddp_status ddp_powersgd_reduce_static(ddp_powersgd* h, float* main_gr
         return st;
     }
     if (!h->ws) return fail(DDP_E_STATE, "%s: call ddp_powersgd_bind first", fn);
-    float* scratch = nullptr;
+    uint8_t* scratch = nullptr;
     const ddp_status sst = static_scratch(&scratch);
     if (sst != DDP_OK) return sst;
-    PsgdArgs a{};
-    a.mg = main_grad;
-    a.stride = replica_stride;
-    a.err = h->err;
-    a.estride = h->estride;
-    a.P = scratch;
-    a.Q = h->q;
-    a.QP = scratch + p_floats;
-    a.mats = reinterpret_cast<const PsgdMat*>(h->ws + h->off_mats);
-    a.W = h->W;
-    a.ef = h->ef && h->err;
-    auto al16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
-    a.vec_ok = al16(main_grad) && replica_stride % 4 == 0 && (!a.ef || (al16(h->err) && h->estride % 4 == 0));
-    a.rows_p = h->rows_p;
-    a.inv_w = 1.0f / static_cast<float>(h->W);
-    a.nvec = h->nvec;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    ddp_status st;
-    switch (h->RP) {
-    case 1: st = launch_all<1>(*h, a, s); break;
-    case 2: st = launch_all<2>(*h, a, s); break;
-    case 4: st = launch_all<4>(*h, a, s); break;
-    default: st = launch_all<8>(*h, a, s); break;
-    }
+    const ddp_status st = launch_rank(*h, make_args(*h, scratch, main_grad, replica_stride), static_cast<cudaStream_t>(stream));
     if (st != DDP_OK) return st;
     ++h->iter;
     return ddp::ok();
