@@ -393,8 +393,9 @@ ddp_status ddp_used_allreduce(const uint8_t* local_used, int32_t ld, int32_t W, 
  *
  * Memory (all the caller's; the library allocates none):
  *   workspace  DEVICE, ddp_powersgd_sizes bytes, 256-byte aligned: tile
- *              tables (written by ddp_powersgd_bind) and the scratch P and
- *              partial sums of Q (overwritten by every reduce).
+ *              tables (written by ddp_powersgd_bind) and the scratch: P, the
+ *              partial sums of Q, the shares of P^T P and completion counters
+ *              (all rewritten by every reduce).
  *   q_state    DEVICE fp32, q_elems: every matrix's Q as N rows of rank_pad
  *              floats (ddp_powersgd_matrix gives the offset); columns past
  *              the effective rank must be 0.  ddp_powersgd_set_q writes one
@@ -460,8 +461,9 @@ ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replic
 
 /*
  * ddp_powersgd_reduce_static -- ddp_powersgd_reduce, allocating nothing and
- * using no caller scratch: the kernels' scratch (the summed P and the partial
- * sums of Q) lives in a fixed device array of DDP_POWERSGD_STATIC_SCRATCH_BYTES
+ * using no caller scratch: the kernels' scratch (the summed P, the partial
+ * sums of Q, the blocks' shares of P^T P and the Q pass's completion
+ * counters) lives in a fixed device array of DDP_POWERSGD_STATIC_SCRATCH_BYTES
  * (8 MiB) inside the library.  The pages have no counterpart: this is an
  * entry point of this library for callers that want no scratch allocation at
  * all.  The workspace bound by ddp_powersgd_bind still supplies the tile
@@ -470,7 +472,8 @@ ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replic
  * Set-up: the first call on each device, with that device current, looks up
  * the array's address (cudaGetSymbolAddress) and keeps it; make that first
  * call before any stream capture.  Nothing of the scratch is read before the
- * same call writes it, so nothing needs clearing.  Calls that overlap in time
+ * same call writes it (the first kernel zeroes the counters), so nothing needs
+ * clearing beforehand.  Calls that overlap in time
  * (any state objects, any streams, on one device) share the array and race:
  * serialise them.  Results are identical to ddp_powersgd_reduce's.
  * Errors: as ddp_powersgd_reduce; DDP_E_CAPACITY when the bucket's scratch
