@@ -24,7 +24,7 @@ DDP_F32, DDP_BF16, DDP_F16 = 0, 1, 2
 DDP_ORDER_REVERSE, DDP_ORDER_FWD_THEN_REVERSE, DDP_ORDER_MEGATRON = 0, 1, 2
 DDP_ALLREDUCE, DDP_REDUCE_SCATTER = 0, 1
 DDP_R_FUSED, DDP_R_COPY_BACK, DDP_R_TIMING, DDP_R_DRY_RUN, DDP_R_COALESCE = 1, 2, 4, 8, 16
-DDP_R_WIRE_BF16, DDP_R_WIRE_F16 = 32, 64
+DDP_R_WIRE_BF16, DDP_R_WIRE_F16, DDP_R_BUCKET_DONE = 32, 64, 128
 DDP_KERNEL_AUTO, DDP_KERNEL_PLAIN = 0, 1
 
 
@@ -92,6 +92,7 @@ _SIGS = {
     "ddp_reducer_mark_ready_many": (C.c_int32, [_vp, _i32p, C.c_int32, _vp]),
     "ddp_reducer_finalize": (C.c_int32, [_vp, _vp, C.c_int64]),
     "ddp_reducer_issue_log": (C.c_int32, [_vp, _i32p, C.c_int32, _i32p]),
+    "ddp_reducer_wait_bucket": (C.c_int32, [_vp, C.c_int32, _vp]),
     "ddp_reducer_bucket_ms": (C.c_int32, [_vp, C.POINTER(C.c_float), C.c_int32]),
     "ddp_reducer_destroy": (None, [_vp]),
     "ddp_set_kernel_variant": (C.c_int32, [C.c_int32]),
@@ -410,6 +411,10 @@ def ddp_reducer_mark_ready_many(r, params, producer_stream=None) -> None:
 
 def ddp_reducer_finalize(r, consumer_stream=None, timeout_us=0) -> None:
     _check(lib().ddp_reducer_finalize(r, _stream(consumer_stream), int(timeout_us)))
+
+
+def ddp_reducer_wait_bucket(r, bucket, consumer_stream=None) -> None:
+    _check(lib().ddp_reducer_wait_bucket(r, int(bucket), _stream(consumer_stream)))
 
 
 def ddp_reducer_issue_log(r, cap=4096) -> list:

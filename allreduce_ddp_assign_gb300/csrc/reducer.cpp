@@ -93,6 +93,7 @@ struct ddp_reducer {
     bool fu_copy_pending = false;
 
     std::vector<ddp_powersgd*> hooks;  // per bucket: the PowerSGD hook, or null
+    std::vector<cudaEvent_t> bdone;    // per bucket: recorded after its reduction (DDP_R_BUCKET_DONE)
 
     bool dry() const { return flags & DDP_R_DRY_RUN; }
     uint8_t* host_bitmap() { return dry() ? fu_host_dry.data() : fu_host; }
@@ -144,9 +145,19 @@ struct ddp_reducer {
         return s;
     }
 
-    // Issue the buckets order[pos .. pos+count-1] (all ready) on the side stream:
-    // wait for their producers, then one launch per bucket, or one coalesced launch.
+    // Issue the buckets order[pos .. pos+count-1] (all ready) on the side stream,
+    // then (DDP_R_BUCKET_DONE) record each bucket's completion event after them.
     ddp_status issue(int32_t pos, int32_t count)
+    {
+        ddp_status st = issue_launches(pos, count);
+        if (st != DDP_OK || dry() || !(flags & DDP_R_BUCKET_DONE)) return st;
+        for (int32_t i = 0; i < count; ++i)
+            if (!cuda_ok(cudaEventRecord(bdone[order[pos + i]], side), "cudaEventRecord", &st)) return st;
+        return DDP_OK;
+    }
+
+    // Wait for the buckets' producers, then one launch per bucket, or one coalesced launch.
+    ddp_status issue_launches(int32_t pos, int32_t count)
     {
         for (int32_t i = 0; i < count; ++i) log.push_back(order[pos + i]);
         if (dry()) return DDP_OK;
@@ -291,6 +302,7 @@ struct ddp_reducer {
         for (cudaEvent_t e : t_end) cudaEventDestroy(e);
         if (done) cudaEventDestroy(done);
         if (fu_copied) cudaEventDestroy(fu_copied);
+        for (cudaEvent_t e : bdone) cudaEventDestroy(e);
         if (fu_host) cudaFreeHost(fu_host);
     }
 };
@@ -313,7 +325,7 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
     if (W < 1 || W > ddp::kMaxReplicas) return fail(DDP_E_INVAL, "%s: W = %d outside [1, %d]", fn, W, ddp::kMaxReplicas);
     if (mode != DDP_ALLREDUCE && mode != DDP_REDUCE_SCATTER) return fail(DDP_E_INVAL, "%s: unknown mode %d", fn, mode);
     if (flags & ~(DDP_R_FUSED | DDP_R_COPY_BACK | DDP_R_TIMING | DDP_R_DRY_RUN | DDP_R_COALESCE | DDP_R_WIRE_BF16 |
-                  DDP_R_WIRE_F16))
+                  DDP_R_WIRE_F16 | DDP_R_BUCKET_DONE))
         return fail(DDP_E_INVAL, "%s: unknown flag bits 0x%x", fn, flags);
     if ((flags & DDP_R_WIRE_BF16) && (flags & DDP_R_WIRE_F16))
         return fail(DDP_E_INVAL, "%s: DDP_R_WIRE_BF16 and DDP_R_WIRE_F16 exclude each other", fn);
@@ -394,6 +406,11 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
             cudaEvent_t e = nullptr;
             if (!mk(&e, cudaEventDisableTiming)) return reject(st);
             r->ready[b].push_back(e);
+        }
+        if (flags & DDP_R_BUCKET_DONE) {
+            r->bdone.assign(nbuckets, nullptr);
+            for (int32_t b = 0; b < nbuckets; ++b)
+                if (!mk(&r->bdone[b], cudaEventDisableTiming)) return reject(st);
         }
         if (flags & DDP_R_TIMING) {
             r->t_begin.assign(nbuckets, nullptr);
@@ -633,6 +650,23 @@ extern "C" ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream
             std::this_thread::sleep_for(std::chrono::microseconds(20));
         }
     }
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_reducer_wait_bucket(ddp_reducer* r, int32_t bucket, void* consumer_stream)
+{
+    using ddp::fail;
+    const char* fn = "ddp_reducer_wait_bucket";
+    if (!r) return fail(DDP_E_INVAL, "%s: reducer is NULL", fn);
+    if (bucket < 0 || bucket >= r->nbuckets) return fail(DDP_E_INVAL, "%s: bucket %d outside [0, %d)", fn, bucket, r->nbuckets);
+    if (!(r->flags & DDP_R_BUCKET_DONE)) return fail(DDP_E_STATE, "%s: reducer built without DDP_R_BUCKET_DONE", fn);
+    if (r->phase == Phase::Idle || std::find(r->log.begin(), r->log.end(), bucket) == r->log.end())
+        return fail(DDP_E_STATE, "%s: bucket %d has not been issued in this iteration", fn, bucket);
+    if (r->dry()) return ddp::ok();
+    ddp_status st = DDP_OK;
+    if (!cuda_ok(cudaStreamWaitEvent(static_cast<cudaStream_t>(consumer_stream), r->bdone[bucket], 0),
+                 "cudaStreamWaitEvent", &st))
+        return st;
     return ddp::ok();
 }
 

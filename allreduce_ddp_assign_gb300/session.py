@@ -10,7 +10,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, DDP_R_WIRE_BF16,
-               DDP_R_WIRE_F16, Plan, ddp_pack, ddp_pack_group,
+               DDP_R_WIRE_F16, DDP_R_BUCKET_DONE, Plan, ddp_pack, ddp_pack_group, ddp_reducer_wait_bucket,
                ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
                ddp_reducer_find_unused, ddp_reducer_mark_ready_many, ddp_reducer_prepare,
@@ -29,7 +29,7 @@ class BucketReducer:
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads, used=None,
                  grads_out=None, fused=True, timing=False, side_stream=None, main_grad=True, grad_reduce_in_fp32=1,
-                 coalesce=False, wire=None, powersgd=None):
+                 coalesce=False, wire=None, powersgd=None, bucket_done=False):
         """powersgd: dict(rank, shapes, q0, error_feedback=True, start_iter=0) registers the
         PowerSGD hook on every bucket; shapes[p] is parameter p's shape and q0(p, n, r)
         its initial Q (n x r), the hook's random draw."""
@@ -48,7 +48,8 @@ class BucketReducer:
         self.out_tab = None if grads_out is None else self.plan.pointer_table(grads_out)
         flags = (DDP_R_FUSED if fused else 0) | (DDP_R_COPY_BACK if grads_out is not None else 0) | \
                 (DDP_R_TIMING if timing else 0) | (DDP_R_COALESCE if coalesce and fused else 0) | \
-                {None: 0, DDP_BF16: DDP_R_WIRE_BF16, DDP_F16: DDP_R_WIRE_F16}[wire]
+                {None: 0, DDP_BF16: DDP_R_WIRE_BF16, DDP_F16: DDP_R_WIRE_F16}[wire] | \
+                (DDP_R_BUCKET_DONE if bucket_done else 0)
         self.handle = ddp_reducer_create(P, self.plan.bucket_of, self.plan.bucket_order, self.plan.descs,
                                          self.plan.bucket_start, self.W, self.mode, flags, self.grads_tab,
                                          None, P, self.main_grad, self.plan.replica_stride, self.out_tab,
@@ -147,11 +148,19 @@ class BucketReducer:
 class HostBucketReducer:
     """Host-buffer front end of BucketReducer.  Each step copies every replica's
     gradients from pinned host memory to the device, runs the synchronised
-    backward's bucket reduction, and copies the reduced main_grad back.
+    backward's bucket reduction, and copies the reduced buckets back.
+
+    The three run as a pipeline over the buckets in issue order: bucket b's
+    host-to-device copies go out on one copy stream and mark its parameters
+    ready (the reducer gates the bucket's reduction on them), and bucket b's
+    device-to-host copy waits for that bucket alone (ddp_reducer_wait_bucket)
+    on a second copy stream, so the two directions and the reductions overlap.
 
     host_in   pinned [W, total] tensor (gradient dtype): replica w's gradients of
               all parameters back to back in parameter order.
-    host_out  pinned [W * replica_stride] fp32 tensor.
+    host_out  pinned [W * replica_stride] fp32 tensor; every bucket's elements
+              (main_grad layout) are written, the alignment gaps between
+              buckets are not.
     """
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, torch_dtype,
@@ -159,11 +168,32 @@ class HostBucketReducer:
         import torch
 
         numels = [int(v) for v in numels]
-        offs = np.concatenate([[0], np.cumsum(numels)]).astype(np.int64)
-        self.dev_in = torch.empty((W, int(offs[-1])), dtype=torch_dtype, device="cuda")
-        grads = [[self.dev_in[w, offs[p]:offs[p + 1]] for p in range(len(numels))] for w in range(W)]
+        self.W = int(W)
+        self.offs = np.concatenate([[0], np.cumsum(numels)]).astype(np.int64)
+        self.dev_in = torch.empty((W, int(self.offs[-1])), dtype=torch_dtype, device="cuda")
+        grads = [[self.dev_in[w, self.offs[p]:self.offs[p + 1]] for p in range(len(numels))] for w in range(W)]
         self.reducer = BucketReducer(numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads,
-                                     used=used, fused=fused, timing=timing, coalesce=coalesce)
+                                     used=used, fused=fused, timing=timing, coalesce=coalesce, bucket_done=True)
+        plan = self.reducer.plan
+        # per bucket in issue order: its parameters as contiguous runs of the host layout
+        self.issue = []
+        for b in plan.bucket_order:
+            b = int(b)
+            mem = sorted(int(p) for p in plan.members[b])
+            runs, lo = [], mem[0] if mem else 0
+            for k in range(1, len(mem) + 1):
+                if k == len(mem) or mem[k] != mem[k - 1] + 1:
+                    runs.append((int(self.offs[lo]), int(self.offs[mem[k - 1] + 1])))
+                    if k < len(mem):
+                        lo = mem[k]
+            ready = [p for p in self.reducer.ready_order if plan.bucket_of[p] == b]
+            self.issue.append((b, runs, np.asarray(ready, np.int32)))
+        self.h2d = torch.cuda.Stream()
+        self.d2h = torch.cuda.Stream()
+        self.reduced = None      # event: the previous step's reductions are done (dev_in may be overwritten)
+        self.downloaded = None   # event: the previous step's copies to the host are done (main_grad may be)
+        self.h2d_bytes = int(self.offs[-1]) * W * self.dev_in.element_size()
+        self.d2h_bytes = sum(int(plan.bucket_numel[b]) for b in range(plan.nbuckets)) * W * 4
 
     @property
     def replica_stride(self) -> int:
@@ -172,11 +202,41 @@ class HostBucketReducer:
     def step(self, host_in, host_out, stream=None):
         import torch
 
+        r = self.reducer
+        plan = r.plan
         stream = torch.cuda.current_stream() if stream is None else stream
-        with torch.cuda.stream(stream):
-            self.dev_in.copy_(host_in, non_blocking=True)
-            self.reducer.step(stream, stream)
-            host_out.copy_(self.reducer.main_grad, non_blocking=True)
+        # dev_in is overwritten once the previous step's reductions have read it; its
+        # device-to-host copies may still be running (they read main_grad only after
+        # this step's reduction of the same bucket, on the same copy stream)
+        if self.reduced is not None:
+            self.h2d.wait_event(self.reduced)
+            r.side.wait_event(self.downloaded)
+        else:
+            self.h2d.wait_stream(stream)
+            r.side.wait_stream(stream)
+        self.d2h.wait_stream(stream)
+        ddp_reducer_prepare(r.handle, 0)
+        with torch.cuda.stream(self.h2d):
+            for b, runs, ready in self.issue:
+                for w in range(self.W):
+                    for lo, hi in runs:
+                        self.dev_in[w, lo:hi].copy_(host_in[w, lo:hi], non_blocking=True)
+                if len(ready):
+                    ddp_reducer_mark_ready_many(r.handle, ready, self.h2d)
+        stride = plan.replica_stride
+        with torch.cuda.stream(self.d2h):
+            for b, _, _ in self.issue:
+                ddp_reducer_wait_bucket(r.handle, b, self.d2h)
+                lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
+                for w in range(self.W):
+                    host_out[w * stride + lo:w * stride + lo + n].copy_(r.main_grad[w * stride + lo:w * stride + lo + n],
+                                                                       non_blocking=True)
+        self.downloaded = torch.cuda.Event()
+        self.downloaded.record(self.d2h)
+        ddp_reducer_finalize(r.handle, stream, 0)
+        self.reduced = torch.cuda.Event()
+        self.reduced.record(stream)
+        stream.wait_stream(self.d2h)
 
     def close(self):
         self.reducer.close()

@@ -572,7 +572,8 @@ enum {
     DDP_R_COALESCE = 16, /* buckets that become issuable together go out in one launch
                             (ddp_fused_bucket_group); needs DDP_R_FUSED */
     DDP_R_WIRE_BF16 = 32, /* reduce through the bf16 compression hook (ddp_bucket_allreduce_wire) */
-    DDP_R_WIRE_F16 = 64   /* reduce through the fp16 compression hook */
+    DDP_R_WIRE_F16 = 64,  /* reduce through the fp16 compression hook */
+    DDP_R_BUCKET_DONE = 128 /* record an event after each bucket's reduction (ddp_reducer_wait_bucket) */
 };
 
 /*
@@ -701,6 +702,16 @@ ddp_status ddp_reducer_mark_ready_many(ddp_reducer* r, const int32_t* params, in
  * queued; call again or synchronise); DDP_E_CUDA.
  */
 ddp_status ddp_reducer_finalize(ddp_reducer* r, void* consumer_stream, int64_t timeout_us);
+
+/*
+ * ddp_reducer_wait_bucket -- make consumer_stream wait for bucket `bucket`'s
+ * reduction in this iteration (Megatron page 3: finish_grad_sync per bucket;
+ * a consumer such as an optimizer or a copy to the host can start on the
+ * early buckets while later ones are still reducing).  Needs DDP_R_BUCKET_DONE.
+ * Errors: DDP_E_INVAL (bucket out of range); DDP_E_STATE (flag not set, or
+ * the bucket was not issued in this iteration); DDP_E_CUDA.
+ */
+ddp_status ddp_reducer_wait_bucket(ddp_reducer* r, int32_t bucket, void* consumer_stream);
 
 /* Buckets issued in this iteration, in issue order (HOST out[cap]); *n = count. */
 ddp_status ddp_reducer_issue_log(const ddp_reducer* r, int32_t* out, int32_t cap, int32_t* n);

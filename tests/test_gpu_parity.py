@@ -753,3 +753,31 @@ def test_overlap_hides_reduction():
     assert line["overlapped_step_ms"] < line["serial_step_ms"]
     assert line["overlapped_step_ms"] >= line["backward_ms"] * 0.98
     assert abs(line["model"]["step_ms"] - line["overlapped_step_ms"]) < 0.25 * line["overlapped_step_ms"]
+
+
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_host_front_end_pipeline_vs_oracle(orc, name):
+    """HostBucketReducer: pinned host gradients in, reduced buckets out, with the
+    copies in both directions pipelined against the reductions bucket by bucket.
+    Two steps in a row with different inputs, every bucket bit for bit."""
+    from allreduce_ddp_assign_gb300.session import HostBucketReducer
+
+    wl = WL.ALL[name]()
+    host = HostBucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                             wl.first_cap_bytes, wl.pad_multiple, torch.float32)
+    plan = host.reducer.plan
+    total = int(host.offs[-1])
+    h_out = torch.full((wl.W * host.replica_stride,), -1.0, dtype=torch.float32, pin_memory=True)
+    for m in range(2):
+        h_in = torch.empty((wl.W, total), dtype=torch.float32, pin_memory=True)
+        for w in range(wl.W):
+            h_in[w] = torch.from_numpy(np.concatenate([WL.grad_np(wl, p, w, m) for p in range(wl.nparams)]))
+        host.step(h_in, h_out)
+        torch.cuda.synchronize()
+        raw = [[[WL.grad_raw_np(wl, p, w, m) for p in range(wl.nparams)] for w in range(wl.W)]]
+        ref = O.run_workload(wl, orc, grads=raw, copy_back=False)
+        out = h_out.numpy().reshape(wl.W, host.replica_stride)
+        for b in range(plan.nbuckets):
+            lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
+            assert_bits_equal(out[:, lo:lo + n], ref["bucket"][b], f"step {m} bucket {b}")
+    host.close()

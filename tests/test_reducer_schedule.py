@@ -274,3 +274,23 @@ def test_used_allreduce_validation_without_launch():
     with pytest.raises(D.DdpError, match="local_used is NULL"):
         D.ddp_used_allreduce(None, 4, 2, 4, None, 0x1000, stream=0)
     D.ddp_used_allreduce(None, 0, 2, 0, None, 0x1000, stream=0)
+
+
+def test_wait_bucket_needs_flag_and_issue():
+    descs = [D.BucketDesc(8, 0, 0, None, None) for _ in range(2)]
+    r = D.ddp_reducer_create(2, [0, 1], [0, 1], descs, [0, 0], 2, D.DDP_ALLREDUCE,
+                             D.DDP_R_DRY_RUN | D.DDP_R_FUSED | D.DDP_R_BUCKET_DONE, replica_stride=8)
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready(r, 0)
+    D.ddp_reducer_wait_bucket(r, 0)
+    with pytest.raises(D.DdpError, match="not been issued"):
+        D.ddp_reducer_wait_bucket(r, 1)
+    with pytest.raises(D.DdpError, match="outside"):
+        D.ddp_reducer_wait_bucket(r, 2)
+    D.ddp_reducer_destroy(r)
+    r = make([0, 1])
+    D.ddp_reducer_prepare(r)
+    D.ddp_reducer_mark_ready(r, 0)
+    with pytest.raises(D.DdpError, match="DDP_R_BUCKET_DONE"):
+        D.ddp_reducer_wait_bucket(r, 0)
+    D.ddp_reducer_destroy(r)
