@@ -89,14 +89,18 @@ used_allreduce_kernel(const uint8_t* __restrict__ local, int64_t ld, int W, int6
     }
 }
 
-int sm_count()
+// Blocks that are resident at once: SMs x blocks per SM (a grid of one wave).
+int resident_blocks()
 {
     static int n = 0;
     if (!n) {
-        int dev = 0, v = 0;
+        int dev = 0, sms = 0, per_sm = 0;
         cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        n = v > 0 ? v : 1;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, used_allreduce_kernel, kThreads, 0) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        n = std::max(1, sms) * per_sm;
     }
     return n;
 }
@@ -118,7 +122,7 @@ extern "C" ddp_status ddp_used_allreduce(const uint8_t* local_used, int32_t ld, 
     const bool vec_rows = (reinterpret_cast<uintptr_t>(local_used) & 15) == 0 && (ld & 15) == 0;
     const int64_t groups = (static_cast<int64_t>(nparams) + kGroup - 1) / kGroup;
     const int64_t want = (groups + kThreads - 1) / kThreads;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8LL * sm_count())));
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, resident_blocks())));
     used_allreduce_kernel<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         local_used, ld, W, nparams, vec_rows, global_count, global_used);
     const cudaError_t err = cudaGetLastError();

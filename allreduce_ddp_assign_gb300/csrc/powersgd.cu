@@ -304,45 +304,56 @@ __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {   // every loop unrolled: the small matrices stay in registers
         double G[RP][RP], R[RP][RP], X[RP][RP];
         bool ok[RP];
-        int k = 0;
+        {
+            int k = 0;
+#pragma unroll
+            for (int c = 0; c < RP; ++c)
+#pragma unroll
+                for (int d = c; d < RP; ++d) {
+                    G[c][d] = G[d][c] = gsum[k];
+                    ++k;
+                }
+        }
+#pragma unroll
         for (int c = 0; c < RP; ++c)
-            for (int d = c; d < RP; ++d) {
-                G[c][d] = G[d][c] = gsum[k];
-                ++k;
-            }
-        for (int c = 0; c < RP; ++c)
+#pragma unroll
             for (int d = 0; d < RP; ++d) R[c][d] = X[c][d] = 0.0;
+#pragma unroll
         for (int c = 0; c < RP; ++c) {
-            ok[c] = false;
-            if (c >= m.r) continue;
             double d = G[c][c];
+#pragma unroll
             for (int q = 0; q < c; ++q)
                 if (ok[q]) d -= R[q][c] * R[q][c];
-            if (!(d > 0.0)) continue;
-            ok[c] = true;
-            R[c][c] = sqrt(d);
+            ok[c] = c < m.r && d > 0.0;
+            const double rc = ok[c] ? sqrt(d) : 1.0;
+            const double inv = 1.0 / rc;
+            R[c][c] = ok[c] ? rc : 0.0;
+#pragma unroll
             for (int e = c + 1; e < RP; ++e) {
                 double s = G[c][e];
+#pragma unroll
                 for (int q = 0; q < c; ++q)
                     if (ok[q]) s -= R[q][c] * R[q][e];
-                R[c][e] = s / R[c][c];
+                R[c][e] = ok[c] ? s * inv : 0.0;
             }
+            X[c][c] = ok[c] ? inv : 0.0;
         }
+#pragma unroll
         for (int c = 0; c < RP; ++c) {   // column c of R^-1 (zero for a dropped column)
-            if (!ok[c]) continue;
-            X[c][c] = 1.0 / R[c][c];
+#pragma unroll
             for (int r = c - 1; r >= 0; --r) {
-                if (!ok[r]) continue;
                 double s = 0.0;
-                for (int q = r + 1; q <= c; ++q)
-                    if (ok[q]) s += R[r][q] * X[q][c];
-                X[r][c] = -s / R[r][r];
+#pragma unroll
+                for (int q = r + 1; q <= c; ++q) s += R[r][q] * X[q][c];
+                X[r][c] = (ok[c] && ok[r]) ? -s * X[r][r] : 0.0;
             }
         }
+#pragma unroll
         for (int c = 0; c < RP; ++c)
+#pragma unroll
             for (int d = 0; d < RP; ++d) rinv[c][d] = static_cast<float>(X[c][d]);
     }
     __syncthreads();

@@ -555,7 +555,7 @@ def run_sweep(args):
             reps, timing = 100, "graph replay, 20 launches x 5, L2-resident"
             del g
         else:
-            reps = 5
+            reps = 5 if nbytes >= (256 << 20) else 20
             times = []
             for r in range(reps + 3):
                 flush.fill_(float(r))
