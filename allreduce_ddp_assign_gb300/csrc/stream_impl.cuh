@@ -255,14 +255,15 @@ __device__ __forceinline__ float4 lds_grad4(const unsigned char* base, int i)
     }
 }
 
-// WR: the 16-bit-input instantiations that round the ring's arithmetic to a
-// wire type (the compression hook).  The other 16-bit-input instantiations
-// have the plain fp32 multiply and add with no wire test in the loop: there the
-// test's predicated rounding path made the consumer warps ALU-bound (GPT-2's
-// bf16 buckets ran 35% slower with it).  The fp32-input instantiations keep the
-// runtime test on a.wire and so serve every wire type; measured back to back on
-// ResNet-50's buckets they run 4.5% faster with it than without (an isolated
-// launch under ncu is 2.5% slower: the gain is in consecutive launches).
+// WR: the instantiations that round the ring's arithmetic to a 16-bit wire type
+// (the compression hook).  The others carry the plain fp32 multiply and add,
+// with no wire test in the loop: there the test's predicated rounding path cost
+// the 16-bit-input fused launches 35% (GPT-2's bf16 buckets: the consumer warps
+// became ALU-bound) and an isolated 1 GiB ring launch 7%.  The fused fp32-input
+// instantiations are the exception: they keep the runtime test on a.wire (and
+// so serve every wire type), because back to back on ResNet-50's buckets they
+// measured 4.5% faster with it (an isolated launch under ncu is 2.5% slower:
+// the gain is in consecutive launches).
 template <int OP, int WT, int DT, bool ACC, bool WR>
 __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
 {
@@ -521,7 +522,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
                             t = has ? Lane<4>::add(m, t) : m;
                         }
                     }
-                    if constexpr (WR || DT == DDP_F32 || OP == OP_RING) {
+                    if constexpr (WR || (DT == DDP_F32 && OP != OP_RING)) {
                         t = ring_term(t, a.inv_w, static_cast<float>(W), a.wire);
                         sum[v] = (kk == 0) ? t : ring_add(sum[v], t, a.wire);
                     } else {
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
                         t = src ? Lane<1>::add(m, t) : m;
                     }
                 }
-                if constexpr (WR || DT == DDP_F32 || OP == OP_RING) {
+                if constexpr (WR || (DT == DDP_F32 && OP != OP_RING)) {
                     t = ring_term(t, a.inv_w, static_cast<float>(W), a.wire);
                     sum = (kk == 0) ? t : ring_add(sum, t, a.wire);
                 } else {
@@ -746,14 +747,15 @@ int tile_for_w(int W)
     }
 }
 
-// the operations a launch of one TU covers.  WR selects the 16-bit-input
-// instantiations with wire rounding; fp32 data (every ring launch, fp32
-// gradients) always takes the instantiations with the runtime wire test.
+// the operations a launch of one TU covers.  WR selects the instantiations with
+// wire rounding (ring launches, and fused launches of 16-bit gradients); fused
+// launches of fp32 gradients always take the instantiations with the runtime
+// wire test.
 template <int OP, bool WR>
 ddp_status launch_op(StreamArgs& a, int dtype, void* stream)
 {
     if constexpr (OP == OP_RING) {
-        return dispatch_w<OP_RING, DDP_F32, false, false>(a, stream);
+        return dispatch_w<OP_RING, DDP_F32, false, WR>(a, stream);
     } else {
         const bool acc = a.accumulate != 0;
         switch (dtype) {

@@ -42,7 +42,8 @@ ddp_status launch_stream(int op, StreamArgs& a, int dtype, void* stream)
     a.status = status_word();
     if (!a.status) return ddp::fail(DDP_E_CUDA, "stream kernel: device status word unavailable");
     a.store_bulk = op != OP_PACK && a.mode == DDP_ALLREDUCE;
-    if (op == OP_RING) return launch_op<OP_RING, false>(a, dtype, stream);   // fp32 data: runtime wire test
+    if (op == OP_RING)
+        return a.wire == DDP_F32 ? launch_op<OP_RING, false>(a, dtype, stream) : launch_op<OP_RING, true>(a, dtype, stream);
     if (op == OP_PACK) return launch_stream_pack(a, dtype, stream);
     return launch_stream_fused(a, dtype, stream);
 }
