@@ -158,9 +158,11 @@ class HostBucketReducer:
 
     host_in   pinned [W, total] tensor (gradient dtype): replica w's gradients of
               all parameters back to back in parameter order.
-    host_out  pinned [W * replica_stride] fp32 tensor; every bucket's elements
-              (main_grad layout) are written, the alignment gaps between
-              buckets are not.
+    host_out  pinned [W * replica_stride] fp32 tensor in main_grad layout.  After an
+              allreduce every bucket's elements are written (the alignment gaps
+              between buckets are not); after a reduce_scatter replica w's copy
+              receives only its own shard w of each bucket, the part a rank
+              keeps (Megatron's start_grad_sync).
     """
 
     def __init__(self, numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, torch_dtype,
@@ -193,7 +195,11 @@ class HostBucketReducer:
         self.reduced = None      # event: the previous step's reductions are done (dev_in may be overwritten)
         self.downloaded = None   # event: the previous step's copies to the host are done (main_grad may be)
         self.h2d_bytes = int(self.offs[-1]) * W * self.dev_in.element_size()
-        self.d2h_bytes = sum(int(plan.bucket_numel[b]) for b in range(plan.nbuckets)) * W * 4
+        self.reduce_scatter = int(mode) == 1
+        if self.reduce_scatter:
+            self.d2h_bytes = sum(int(plan.bucket_numel[b]) for b in range(plan.nbuckets)) * 4
+        else:
+            self.d2h_bytes = sum(int(plan.bucket_numel[b]) for b in range(plan.nbuckets)) * W * 4
 
     @property
     def replica_stride(self) -> int:
@@ -229,8 +235,10 @@ class HostBucketReducer:
                 ddp_reducer_wait_bucket(r.handle, b, self.d2h)
                 lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
                 for w in range(self.W):
-                    host_out[w * stride + lo:w * stride + lo + n].copy_(r.main_grad[w * stride + lo:w * stride + lo + n],
-                                                                       non_blocking=True)
+                    a, z = w * stride + lo, w * stride + lo + n
+                    if self.reduce_scatter:   # shard w = bucket elements [w n / W, (w + 1) n / W)
+                        a, z = a + w * (n // self.W), a + (w + 1) * (n // self.W)
+                    host_out[a:z].copy_(r.main_grad[a:z], non_blocking=True)
         self.downloaded = torch.cuda.Event()
         self.downloaded.record(self.d2h)
         ddp_reducer_finalize(r.handle, stream, 0)

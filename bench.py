@@ -438,7 +438,7 @@ def run_ours(args, wl):
         e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
         e2e = {"value": round(job_value(world, step_bytes, Ke, e_ms), 3), "unit": "GB/s",
                "h2d_bytes_per_step": int(h_in.numel() * h_in.element_size()),
-               "d2h_bytes_per_step": int(h_out.numel() * 4), "steps": Ke}
+               "d2h_bytes_per_step": int(host.d2h_bytes), "steps": Ke}
         host.close()
 
     cpu = None

@@ -781,3 +781,31 @@ def test_host_front_end_pipeline_vs_oracle(orc, name):
             lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
             assert_bits_equal(out[:, lo:lo + n], ref["bucket"][b], f"step {m} bucket {b}")
     host.close()
+
+
+def test_host_front_end_reduce_scatter_shards(orc):
+    """Reduce_scatter through the host front end: replica w's host copy receives
+    exactly shard w of every bucket (bit for bit), and nothing outside it."""
+    from allreduce_ddp_assign_gb300.session import HostBucketReducer
+
+    wl = WL.Workload("linear12_rs", WL.linear12(), 4, 1, 2, 8 << 20, 8 << 20, 4, 0, "dyadic12", 1.0, 91)
+    host = HostBucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                             wl.first_cap_bytes, wl.pad_multiple, torch.float32)
+    plan = host.reducer.plan
+    total = int(host.offs[-1])
+    h_in = torch.empty((wl.W, total), dtype=torch.float32, pin_memory=True)
+    for w in range(wl.W):
+        h_in[w] = torch.from_numpy(np.concatenate([WL.grad_np(wl, p, w) for p in range(wl.nparams)]))
+    h_out = torch.full((wl.W * host.replica_stride,), -5.0, dtype=torch.float32, pin_memory=True)
+    host.step(h_in, h_out)
+    torch.cuda.synchronize()
+    ref = O.run_workload(wl, orc, copy_back=False)
+    out = h_out.numpy().reshape(wl.W, host.replica_stride)
+    for b in range(plan.nbuckets):
+        lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
+        k = n // wl.W
+        for w in range(wl.W):
+            assert_bits_equal(out[w, lo + w * k:lo + (w + 1) * k], ref["bucket"][b][w, w * k:(w + 1) * k],
+                              f"bucket {b} shard {w}")
+            assert np.all(out[w, lo:lo + w * k] == -5.0) and np.all(out[w, lo + (w + 1) * k:lo + n] == -5.0)
+    host.close()
