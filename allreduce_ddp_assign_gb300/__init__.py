@@ -97,6 +97,7 @@ _SIGS = {
     "ddp_reducer_destroy": (None, [_vp]),
     "ddp_set_kernel_variant": (C.c_int32, [C.c_int32]),
     "ddp_device_status": (C.c_int32, [_vp, _i32p, C.c_int32]),
+    "ddp_wait_selftest": (C.c_int32, [C.c_int32, C.c_int64, _vp]),
     "ddp_status_str": (C.c_char_p, [C.c_int32]),
     "ddp_last_error_message": (C.c_char_p, []),
     "ddp_version": (C.c_int32, []),
@@ -452,6 +453,10 @@ def ddp_device_status(stream=None, reset=False) -> int:
     return v.value
 
 
+def ddp_wait_selftest(arrive, limit_ns, stream=None) -> None:
+    _check(lib().ddp_wait_selftest(int(arrive), int(limit_ns), _stream(stream)))
+
+
 def ddp_status_str(s: int) -> str:
     return lib().ddp_status_str(int(s)).decode()
 
@@ -467,3 +472,4 @@ def ddp_version() -> int:
 from .plan import Plan  # noqa: E402  (plumbing over the calls above)
 
 __all__ = [n for n in _SIGS] + ["Plan", "BucketDesc", "DdpError", "lib", "library_path"]
+

@@ -171,14 +171,14 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
-// Wait for the phase with the given parity; false after about kWaitNs.
-__device__ __forceinline__ bool wait_bounded(uint64_t* b, uint32_t parity)
+// Wait for the phase with the given parity; false after about limit_ns.
+__device__ __forceinline__ bool wait_bounded(uint64_t* b, uint32_t parity, uint64_t limit_ns = kWaitNs)
 {
     if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1; i < (1u << 28); ++i) {
         if (mbar_try_wait(b, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitNs) break;
+        if ((i & 255u) == 0 && globaltimer() - t0 > limit_ns) break;
     }
     return false;
 }

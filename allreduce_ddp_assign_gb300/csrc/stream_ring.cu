@@ -65,7 +65,50 @@ ddp_status read_device_status(void* stream, int32_t* out, int reset)
     return ddp::ok();
 }
 
+namespace {
+
+// The failure path of the streaming kernels' waits, on its own: one block waits
+// (bounded by limit_ns) on an mbarrier that expects one arrival, which a thread
+// makes only when `arrive` is set.  A thread that gives up records the timeout
+// in the status word as the streaming kernels do; the block then invalidates
+// the barrier and returns.
+__global__ void wait_selftest_kernel(int* status, int arrive, uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (arrive && threadIdx.x == 0) mbar_arrive(&bar);
+    const bool got = wait_bounded(&bar, 0, limit_ns);
+    if (!got) record_error(status, kErrWaitTimeout);
+    __syncthreads();
+    if (threadIdx.x == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(su32(&bar)) : "memory");
+}
+
+}  // namespace
+
+ddp_status wait_selftest(int32_t arrive, int64_t limit_ns, void* stream)
+{
+    if (limit_ns < 1000 || limit_ns > static_cast<int64_t>(kWaitNs))
+        return ddp::fail(DDP_E_INVAL, "ddp_wait_selftest: limit_ns = %lld outside [1000, %llu]",
+                         static_cast<long long>(limit_ns), static_cast<unsigned long long>(kWaitNs));
+    int* status = status_word();
+    if (!status) return ddp::fail(DDP_E_CUDA, "ddp_wait_selftest: device status word unavailable");
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, arrive != 0,
+                                                                          static_cast<uint64_t>(limit_ns));
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_wait_selftest: launch failed: %s", cudaGetErrorString(err));
+    return ddp::ok();
+}
+
 }  // namespace ddpk
+
+extern "C" ddp_status ddp_wait_selftest(int32_t arrive, int64_t limit_ns, void* stream)
+{
+    return ddpk::wait_selftest(arrive, limit_ns, stream);
+}
 
 extern "C" ddp_status ddp_device_status(void* stream, int32_t* status, int32_t reset)
 {

@@ -760,6 +760,18 @@ ddp_status ddp_set_kernel_variant(int32_t variant);
  */
 ddp_status ddp_device_status(void* stream, int32_t* status, int32_t reset);
 
+/*
+ * ddp_wait_selftest -- exercise the streaming kernels' failure path without a
+ * fault: one block waits, bounded by limit_ns (1 us .. 2 s), on an mbarrier
+ * that completes only if arrive != 0.  When nothing arrives the wait gives up,
+ * bit 0 of the device status word is set exactly as a streaming kernel sets it,
+ * and the block returns; the context stays usable.  Asynchronous on `stream`;
+ * read the result with ddp_device_status.  The pages have no counterpart: this
+ * is the library's own check of its failure detection.
+ * Errors: DDP_E_INVAL (limit out of range); DDP_E_CUDA.
+ */
+ddp_status ddp_wait_selftest(int32_t arrive, int64_t limit_ns, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Errors and version                                                        */
 /* ------------------------------------------------------------------------ */

@@ -99,3 +99,10 @@ def test_assign_capacity():
                                     small[1].ctypes.data_as(i64), small[2].ctypes.data_as(i32),
                                     small[3].ctypes.data_as(i32), 2, C.byref(nb))
     assert st == D.DDP_E_CAPACITY and nb.value == 5
+
+
+def test_wait_selftest_validation():
+    with pytest.raises(D.DdpError, match="limit_ns"):
+        D.ddp_wait_selftest(0, 10, stream=0)
+    with pytest.raises(D.DdpError, match="limit_ns"):
+        D.ddp_wait_selftest(0, 3_000_000_000, stream=0)

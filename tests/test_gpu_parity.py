@@ -441,6 +441,7 @@ def test_reducer_waits_for_producer_stream(orc):
 def test_reducer_finalize_timeout_then_recovers(orc):
     wl = WL.c1_mlp()
     sess = make_session(wl, device_grads(wl))
+    sess.step()                # loads the library's kernels first (a lazy module load can wait for the GPU)
     torch.cuda.synchronize()
     with torch.cuda.stream(sess.side):
         torch.cuda._sleep(400_000_000)   # ~0.2 s of spinning on the side stream (bounded)
@@ -461,6 +462,7 @@ def test_finalize_orders_the_default_stream(orc):
     even though the side stream was held back first."""
     wl = WL.c1_mlp()
     sess = make_session(wl, device_grads(wl))
+    sess.step()                # loads the library's kernels first (a lazy module load can wait for the GPU)
     sess.main_grad.zero_()
     torch.cuda.synchronize()
     with torch.cuda.stream(sess.side):
@@ -809,3 +811,21 @@ def test_host_front_end_reduce_scatter_shards(orc):
                               f"bucket {b} shard {w}")
             assert np.all(out[w, lo:lo + w * k] == -5.0) and np.all(out[w, lo + (w + 1) * k:lo + n] == -5.0)
     host.close()
+
+
+def test_wait_failure_path_reports_and_recovers(orc):
+    """Failure detection without a fault: a bounded wait on a barrier nothing
+    completes gives up after its limit and sets the device status word; with the
+    arrival it completes cleanly; afterwards the context still reduces correctly."""
+    assert D.ddp_device_status(reset=True) in (0, 1)
+    D.ddp_wait_selftest(1, 1_000_000)
+    assert D.ddp_device_status() == 0
+    D.ddp_wait_selftest(0, 1_000_000)        # nothing arrives: gives up after ~1 ms
+    assert D.ddp_device_status(reset=True) == 1
+    assert D.ddp_device_status() == 0
+    x = WL.bucket_np(4096 * 4 * 8, 8)
+    t = torch.from_numpy(x).to(DEV)
+    D.ddp_bucket_allreduce(t, t.shape[1], t.shape[1], 8, D.DDP_ALLREDUCE)
+    want, _ = orc.ring(x.copy())
+    assert_bits_equal(t.cpu().numpy(), want, "allreduce after the timed-out wait")
+    assert D.ddp_device_status() == 0
