@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import BucketDesc, ddp_assign_buckets
+from . import BucketDesc, ddp_assign_buckets, ddp_assign_buckets_ordered
 
 ALIGN_ELEMS = 64
 
@@ -30,6 +30,8 @@ class Plan:
         a = ddp_assign_buckets(self.numels, self.dtypes, cap_bytes, first_cap_bytes, order, pad_multiple,
                                grad_reduce_in_fp32)
         self.assignment = a
+        self.caps = dict(cap_bytes=int(cap_bytes), first_cap_bytes=int(first_cap_bytes), order=int(order),
+                         pad_multiple=int(pad_multiple), grad_reduce_in_fp32=int(grad_reduce_in_fp32))
         self.nbuckets = B = a["nbuckets"]
         self.bucket_of = a["bucket_of"]
         self.offset_of = a["offset_of"]
@@ -65,6 +67,26 @@ class Plan:
             self.descs.append(BucketDesc(int(self.bucket_numel[b]), len(self.members[b]), int(self.bucket_dtype[b]),
                                          self.seg_offset_dev.data_ptr() + 8 * o,
                                          self.seg_param_dev.data_ptr() + 4 * q))
+
+    # -- description ----------------------------------------------------------
+    def describe(self) -> dict:
+        """The plan as DDP's logging data reports it ("DDP: ring AllReduce and
+        gradient buckets" 17.13: bucket_sizes): per bucket its bytes, padded
+        elements, dtype and parameter indices, and the issue order."""
+        B = self.nbuckets
+        return dict(num_buckets=B, bucket_sizes=[int(self.bucket_bytes[b]) for b in range(B)],
+                    bucket_numel=[int(self.bucket_numel[b]) for b in range(B)],
+                    bucket_dtype=[int(self.bucket_dtype[b]) for b in range(B)],
+                    bucket_params=[list(self.members[b]) for b in range(B)],
+                    bucket_order=[int(v) for v in self.bucket_order], **self.caps)
+
+    def rebuilt(self, sequence) -> dict:
+        """The buckets a rebuild would form over the observed gradient-ready
+        sequence (ddp_assign_buckets_ordered), as plain lists."""
+        a = ddp_assign_buckets_ordered(self.numels, sequence, self.dtypes, self.caps["cap_bytes"],
+                                       self.caps["first_cap_bytes"], self.caps["pad_multiple"],
+                                       self.caps["grad_reduce_in_fp32"])
+        return dict(num_buckets=int(a["nbuckets"]), bucket_sizes=[int(v) for v in a["bucket_bytes"]])
 
     # -- buffers and tables -------------------------------------------------
     def alloc_main_grad(self, W: int, fill: float = 0.0):

@@ -14,7 +14,7 @@ from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, 
                ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
                ddp_reducer_find_unused, ddp_reducer_mark_ready_many, ddp_reducer_prepare,
-               ddp_reducer_register_powersgd, ddp_reducer_set_local_used)
+               ddp_reducer_ready_order, ddp_reducer_register_powersgd, ddp_reducer_set_local_used, DdpError)
 
 
 class BucketReducer:
@@ -126,6 +126,21 @@ class BucketReducer:
 
     def issue_log(self):
         return ddp_reducer_issue_log(self.handle)
+
+    def logging_data(self) -> dict:
+        """DDP's logging data ("DDP: ring AllReduce and gradient buckets" 17.13):
+        the plan's bucket sizes and parameters, and once an iteration has been
+        finalized the order its gradients arrived in and the rebuilt bucket sizes
+        that order gives (rebuilt_bucket_sizes)."""
+        d = self.plan.describe()
+        try:
+            seq = ddp_reducer_ready_order(self.handle)
+        except DdpError:
+            return d
+        d["ready_order"] = [int(p) for p in seq]
+        if len(seq) == self.plan.nparams:
+            d["rebuilt_bucket_sizes"] = self.plan.rebuilt(seq)["bucket_sizes"]
+        return d
 
     def bucket_ms(self):
         return ddp_reducer_bucket_ms(self.handle, self.plan.nbuckets)

@@ -79,13 +79,15 @@ def test_allreduce_nonfinite_propagates(orc):
     x = np.ones((W, n), np.float32)
     x[2, 10] = np.inf
     x[1, 20], x[3, 20] = np.inf, -np.inf
+    x[0, 3000] = np.nan            # a poisoned gradient on one rank reaches every rank
     t = torch.from_numpy(x).to(DEV)
     D.ddp_bucket_allreduce(t, n, n, W, D.DDP_ALLREDUCE)
     got = t.cpu().numpy()
     want, _ = orc.ring(x.copy())
-    assert np.all(np.isposinf(got[:, 10])) and np.all(np.isnan(got[:, 20]))
+    assert np.all(np.isposinf(got[:, 10])) and np.all(np.isnan(got[:, 20])) and np.all(np.isnan(got[:, 3000]))
+    assert np.all(np.isnan(want[:, 3000]))
     mask = np.ones(n, bool)
-    mask[20] = False
+    mask[[20, 3000]] = False
     assert_bits_equal(got[:, mask], want[:, mask])
 
 
@@ -829,3 +831,18 @@ def test_wait_failure_path_reports_and_recovers(orc):
     want, _ = orc.ring(x.copy())
     assert_bits_equal(t.cpu().numpy(), want, "allreduce after the timed-out wait")
     assert D.ddp_device_status() == 0
+
+
+def test_reducer_logging_data_after_iteration():
+    """After one iteration the reducer reports the plan, the gradient-ready order it
+    saw and the rebuilt bucket sizes of that order (twelve Linear layers: the DDP
+    chapter's 4198400 / 29388800 / 16793600)."""
+    wl = WL.Workload("linear12", WL.linear12(), 2, 0, 1, 25 << 20, 1 << 20, 1, 0, "dyadic12", 1.0, 78)
+    sess = make_session(wl, device_grads(wl))
+    assert "ready_order" not in sess.logging_data()
+    sess.step()
+    torch.cuda.synchronize()
+    d = sess.logging_data()
+    assert d["ready_order"] == list(range(wl.nparams - 1, -1, -1))
+    assert d["rebuilt_bucket_sizes"] == [4198400, 29388800, 16793600]
+    sess.close()

@@ -78,3 +78,17 @@ def test_overlap_timeline_vs_oracle(orc):
         want = orc.overlap_timeline(ready, r["bucket_of"], r["bucket_order"], r["bucket_bytes"], a, b)
         assert np.array_equal(got["start_ms"], want["start_ms"]) and np.array_equal(got["end_ms"], want["end_ms"])
         assert got["step_ms"] == want["step_ms"] and got["serial_ms"] == want["serial_ms"]
+
+
+def test_plan_describe_and_rebuild_twelve_linear():
+    """The plan's logging data: the twelve Linear(1024, 1024) layers give the DDP
+    chapter's rebuilt byte list (17.13) when rebuilt over the reverse order, and the
+    description lists every parameter once."""
+    from allreduce_ddp_assign_gb300.plan import Plan
+
+    numels = [n for _ in range(12) for n in (1024 * 1024, 1024)]
+    plan = Plan(numels, device="cpu")
+    d = plan.describe()
+    assert sorted(p for b in d["bucket_params"] for p in b) == list(range(24))
+    assert d["num_buckets"] == len(d["bucket_sizes"]) == plan.nbuckets
+    assert plan.rebuilt(list(range(23, -1, -1)))["bucket_sizes"] == [4198400, 29388800, 16793600]
