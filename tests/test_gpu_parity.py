@@ -846,3 +846,32 @@ def test_reducer_logging_data_after_iteration():
     assert d["ready_order"] == list(range(wl.nparams - 1, -1, -1))
     assert d["rebuilt_bucket_sizes"] == [4198400, 29388800, 16793600]
     sess.close()
+
+
+def test_host_front_end_bf16_megatron_reduce_scatter(orc):
+    """bf16 gradients from pinned host memory, Megatron buckets (padded to W),
+    reduce_scatter: each replica's shard of every bucket, bit for bit."""
+    from allreduce_ddp_assign_gb300.session import HostBucketReducer
+
+    wl = WL.Workload("linear12_bf16_rs", WL.linear12(), 4, 1, 2, 6 << 20, 6 << 20, 4, WL.BF16, "normal", 1e-2, 92)
+    host = HostBucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                             wl.first_cap_bytes, wl.pad_multiple, torch.bfloat16)
+    plan = host.reducer.plan
+    total = int(host.offs[-1])
+    h_in = torch.empty((wl.W, total), dtype=torch.bfloat16, pin_memory=True)
+    for w in range(wl.W):
+        raw = np.concatenate([WL.grad_raw_np(wl, p, w) for p in range(wl.nparams)]).astype(np.uint16)
+        h_in[w] = torch.from_numpy(raw.view(np.int16)).view(torch.bfloat16)
+    h_out = torch.full((wl.W * host.replica_stride,), -5.0, dtype=torch.float32, pin_memory=True)
+    host.step(h_in, h_out)
+    torch.cuda.synchronize()
+    ref = O.run_workload(wl, orc, copy_back=False)
+    out = h_out.numpy().reshape(wl.W, host.replica_stride)
+    assert plan.nbuckets > 1
+    for b in range(plan.nbuckets):
+        lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
+        k = n // wl.W
+        for w in range(wl.W):
+            assert_bits_equal(out[w, lo + w * k:lo + (w + 1) * k], ref["bucket"][b][w, w * k:(w + 1) * k],
+                              f"bucket {b} shard {w}")
+    host.close()
