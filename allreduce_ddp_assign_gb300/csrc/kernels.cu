@@ -318,11 +318,26 @@ void set_mg(Ctx& cx, float* mg, int64_t stride)
 int g_variant = DDP_KERNEL_AUTO;
 int kernel_variant() { return g_variant; }
 
+// Under DDP_KERNEL_AUTO, a launch of one bucket with at most this many elements over
+// all replicas (numel x W) goes to the plain kernel: the streaming kernel's fixed
+// cost (a CTA per SM, barrier set-up, filling the stage ring) outweighs its higher
+// bandwidth there.  Measured on GB300: a 0.2M-element bucket at W = 4 takes 8.2 us
+// plain against 11.8 us streaming; the crossover lies between 2^21 and 2^22.
+constexpr int64_t kSmallLaunch = int64_t{1} << 21;
+
+bool use_stream(int op, int32_t W, int32_t dtype, bool acc, int32_t mode, int64_t numel, int32_t nbuckets)
+{
+    const int v = kernel_variant();
+    if (v == DDP_KERNEL_PLAIN) return false;
+    if (v == DDP_KERNEL_AUTO && nbuckets == 1 && numel * W <= kSmallLaunch) return false;
+    return stream_supported(op, W, dtype, acc, mode);
+}
+
 }  // namespace ddpk
 
 extern "C" ddp_status ddp_set_kernel_variant(int32_t variant)
 {
-    if (variant != DDP_KERNEL_AUTO && variant != DDP_KERNEL_PLAIN)
+    if (variant != DDP_KERNEL_AUTO && variant != DDP_KERNEL_PLAIN && variant != DDP_KERNEL_STREAM)
         return ddp::fail(DDP_E_INVAL, "ddp_set_kernel_variant: unknown variant %d", variant);
     ddpk::g_variant = variant;
     return ddp::ok();
@@ -340,7 +355,7 @@ ddp_status launch_allreduce(float* replicas, int64_t stride, int64_t n, int32_t 
     Ctx cx = base_ctx(n, W, true, mode);
     set_mg(cx, replicas, stride);
     cx.wire = wire;
-    if (kernel_variant() == DDP_KERNEL_AUTO && cx.mg_vec && stream_supported(OP_RING, W, DDP_F32, false, mode)) {
+    if (cx.mg_vec && use_stream(OP_RING, W, DDP_F32, false, mode, n, 1)) {
         StreamArgs a{};
         a.total = n;
         a.stride = stride;
@@ -359,7 +374,7 @@ ddp_status launch_pack(const ddp_bucket_desc& b, const void* const* grads, const
                        int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream)
 {
     if (b.numel == 0) return ok();
-    if (kernel_variant() == DDP_KERNEL_AUTO && stream_supported(OP_PACK, W, b.dtype, accumulate != 0, DDP_ALLREDUCE)) {
+    if (use_stream(OP_PACK, W, b.dtype, accumulate != 0, DDP_ALLREDUCE, b.numel, 1)) {
         float* mgs[1] = {main_grad};
         return launch_pack_group(&b, mgs, 1, grads, used, ld, W, accumulate, stride, stream);
     }
@@ -409,7 +424,7 @@ ddp_status launch_fused(const ddp_bucket_desc& b, const void* const* grads, cons
     cx.global_used = global_used;
     cx.accumulate = accumulate != 0;
     cx.wire = wire;
-    if (kernel_variant() == DDP_KERNEL_AUTO && stream_supported(OP_FUSED, W, b.dtype, cx.accumulate, mode)) {
+    if (use_stream(OP_FUSED, W, b.dtype, cx.accumulate, mode, b.numel, 1)) {
         float* mgs[1] = {main_grad};
         return launch_fused_group(&b, mgs, 1, grads, used, ld, W, mode, accumulate, stride, grads_out, global_used,
                                   stream, wire);
@@ -428,10 +443,14 @@ ddp_status launch_group(int op, const ddp_bucket_desc* bs, float* const* mgs, in
     int32_t i = 0;
     while (i < nb) {
         const int32_t dt = bs[i].dtype;
-        if (kernel_variant() != DDP_KERNEL_AUTO || !stream_supported(op, W, dt, acc, mode)) {
-            const ddp_status st = single(i);
-            if (st != DDP_OK) return st;
-            ++i;
+        int32_t run = 0;
+        int64_t run_numel = 0;
+        while (i + run < nb && run < kMaxBatch && bs[i + run].dtype == dt) run_numel += bs[i + run++].numel;
+        if (!use_stream(op, W, dt, acc, mode, run_numel, run)) {
+            for (const int32_t end = i + run; i < end; ++i) {
+                const ddp_status st = single(i);
+                if (st != DDP_OK) return st;
+            }
             continue;
         }
         StreamArgs a{};

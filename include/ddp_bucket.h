@@ -739,16 +739,19 @@ void ddp_reducer_destroy(ddp_reducer* r);
 /* ------------------------------------------------------------------------ */
 /*
  * Two implementations compute every data-path call with identical results:
- *   DDP_KERNEL_AUTO   (default) ddp_bucket_allreduce and ddp_fused_bucket use
- *                     the TMA-pipelined streaming kernel where its shared-memory
- *                     stage ring fits (2 <= W <= 16, vector-aligned main_grad
- *                     for the allreduce); everything else uses the plain kernel.
+ *   DDP_KERNEL_STREAM every launch the TMA-pipelined streaming kernel can take
+ *                     (its shared-memory stage ring fits: 2 <= W <= 16, and a
+ *                     vector-aligned main_grad for the allreduce) uses it; the
+ *                     rest use the plain kernel.
+ *   DDP_KERNEL_AUTO   (default) as DDP_KERNEL_STREAM, except that a launch of a
+ *                     single bucket with numel x W <= 2^21 elements uses the
+ *                     plain kernel, which finishes such small launches first.
  *   DDP_KERNEL_PLAIN  every call uses the plain kernel (16-byte loads straight
  *                     into registers).
  * The choice is process-wide and applies to calls made after it.
  * Errors: DDP_E_INVAL for an unknown variant.
  */
-enum { DDP_KERNEL_AUTO = 0, DDP_KERNEL_PLAIN = 1 };
+enum { DDP_KERNEL_AUTO = 0, DDP_KERNEL_PLAIN = 1, DDP_KERNEL_STREAM = 2 };
 ddp_status ddp_set_kernel_variant(int32_t variant);
 
 /*

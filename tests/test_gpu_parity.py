@@ -21,10 +21,12 @@ if not torch.cuda.is_available():  # pragma: no cover
 DEV = torch.device("cuda:0")
 
 
-@pytest.fixture(params=[D.DDP_KERNEL_AUTO, D.DDP_KERNEL_PLAIN], ids=["auto", "plain"])
+@pytest.fixture(params=[D.DDP_KERNEL_AUTO, D.DDP_KERNEL_PLAIN, D.DDP_KERNEL_STREAM],
+                ids=["auto", "plain", "stream"])
 def variant(request):
-    """Both implementations (the TMA-pipelined streaming kernel where it applies,
-    and the plain 16-byte-load kernel) must match the oracle."""
+    """Both implementations (the TMA-pipelined streaming kernel wherever it applies,
+    and the plain 16-byte-load kernel) and the default mix of the two (small
+    single-bucket launches plain) must match the oracle."""
     D.ddp_set_kernel_variant(request.param)
     yield request.param
     D.ddp_set_kernel_variant(D.DDP_KERNEL_AUTO)
