@@ -20,7 +20,10 @@
 //                       the split's rows shared by the block's warps; the last
 //                       block of a column block sums the partials in a fixed
 //                       order into Q = (sum_w M_w^T P) / W
-//   psgd_out_kernel     per row: G^ = P Q^T written to every replica, E = M - G^
+//   psgd_out_kernel     G^ = P Q^T written to every replica, E = M - G^: flat
+//                       tiles of 16-byte quads over the matrix's rows laid end to
+//                       end (a warp per row where rows are not 16-byte multiples),
+//                       one wave of blocks looping over the tiles
 // Every kernel streams its matrix once: the contraction is rank R (1..8)
 // against a row or column of M, R fused multiply-adds per element and 4 to 12
 // bytes per element, far below the CUDA cores' arithmetic ridge, so the work is
@@ -46,7 +49,8 @@ constexpr int kRowsPerSplit = 256;     // rows of one partial M^T P
 constexpr int kMaxPairs = 256;         // (row, replica) pairs per P tile
 constexpr int kMaxRowsP = 16;          // rows per P tile
 constexpr int kGW = 4;                 // replicas a warp carries at once in the P pass
-constexpr int kOutBatch = 4;           // replicas whose error loads the output pass issues together
+constexpr int kOutBatch = 8;           // replicas whose error loads the output pass issues together
+constexpr int kOutQuads = 2048;        // 16-byte quads per flat output tile
 constexpr int64_t kVecPiece = 16384;   // elements of a 1-D tensor per block
 
 struct PsgdMat {
@@ -85,6 +89,7 @@ struct PsgdArgs {
     const int4* tiles;
     const PsgdVec* vecs;
     int32_t n_ptiles; // blocks of the P launch past this take the 1-D tensors
+    int32_t n_otiles; // output tiles (the output launch's blocks loop over them)
     int32_t ncnt;
     int32_t W;
     int32_t ef;
@@ -482,10 +487,11 @@ __global__ void __launch_bounds__(kThreads) psgd_qpart_kernel(const PsgdArgs a)
 // ---------------------------------------------------------------------------
 // G^ = P Q^T on every replica, E = M - G^  (tile: {mat, row0, nrows}; one warp per row)
 // ---------------------------------------------------------------------------
+// Output rows of a row tile {mat, row0, rows, 0}: a warp per row (matrices whose
+// rows are not 16-byte multiples).
 template <int RP>
-__global__ void __launch_bounds__(kThreads) psgd_out_kernel(const PsgdArgs a)
+__device__ void out_rows(const PsgdArgs& a, const int4 t)
 {
-    const int4 t = a.tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp >= t.z) return;
     const PsgdMat m = a.mats[t.x];
@@ -494,54 +500,99 @@ __global__ void __launch_bounds__(kThreads) psgd_out_kernel(const PsgdArgs a)
     load_row<RP>(a.P + m.p_off + static_cast<int64_t>(row) * RP, pr);
     const float* q = a.Q + m.q_off;
     const int64_t base = m.off + static_cast<int64_t>(row) * m.N;
-    const bool vec = m.vec && a.vec_ok;
-    if (vec) {
-        for (int j = 4 * lane; j < m.N; j += 128) {
-            float h[4];
+    for (int j = lane; j < m.N; j += 32) {
+        float qv[RP];
+        load_row<RP>(q + static_cast<int64_t>(j) * RP, qv);
+        float h = 0.f;
+#pragma unroll
+        for (int r = 0; r < RP; ++r) h = fmaf(pr[r], qv[r], h);
+        for (int w = 0; w < a.W; ++w) {
+            if (a.ef) {
+                float* e = a.err + w * a.estride + base + j;
+                *e = __fsub_rn(*e, h);
+            }
+            a.mg[w * a.stride + base + j] = h;
+        }
+    }
+}
+
+// Output of a flat tile {mat, quad0, quads, 1}: the matrix's rows laid end to end
+// as 16-byte quads (N a multiple of 4), thread i taking quads i, i + 256, ...  Each
+// quad's error loads for a batch of replicas are issued before the reads of P and
+// Q that give G^ = P Q^T, then G^ goes to every replica and E - G^ back into E.
+template <int RP>
+__device__ void out_quads(const PsgdArgs& a, const int4 t)
+{
+    const PsgdMat m = a.mats[t.x];
+    const int64_t n4 = m.N >> 2;
+    const float* q = a.Q + m.q_off;
+    const float* p = a.P + m.p_off;
+    for (int k = threadIdx.x; k < t.z; k += kThreads) {
+        const int64_t quad = static_cast<int64_t>(t.y) + k;
+        const int64_t row = quad / n4;
+        const int64_t col = (quad - row * n4) * 4;
+        const int64_t e = m.off + quad * 4;
+        float h[4];
+        auto compute_h = [&]() {
+            float pr[RP];
+            load_row<RP>(p + row * RP, pr);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float qv[RP];
-                load_row<RP>(q + static_cast<int64_t>(j + c) * RP, qv);
-                float s = 0.f;
+                load_row<RP>(q + (col + c) * RP, qv);
+                float v = 0.f;
 #pragma unroll
-                for (int r = 0; r < RP; ++r) s = fmaf(pr[r], qv[r], s);
-                h[c] = s;
+                for (int r = 0; r < RP; ++r) v = fmaf(pr[r], qv[r], v);
+                h[c] = v;
             }
-            const float4 hv = make_float4(h[0], h[1], h[2], h[3]);
+        };
+        if (a.vec_ok) {
             for (int w0 = 0; w0 < a.W; w0 += kOutBatch) {
                 const int nb = min(kOutBatch, a.W - w0);
-                if (a.ef) {   // the batch's loads first, then its stores
-                    float4 x[kOutBatch];
-#pragma unroll
-                    for (int k = 0; k < kOutBatch; ++k)
-                        if (k < nb) x[k] = __ldcs(reinterpret_cast<const float4*>(a.err + (w0 + k) * a.estride + base + j));
-#pragma unroll
-                    for (int k = 0; k < kOutBatch; ++k)
-                        if (k < nb)
-                            __stcs(reinterpret_cast<float4*>(a.err + (w0 + k) * a.estride + base + j),
-                                   make_float4(__fsub_rn(x[k].x, h[0]), __fsub_rn(x[k].y, h[1]), __fsub_rn(x[k].z, h[2]),
-                                               __fsub_rn(x[k].w, h[3])));
-                }
-#pragma unroll
-                for (int k = 0; k < kOutBatch; ++k)
-                    if (k < nb) __stcs(reinterpret_cast<float4*>(a.mg + (w0 + k) * a.stride + base + j), hv);
-            }
-        }
-    } else {
-        for (int j = lane; j < m.N; j += 32) {
-            float qv[RP];
-            load_row<RP>(q + static_cast<int64_t>(j) * RP, qv);
-            float h = 0.f;
-#pragma unroll
-            for (int r = 0; r < RP; ++r) h = fmaf(pr[r], qv[r], h);
-            for (int w = 0; w < a.W; ++w) {
+                float4 x[kOutBatch];
                 if (a.ef) {
-                    float* e = a.err + w * a.estride + base + j;
-                    *e = __fsub_rn(*e, h);
+#pragma unroll
+                    for (int b = 0; b < kOutBatch; ++b)
+                        if (b < nb) x[b] = __ldcs(reinterpret_cast<const float4*>(a.err + (w0 + b) * a.estride + e));
                 }
-                a.mg[w * a.stride + base + j] = h;
+                if (w0 == 0) compute_h();
+                const float4 hv = make_float4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+                for (int b = 0; b < kOutBatch; ++b) {
+                    if (b >= nb) continue;
+                    if (a.ef)
+                        __stcs(reinterpret_cast<float4*>(a.err + (w0 + b) * a.estride + e),
+                               make_float4(__fsub_rn(x[b].x, h[0]), __fsub_rn(x[b].y, h[1]), __fsub_rn(x[b].z, h[2]),
+                                           __fsub_rn(x[b].w, h[3])));
+                    __stcs(reinterpret_cast<float4*>(a.mg + (w0 + b) * a.stride + e), hv);
+                }
             }
+        } else {
+            compute_h();
+            for (int w = 0; w < a.W; ++w)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (a.ef) {
+                        float* ep = a.err + w * a.estride + e + c;
+                        *ep = __fsub_rn(*ep, h[c]);
+                    }
+                    a.mg[w * a.stride + e + c] = h[c];
+                }
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// G^ = P Q^T written to every replica, E <- M - G^ (the blocks loop over the
+// output tiles)
+// ---------------------------------------------------------------------------
+template <int RP>
+__global__ void __launch_bounds__(kThreads, 3) psgd_out_kernel(const PsgdArgs a)
+{
+    for (int i = blockIdx.x; i < a.n_otiles; i += gridDim.x) {
+        const int4 t = a.tiles[i];
+        if (t.w) out_quads<RP>(a, t);
+        else out_rows<RP>(a, t);
     }
 }
 
@@ -603,6 +654,23 @@ PsgdArgs make_args(const ddp_powersgd& h, uint8_t* scratch, float* main_grad, in
     return a;
 }
 
+// Blocks of the output launch: one wave (SMs x resident blocks of the kernel).
+template <int RP>
+size_t out_blocks()
+{
+    static int per_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    if (!per_sm[dev]) {
+        int sms = 0, v = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, psgd_out_kernel<RP>, kThreads, 0) != cudaSuccess || v < 1)
+            v = 1;
+        per_sm[dev] = std::max(1, sms) * v;
+    }
+    return static_cast<size_t>(per_sm[dev]);
+}
+
 template <int RP>
 ddp_status launch_all(const ddp_powersgd& h, const PsgdArgs& base, cudaStream_t s)
 {
@@ -617,7 +685,8 @@ ddp_status launch_all(const ddp_powersgd& h, const PsgdArgs& base, cudaStream_t 
         a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tq);
         psgd_qpart_kernel<RP><<<static_cast<unsigned>(h.t_q.size()), kThreads, 0, s>>>(a);
         a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_to);
-        psgd_out_kernel<RP><<<static_cast<unsigned>(h.t_o.size()), kThreads, 0, s>>>(a);
+        a.n_otiles = static_cast<int32_t>(h.t_o.size());
+        psgd_out_kernel<RP><<<static_cast<unsigned>(std::min<size_t>(h.t_o.size(), out_blocks<RP>())), kThreads, 0, s>>>(a);
     }
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "ddp_powersgd_reduce: kernel launch failed: %s", cudaGetErrorString(err));
@@ -705,8 +774,15 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
         for (int32_t r0 = 0; r0 < m.M; r0 += h->rows_p)
             h->t_p.push_back(make_int4(mi, r0, std::min(h->rows_p, m.M - r0), 0));
         m.ntp = static_cast<int32_t>(h->t_p.size()) - m.pt0;
-        for (int32_t r0 = 0; r0 < m.M; r0 += kRowsOut)
-            h->t_o.push_back(make_int4(mi, r0, std::min(kRowsOut, m.M - r0), 0));
+        const int64_t quads = rows * cols / 4;
+        if (m.vec && quads < (int64_t{1} << 31) - kOutQuads) {
+            for (int64_t q0 = 0; q0 < quads; q0 += kOutQuads)
+                h->t_o.push_back(make_int4(mi, static_cast<int32_t>(q0),
+                                           static_cast<int32_t>(std::min<int64_t>(kOutQuads, quads - q0)), 1));
+        } else {
+            for (int32_t r0 = 0; r0 < m.M; r0 += kRowsOut)
+                h->t_o.push_back(make_int4(mi, r0, std::min(kRowsOut, m.M - r0), 0));
+        }
         const int32_t ncb = (m.N + m.cbw - 1) / m.cbw, units = m.S * W;
         m.cnt0 = h->ncnt;
         h->ncnt += ncb;
