@@ -765,7 +765,7 @@ def run_powersgd(args):
             "compression_ratio": round(tot_elems / tot_comm, 1),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "bytes_per_step": tot_bytes,
-                         "kernel": "the hook's six launches per bucket, summed"},
+                         "kernel": "the hook's four launches per bucket (P, orthonormalisation, Q, output), summed"},
             "per_bucket": per_bucket, "steps": args.steps}
     print(json.dumps(line), flush=True)
     sess.close()
