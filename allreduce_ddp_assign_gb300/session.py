@@ -170,6 +170,9 @@ class HostBucketReducer:
     ready (the reducer gates the bucket's reduction on them), and bucket b's
     device-to-host copy waits for that bucket alone (ddp_reducer_wait_bucket)
     on a second copy stream, so the two directions and the reductions overlap.
+    Consecutive steps overlap too, bucket by bucket: step k + 1's copies into
+    bucket b's gradients wait only for step k's reduction of bucket b, and its
+    reduction of bucket b only for step k's copy of bucket b to the host.
 
     host_in   pinned [W, total] tensor (gradient dtype): replica w's gradients of
               all parameters back to back in parameter order.
@@ -207,8 +210,10 @@ class HostBucketReducer:
             self.issue.append((b, runs, np.asarray(ready, np.int32)))
         self.h2d = torch.cuda.Stream()
         self.d2h = torch.cuda.Stream()
-        self.reduced = None      # event: the previous step's reductions are done (dev_in may be overwritten)
-        self.downloaded = None   # event: the previous step's copies to the host are done (main_grad may be)
+        self.gate = torch.cuda.Stream()   # carries only waits and event records
+        # per bucket in issue order: the previous step's copy of it to the host is done
+        # (its main_grad may be overwritten); None before the first step
+        self.downloaded = None
         self.h2d_bytes = int(self.offs[-1]) * W * self.dev_in.element_size()
         self.reduce_scatter = int(mode) == 1
         if self.reduce_scatter:
@@ -226,25 +231,41 @@ class HostBucketReducer:
         r = self.reducer
         plan = r.plan
         stream = torch.cuda.current_stream() if stream is None else stream
-        # dev_in is overwritten once the previous step's reductions have read it; its
-        # device-to-host copies may still be running (they read main_grad only after
-        # this step's reduction of the same bucket, on the same copy stream)
-        if self.reduced is not None:
-            self.h2d.wait_event(self.reduced)
-            r.side.wait_event(self.downloaded)
-        else:
+        first = self.downloaded is None
+        if first:
             self.h2d.wait_stream(stream)
             r.side.wait_stream(stream)
+        else:
+            # a bucket with no parameter to mark (all of them unused everywhere) goes
+            # out at prepare: its main_grad must be on the host first
+            for i, (_, _, ready) in enumerate(self.issue):
+                if not len(ready):
+                    r.side.wait_event(self.downloaded[i])
+            # the previous step's completion of each bucket, taken before prepare starts
+            # this step (the gradients of bucket b are free once it is reduced)
+            reduced = []
+            for b, _, _ in self.issue:
+                ddp_reducer_wait_bucket(r.handle, b, self.gate)
+                ev = torch.cuda.Event()
+                ev.record(self.gate)
+                reduced.append(ev)
         self.d2h.wait_stream(stream)
         ddp_reducer_prepare(r.handle, 0)
         with torch.cuda.stream(self.h2d):
-            for b, runs, ready in self.issue:
+            for i, (b, runs, ready) in enumerate(self.issue):
+                if not first:
+                    self.h2d.wait_event(reduced[i])
                 for w in range(self.W):
                     for lo, hi in runs:
                         self.dev_in[w, lo:hi].copy_(host_in[w, lo:hi], non_blocking=True)
+                if not first:
+                    # and its main_grad once the previous step copied it to the host: the
+                    # side stream takes this wait just before the bucket's reduction
+                    r.side.wait_event(self.downloaded[i])
                 if len(ready):
                     ddp_reducer_mark_ready_many(r.handle, ready, self.h2d)
         stride = plan.replica_stride
+        downloaded = []
         with torch.cuda.stream(self.d2h):
             for b, _, _ in self.issue:
                 ddp_reducer_wait_bucket(r.handle, b, self.d2h)
@@ -254,11 +275,11 @@ class HostBucketReducer:
                     if self.reduce_scatter:   # shard w = bucket elements [w n / W, (w + 1) n / W)
                         a, z = a + w * (n // self.W), a + (w + 1) * (n // self.W)
                     host_out[a:z].copy_(r.main_grad[a:z], non_blocking=True)
-        self.downloaded = torch.cuda.Event()
-        self.downloaded.record(self.d2h)
+                ev = torch.cuda.Event()
+                ev.record(self.d2h)
+                downloaded.append(ev)
+        self.downloaded = downloaded
         ddp_reducer_finalize(r.handle, stream, 0)
-        self.reduced = torch.cuda.Event()
-        self.reduced.record(stream)
         stream.wait_stream(self.d2h)
 
     def close(self):

@@ -789,6 +789,41 @@ def test_host_front_end_pipeline_vs_oracle(orc, name):
     host.close()
 
 
+@pytest.mark.parametrize("name", ["c1", "c2"])
+def test_host_front_end_steps_back_to_back(orc, name):
+    """Three steps issued without a host synchronisation between them, each with its
+    own inputs and output buffer: step k + 1's uploads and reductions overlap step k's
+    downloads bucket by bucket, and every step's output must still be its own inputs'
+    reduction, bit for bit."""
+    from allreduce_ddp_assign_gb300.session import HostBucketReducer
+
+    wl = WL.ALL[name]()
+    host = HostBucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                             wl.first_cap_bytes, wl.pad_multiple, torch.float32)
+    plan = host.reducer.plan
+    total = int(host.offs[-1])
+    h_in, h_out = [], []
+    for m in range(3):
+        x = torch.empty((wl.W, total), dtype=torch.float32, pin_memory=True)
+        for w in range(wl.W):
+            x[w] = torch.from_numpy(np.concatenate([WL.grad_np(wl, p, w, m) for p in range(wl.nparams)]))
+        h_in.append(x)
+        h_out.append(torch.full((wl.W * host.replica_stride,), -1.0, dtype=torch.float32, pin_memory=True))
+    host.step(h_in[0], h_out[0])   # first step (and lazy module loading) outside the race
+    torch.cuda.synchronize()
+    for m in range(3):
+        host.step(h_in[m], h_out[m])
+    torch.cuda.synchronize()
+    for m in range(3):
+        raw = [[[WL.grad_raw_np(wl, p, w, m) for p in range(wl.nparams)] for w in range(wl.W)]]
+        ref = O.run_workload(wl, orc, grads=raw, copy_back=False)
+        out = h_out[m].numpy().reshape(wl.W, host.replica_stride)
+        for b in range(plan.nbuckets):
+            lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
+            assert_bits_equal(out[:, lo:lo + n], ref["bucket"][b], f"step {m} bucket {b}")
+    host.close()
+
+
 def test_host_front_end_reduce_scatter_shards(orc):
     """Reduce_scatter through the host front end: replica w's host copy receives
     exactly shard w of every bucket (bit for bit), and nothing outside it."""
