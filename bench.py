@@ -296,28 +296,45 @@ def run_ours(args, wl):
     launches = step_launches(wl, sess.plan)
     step_bytes = sum(x[2] for x in launches)
 
+    # A step that moves less than twice the L2 would find its inputs in L2 on the next
+    # step: such workloads rotate over R copies of their gradients and main_grad (R
+    # sessions sharing one side stream), R x the step's bytes above twice the L2, so
+    # every step reads from HBM.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = 1
+    if wl.micro_steps == 1 and step_bytes < 2 * l2:
+        R = min(64, -(-2 * l2 // step_bytes) + 1)
+    sessions = [sess]
+    for _ in range(R - 1):
+        copy = [[None if t is None else t.clone() for t in row] for row in micro[-1]]
+        sessions.append(BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                                      wl.first_cap_bytes, wl.pad_multiple, copy, used=used, fused=True,
+                                      timing=not coalesce, coalesce=coalesce, side_stream=sess.side))
+    l2_note = (f"inputs rotated over {R} copies ({R} x {step_bytes} B > 2 x L2 of {l2} B)" if R > 1
+               else "inputs larger than L2 (no flush)")
+
     pack_ev = []
 
-    def step(timed=False):
+    def step(k, timed=False):
+        s_ = sessions[k % R]
         if wl.micro_steps > 1:
             if timed:
                 ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 ev[0].record(compute)
             for m in range(wl.micro_steps - 1):   # no_sync micro-steps: local accumulation on the compute stream
-                sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
+                s_.accumulate_local(tabs[m], first=m == 0, stream=compute)
             if timed:
                 ev[1].record(compute)
                 pack_ev.append(ev)
-        sess.backward(compute, accumulate=wl.micro_steps > 1)
-        sess.finalize(compute)
+        s_.backward(compute, accumulate=wl.micro_steps > 1)
+        s_.finalize(compute)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    for k in range(max(args.warmup, 3) * R):
+        step(k)
     torch.cuda.synchronize()
 
     K = args.steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    side_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with ClockSampler(local) as clocks:
         if dist:
             dist.barrier()
@@ -325,44 +342,56 @@ def run_ours(args, wl):
         clocks.mark("t0")
         ev0.record(compute)
         for k in range(K):
-            side_ev[k][0].record(sess.side)
-            step(timed=True)
-            side_ev[k][1].record(sess.side)
+            step(k)
         ev1.record(compute)
         torch.cuda.synchronize()
         clocks.mark("t1")
         if dist:
             dist.barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
-    side_ms = sum(a.elapsed_time(b) for a, b in side_ev)
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     value = job_value(world, step_bytes, K, elapsed_ms)
 
-    # the same step with one launch per bucket (no coalescing): per-bucket figures
-    pb_sess = sess
-    if coalesce:
-        pb_sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
-                                wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True, timing=True,
-                                main_grad=True)
-    def pb_step():
-        for m in range(wl.micro_steps - 1):
-            pb_sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
-        pb_sess.backward(compute, accumulate=wl.micro_steps > 1)
-        pb_sess.finalize(compute)
-    for _ in range(3):
-        pb_step()
+    # the dominant kernel's time inside the step: the same K steps again with CUDA
+    # events around each step's launches on the side stream (kept out of the run
+    # above, whose per-step event records would add host time to small steps)
+    side_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        side_ev[k][0].record(sess.side)
+        step(k, timed=True)
+        side_ev[k][1].record(sess.side)
     torch.cuda.synchronize()
-    Kp = max(3, min(K, 50))
-    pa, pb_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pa.record(compute)
-    for _ in range(Kp):
-        pb_step()
-    pb_ev.record(compute)
-    torch.cuda.synchronize()
-    pb_value = job_value(1, step_bytes, Kp, pa.elapsed_time(pb_ev))
-    per_bucket_ms = [float(x) for x in pb_sess.bucket_ms()]
-    if pb_sess is not sess:
-        pb_sess.close()
+    side_ms = sum(a.elapsed_time(b) for a, b in side_ev)
+
+    # the same step with one launch per bucket (no coalescing): per-bucket figures.
+    # Workloads rotated over copies are single-bucket steps: there the coalesced
+    # figure is the per-bucket one and this part is skipped.
+    pb_value, per_bucket_ms, Kp = None, None, max(3, min(K, 50))
+    if R == 1:
+        pb_sess = sess
+        if coalesce:
+            pb_sess = BucketReducer(wl.numels, [wl.dtype] * wl.nparams, wl.W, wl.mode, wl.order, wl.cap_bytes,
+                                    wl.first_cap_bytes, wl.pad_multiple, micro[-1], used=used, fused=True,
+                                    timing=True, main_grad=True)
+
+        def pb_step():
+            for m in range(wl.micro_steps - 1):
+                pb_sess.accumulate_local(tabs[m], first=m == 0, stream=compute)
+            pb_sess.backward(compute, accumulate=wl.micro_steps > 1)
+            pb_sess.finalize(compute)
+        for _ in range(3):
+            pb_step()
+        torch.cuda.synchronize()
+        pa, pb_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        pa.record(compute)
+        for _ in range(Kp):
+            pb_step()
+        pb_ev.record(compute)
+        torch.cuda.synchronize()
+        pb_value = job_value(1, step_bytes, Kp, pa.elapsed_time(pb_ev))
+        per_bucket_ms = [float(x) for x in pb_sess.bucket_ms()]
+        if pb_sess is not sess:
+            pb_sess.close()
 
     # the dominant kernel: the fused pack+reduce launch(es) on the side stream (the
     # no_sync packs of an accumulating workload run on the compute stream)
@@ -402,8 +431,9 @@ def run_ours(args, wl):
             for r in range(Kp + 3):
                 if r == 3:
                     ka.record(sess.side)
-                D2.ddp_fused_bucket_group(descs, starts, sess.grads_tab, sess.used_tab, wl.nparams, wl.W, wl.mode, 0,
-                                          sess.main_grad, plan.replica_stride, None, None, sess.side)
+                s_ = sessions[r % R]
+                D2.ddp_fused_bucket_group(descs, starts, s_.grads_tab, s_.used_tab, wl.nparams, wl.W, wl.mode, 0,
+                                          s_.main_grad, plan.replica_stride, None, None, sess.side)
             kb.record(sess.side)
         torch.cuda.synchronize()
         kms = ka.elapsed_time(kb) / Kp
@@ -456,14 +486,15 @@ def run_ours(args, wl):
             "data": "synthetic (seeded splitmix64 gradients of the model's parameter shapes)",
             "config": {"workload": wl.name, "W": wl.W, "mode": "allreduce" if wl.mode == 0 else "reduce_scatter",
                        "buckets": sess.plan.nbuckets, "params": wl.nparams, "elements": sum(wl.numels),
-                       "bytes_per_step": step_bytes, "l2": "inputs larger than L2 (no flush)",
+                       "bytes_per_step": step_bytes, "l2": l2_note,
                        "parallelism": f"replicas x{world}", "pct_of_nominal_8TBs": round(100 * value / NOMINAL_HBM_GBS, 2),
                        "buckets_per_s": round(world * K * sess.plan.nbuckets / (elapsed_ms * 1e-3), 1),
                        "issue": "coalesced (ready buckets in one launch)" if coalesce else "one launch per bucket",
-                       "per_bucket_issue": {"value": round(pb_value, 1), "unit": "GB/s", "steps": Kp,
-                                            "per_bucket_gbs": [round(x[2] / (per_bucket_ms[x[1]] * 1e-3) / 1e9, 1)
-                                                               if per_bucket_ms[x[1]] > 0 else None for x in fused],
-                                            "bucket_bytes": [int(x[2]) for x in fused]}},
+                       "per_bucket_issue": None if pb_value is None else {
+                           "value": round(pb_value, 1), "unit": "GB/s", "steps": Kp,
+                           "per_bucket_gbs": [round(x[2] / (per_bucket_ms[x[1]] * 1e-3) / 1e9, 1)
+                                              if per_bucket_ms[x[1]] > 0 else None for x in fused],
+                           "bucket_bytes": [int(x[2]) for x in fused]}},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
                          "kernel": tag, "timing": timing_src, "kernel_only": kernel_only,
@@ -475,7 +506,8 @@ def run_ours(args, wl):
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
-    sess.close()
+    for s_ in sessions:
+        s_.close()
     if dist:
         dist.barrier()
         dist.destroy_process_group()
