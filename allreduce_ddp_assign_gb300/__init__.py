@@ -98,6 +98,7 @@ _SIGS = {
     "ddp_set_kernel_variant": (C.c_int32, [C.c_int32]),
     "ddp_device_status": (C.c_int32, [_vp, _i32p, C.c_int32]),
     "ddp_wait_selftest": (C.c_int32, [C.c_int32, C.c_int64, _vp]),
+    "ddp_copy_rows": (C.c_int32, [_vp, C.c_int64, _vp, C.c_int64, C.c_int64, C.c_int64, _vp]),
     "ddp_status_str": (C.c_char_p, [C.c_int32]),
     "ddp_last_error_message": (C.c_char_p, []),
     "ddp_version": (C.c_int32, []),
@@ -455,6 +456,12 @@ def ddp_device_status(stream=None, reset=False) -> int:
 
 def ddp_wait_selftest(arrive, limit_ns, stream=None) -> None:
     _check(lib().ddp_wait_selftest(int(arrive), int(limit_ns), _stream(stream)))
+
+
+def ddp_copy_rows(dst, dst_pitch, src, src_pitch, row_bytes, rows, stream=None) -> None:
+    """Pointers (tensors or integer addresses) and pitches in bytes."""
+    _check(lib().ddp_copy_rows(_ptr(dst), int(dst_pitch), _ptr(src), int(src_pitch), int(row_bytes), int(rows),
+                               _stream(stream)))
 
 
 def ddp_status_str(s: int) -> str:

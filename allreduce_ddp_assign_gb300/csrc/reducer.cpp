@@ -713,3 +713,25 @@ extern "C" void ddp_reducer_destroy(ddp_reducer* r)
     r->destroy_events();
     delete r;
 }
+
+extern "C" ddp_status ddp_copy_rows(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch,
+                                    int64_t row_bytes, int64_t rows, void* stream)
+{
+    const char* fn = "ddp_copy_rows";
+    if (row_bytes < 0 || rows < 0)
+        return ddp::fail(DDP_E_INVAL, "%s: negative size (row_bytes %lld, rows %lld)", fn,
+                         static_cast<long long>(row_bytes), static_cast<long long>(rows));
+    if (row_bytes == 0 || rows == 0) return ddp::ok();
+    if (!dst || !src) return ddp::fail(DDP_E_INVAL, "%s: NULL pointer", fn);
+    if (dst_pitch < row_bytes || src_pitch < row_bytes)
+        return ddp::fail(DDP_E_INVAL, "%s: pitch below the row (dst %lld, src %lld, row %lld bytes)", fn,
+                         static_cast<long long>(dst_pitch), static_cast<long long>(src_pitch),
+                         static_cast<long long>(row_bytes));
+    ddp_status st = DDP_OK;
+    if (!cuda_ok(cudaMemcpy2DAsync(dst, static_cast<size_t>(dst_pitch), src, static_cast<size_t>(src_pitch),
+                                   static_cast<size_t>(row_bytes), static_cast<size_t>(rows), cudaMemcpyDefault,
+                                   static_cast<cudaStream_t>(stream)),
+                 "cudaMemcpy2DAsync", &st))
+        return st;
+    return ddp::ok();
+}

@@ -10,7 +10,8 @@ from __future__ import annotations
 import numpy as np
 
 from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, DDP_R_WIRE_BF16,
-               DDP_R_WIRE_F16, DDP_R_BUCKET_DONE, Plan, ddp_pack, ddp_pack_group, ddp_reducer_wait_bucket,
+               DDP_R_WIRE_F16, DDP_R_BUCKET_DONE, Plan, ddp_copy_rows, ddp_pack, ddp_pack_group,
+               ddp_reducer_wait_bucket,
                ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
                ddp_reducer_find_unused, ddp_reducer_mark_ready_many, ddp_reducer_prepare,
@@ -231,6 +232,12 @@ class HostBucketReducer:
         r = self.reducer
         plan = r.plan
         stream = torch.cuda.current_stream() if stream is None else stream
+        es = self.dev_in.element_size()
+        if host_in.shape != self.dev_in.shape or host_in.dtype != self.dev_in.dtype or host_in.stride(1) != 1:
+            raise ValueError(f"host_in must be a [W, total] {self.dev_in.dtype} tensor with contiguous rows")
+        if host_out.dtype != torch.float32 or not host_out.is_contiguous() or \
+                host_out.numel() < self.W * self.reducer.plan.replica_stride:
+            raise ValueError("host_out must be a contiguous fp32 tensor of W * replica_stride elements")
         first = self.downloaded is None
         if first:
             self.h2d.wait_stream(stream)
@@ -255,9 +262,10 @@ class HostBucketReducer:
             for i, (b, runs, ready) in enumerate(self.issue):
                 if not first:
                     self.h2d.wait_event(reduced[i])
-                for w in range(self.W):
-                    for lo, hi in runs:
-                        self.dev_in[w, lo:hi].copy_(host_in[w, lo:hi], non_blocking=True)
+                for lo, hi in runs:   # the W replicas' slices of a run, one pitch apart: one copy
+                    ddp_copy_rows(self.dev_in.data_ptr() + lo * es, self.dev_in.stride(0) * es,
+                                  host_in.data_ptr() + lo * es, host_in.stride(0) * es, (hi - lo) * es, self.W,
+                                  self.h2d)
                 if not first:
                     # and its main_grad once the previous step copied it to the host: the
                     # side stream takes this wait just before the bucket's reduction
@@ -270,11 +278,13 @@ class HostBucketReducer:
             for b, _, _ in self.issue:
                 ddp_reducer_wait_bucket(r.handle, b, self.d2h)
                 lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
-                for w in range(self.W):
-                    a, z = w * stride + lo, w * stride + lo + n
-                    if self.reduce_scatter:   # shard w = bucket elements [w n / W, (w + 1) n / W)
-                        a, z = a + w * (n // self.W), a + (w + 1) * (n // self.W)
-                    host_out[a:z].copy_(r.main_grad[a:z], non_blocking=True)
+                if self.reduce_scatter:   # replica w's shard w: elements [w n / W, (w + 1) n / W) of the bucket
+                    k = n // self.W
+                    pitch, row = (stride + k) * 4, k * 4
+                else:
+                    pitch, row = stride * 4, n * 4
+                ddp_copy_rows(host_out.data_ptr() + lo * 4, pitch, r.main_grad.data_ptr() + lo * 4, pitch, row,
+                              self.W, self.d2h)
                 ev = torch.cuda.Event()
                 ev.record(self.d2h)
                 downloaded.append(ev)

@@ -775,6 +775,20 @@ ddp_status ddp_device_status(void* stream, int32_t* status, int32_t reset);
  */
 ddp_status ddp_wait_selftest(int32_t arrive, int64_t limit_ns, void* stream);
 
+/*
+ * ddp_copy_rows -- copy `rows` rows of `row_bytes` bytes each, row i from
+ * src + i * src_pitch to dst + i * dst_pitch, as one copy command on `stream`
+ * (cudaMemcpy2DAsync, direction inferred from the pointers; host memory must be
+ * pinned for the copy to be asynchronous).  A host-buffer front end moves a
+ * bucket's W replica slices, which are one pitch apart on both sides, with one
+ * call instead of W.  The pages have no counterpart: this is plumbing for callers
+ * whose gradients live in host memory.
+ * Errors: DDP_E_INVAL (negative sizes, a pitch below row_bytes, a NULL pointer
+ * with rows and row_bytes > 0); DDP_E_CUDA (the copy was refused).
+ */
+ddp_status ddp_copy_rows(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch, int64_t row_bytes,
+                         int64_t rows, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Errors and version                                                        */
 /* ------------------------------------------------------------------------ */

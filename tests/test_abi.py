@@ -106,3 +106,15 @@ def test_wait_selftest_validation():
         D.ddp_wait_selftest(0, 10, stream=0)
     with pytest.raises(D.DdpError, match="limit_ns"):
         D.ddp_wait_selftest(0, 3_000_000_000, stream=0)
+
+
+def test_copy_rows_validation():
+    """Refused on the host before any copy is issued; empty copies are no-ops."""
+    with pytest.raises(D.DdpError, match="negative size"):
+        D.ddp_copy_rows(0x1000, 64, 0x2000, 64, -1, 2, stream=0)
+    with pytest.raises(D.DdpError, match="NULL pointer"):
+        D.ddp_copy_rows(None, 64, 0x2000, 64, 64, 2, stream=0)
+    with pytest.raises(D.DdpError, match="pitch below the row"):
+        D.ddp_copy_rows(0x1000, 32, 0x2000, 64, 64, 2, stream=0)
+    D.ddp_copy_rows(None, 0, None, 0, 0, 5, stream=0)
+    D.ddp_copy_rows(None, 0, None, 0, 64, 0, stream=0)
