@@ -249,7 +249,10 @@ ddp_status launch_instance(const Ctx& cx, void* stream)
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, 0) != cudaSuccess || v < 1) v = 1;
         blocks_per_sm = v;
     }
-    const int64_t want = (cx.n + kMinElemsPerCta - 1) / kMinElemsPerCta;
+    // at least a CTA per ring chunk (down to 16-element slices): on a small bucket the
+    // pieces then run side by side instead of one after another in one CTA
+    int64_t want = (cx.n + kMinElemsPerCta - 1) / kMinElemsPerCta;
+    if (cx.nchunks > 1) want = std::max<int64_t>(want, std::min<int64_t>(cx.nchunks, (cx.n + 15) / 16));
     const int64_t room = static_cast<int64_t>(sm_count()) * blocks_per_sm;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min(want, room)));
     kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(cx);
