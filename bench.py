@@ -261,6 +261,16 @@ def profile_traffic(kernel_tag: str):
     return None
 
 
+def rotation_copies(step_bytes: int, l2_bytes: int, micro_steps: int = 1) -> int:
+    """Copies of a workload's inputs the timed steps rotate over so that each step
+    reads from HBM: 1 when a step moves at least twice the L2, else enough copies
+    that together they exceed twice the L2 (at most 64; no_sync workloads are large
+    and keep one)."""
+    if micro_steps != 1 or step_bytes >= 2 * l2_bytes or step_bytes <= 0:
+        return 1
+    return min(64, -(-2 * l2_bytes // step_bytes) + 1)
+
+
 def run_ours(args, wl):
     import torch
 
@@ -301,9 +311,7 @@ def run_ours(args, wl):
     # sessions sharing one side stream), R x the step's bytes above twice the L2, so
     # every step reads from HBM.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    R = 1
-    if wl.micro_steps == 1 and step_bytes < 2 * l2:
-        R = min(64, -(-2 * l2 // step_bytes) + 1)
+    R = rotation_copies(step_bytes, l2, wl.micro_steps)
     sessions = [sess]
     for _ in range(R - 1):
         copy = [[None if t is None else t.clone() for t in row] for row in micro[-1]]

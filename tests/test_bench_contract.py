@@ -40,3 +40,17 @@ def test_reference_arm_json_line():
 def test_reference_arm_other_ranks_print_nothing():
     lines = run_bench({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}, "--steps", "1", "--warmup", "3")
     assert lines == []
+
+
+def test_rotation_copies():
+    """Steps smaller than twice the L2 rotate over enough input copies to exceed it."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    l2 = 135_528_448                                    # GB300's L2 as the device reports it
+    assert bench.rotation_copies(1_635_650_048, l2) == 1          # ResNet-50 W=8: far above
+    assert bench.rotation_copies(2 * l2, l2) == 1
+    r = bench.rotation_copies(6_390_080, l2)                       # the MLP W=4 step
+    assert r == 44 and r * 6_390_080 > 2 * l2
+    assert bench.rotation_copies(1000, l2) == 64                   # capped
+    assert bench.rotation_copies(6_390_080, l2, micro_steps=4) == 1
