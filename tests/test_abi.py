@@ -118,3 +118,23 @@ def test_copy_rows_validation():
         D.ddp_copy_rows(0x1000, 32, 0x2000, 64, 64, 2, stream=0)
     D.ddp_copy_rows(None, 0, None, 0, 0, 5, stream=0)
     D.ddp_copy_rows(None, 0, None, 0, 64, 0, stream=0)
+
+
+def header_constants():
+    """Every NAME = value inside an enum of the header, comments removed."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    consts = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", text, flags=re.S):
+        for name, value in re.findall(r"(DDP_\w+)\s*=\s*(\d+)", body):
+            consts[name] = int(value)
+    return consts
+
+
+def test_binding_constants_match_the_header():
+    consts = header_constants()
+    assert len(consts) >= 25, consts
+    missing = [n for n in consts if not hasattr(D, n)]
+    assert not missing, missing
+    wrong = {n: (getattr(D, n), v) for n, v in consts.items() if getattr(D, n) != v}
+    assert not wrong, wrong
