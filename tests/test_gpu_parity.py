@@ -912,3 +912,52 @@ def test_host_front_end_bf16_megatron_reduce_scatter(orc):
             assert_bits_equal(out[w, lo + w * k:lo + (w + 1) * k], ref["bucket"][b][w, w * k:(w + 1) * k],
                               f"bucket {b} shard {w}")
     host.close()
+
+
+@pytest.mark.parametrize("coalesce", [False, True])
+def test_reducer_mixed_dtypes_vs_oracle(orc, coalesce):
+    """fp32, bf16 and fp16 gradients in one model: each dtype gets its own buckets and
+    cap sequence (reading U6), every bucket is fp32 main_grad.  The reducer's plan
+    equals the oracle's assignment and every bucket its ring result, bit for bit."""
+    from allreduce_ddp_assign_gb300.session import BucketReducer
+
+    numels = [3000, 64, 5000, 128, 7000, 257, 4097, 33, 6000, 90, 2500, 1]
+    dtypes = [[D.DDP_F32, D.DDP_BF16, D.DDP_F16][p % 3] for p in range(len(numels))]
+    W, cap, first = 4, 16 << 10, 8 << 10
+    rng = np.random.default_rng(33)
+    raw, dev = [], []
+    for w in range(W):
+        rr, dd = [], []
+        for n, dt in zip(numels, dtypes):
+            v = rng.standard_normal(n).astype(np.float32)
+            if dt == D.DDP_BF16:
+                bits = WL.f32_to_bf16_bits_np(v)
+                rr.append(bits)
+                dd.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV))
+            elif dt == D.DDP_F16:
+                h = v.astype(np.float16)
+                rr.append(h.view(np.uint16))
+                dd.append(torch.from_numpy(h).to(DEV))
+            else:
+                rr.append(v)
+                dd.append(torch.from_numpy(v).to(DEV))
+        raw.append(rr)
+        dev.append(dd)
+    sess = BucketReducer(numels, dtypes, W, D.DDP_ALLREDUCE, D.DDP_ORDER_REVERSE, cap, first, 1, dev,
+                         coalesce=coalesce)
+    sess.step()
+    torch.cuda.synchronize()
+    plan = orc.assign(numels, dtypes, cap, first, D.DDP_ORDER_REVERSE, 1, 1)
+    assert sess.plan.nbuckets == plan["nbuckets"] > 3
+    assert [int(x) for x in sess.plan.bucket_of] == [int(x) for x in plan["bucket_of"]]
+    assert [int(x) for x in sess.plan.offset_of] == [int(x) for x in plan["offset_of"]]
+    for b in range(plan["nbuckets"]):
+        mem = plan["members"][b]
+        assert len({dtypes[p] for p in mem}) == 1
+        offs = [int(plan["offset_of"][p]) for p in mem]
+        packed = orc.pack([[raw[w][p] for p in mem] for w in range(W)], offs, int(plan["bucket_numel"][b]),
+                          [dtypes[p] for p in mem])
+        want, _ = orc.ring(packed)
+        assert_bits_equal(sess.plan.bucket_view(sess.main_grad, b).cpu().numpy(), want, f"bucket {b}")
+    assert sess.issue_log() == [int(x) for x in plan["bucket_order"]]
+    sess.close()
