@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "common.h"
 
@@ -92,15 +93,16 @@ used_allreduce_kernel(const uint8_t* __restrict__ local, int64_t ld, int W, int6
 // Blocks that are resident at once: SMs x blocks per SM (a grid of one wave).
 int resident_blocks()
 {
-    static int n = 0;
+    static std::atomic<int> cached[ddp::kMaxDevices] = {};
+    const int dev = ddp::current_device();
+    int n = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
     if (!n) {
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int per_sm = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, used_allreduce_kernel, kThreads, 0) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
-        n = std::max(1, sms) * per_sm;
+        n = ddp::device_sm_count() * per_sm;
+        if (dev >= 0) cached[dev].store(n, std::memory_order_relaxed);
     }
     return n;
 }

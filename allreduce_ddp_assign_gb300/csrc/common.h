@@ -15,6 +15,16 @@ ddp_status ok();
 
 constexpr int32_t kMaxReplicas = 64;
 
+// Launch caches (occupancy, SM counts, function attributes, symbol addresses)
+// are kept per device index below this bound, in atomics, so that several host
+// threads and several devices in one process each see their own values.
+constexpr int kMaxDevices = 64;
+// The current device's index, or -1 when it cannot be read or is >= kMaxDevices
+// (such a device is served without caching).
+int current_device();
+// Multiprocessors of the current device (cached per device; 132 if unknown).
+int device_sm_count();
+
 // Device data-path launchers (kernels.cu); arguments are already validated.
 ddp_status launch_pack(const ddp_bucket_desc& b, const void* const* grads, const uint8_t* used, int32_t ld,
                        int32_t W, float* main_grad, int64_t stride, int32_t accumulate, void* stream);

@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <vector>
 
@@ -226,34 +227,25 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int sm_count()
-{
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
-    if (!cached[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = v > 0 ? v : 132;
-    }
-    return cached[dev];
-}
-
 template <int OP, int WT, int DT>
 ddp_status launch_instance(const Ctx& cx, void* stream)
 {
-    static int blocks_per_sm = 0;
+    // resident CTAs per SM of this instantiation, per device (0: not asked yet)
+    static std::atomic<int> occupancy[ddp::kMaxDevices] = {};
     auto kern = bucket_kernel<OP, WT, DT>;
+    const int dev = ddp::current_device();
+    int blocks_per_sm = dev >= 0 ? occupancy[dev].load(std::memory_order_relaxed) : 0;
     if (!blocks_per_sm) {
         int v = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreads, 0) != cudaSuccess || v < 1) v = 1;
         blocks_per_sm = v;
+        if (dev >= 0) occupancy[dev].store(v, std::memory_order_relaxed);
     }
     // at least a CTA per ring chunk (down to 16-element slices): on a small bucket the
     // pieces then run side by side instead of one after another in one CTA
     int64_t want = (cx.n + kMinElemsPerCta - 1) / kMinElemsPerCta;
     if (cx.nchunks > 1) want = std::max<int64_t>(want, std::min<int64_t>(cx.nchunks, (cx.n + 15) / 16));
-    const int64_t room = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+    const int64_t room = static_cast<int64_t>(ddp::device_sm_count()) * blocks_per_sm;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min(want, room)));
     kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(cx);
     const cudaError_t err = cudaGetLastError();
@@ -318,8 +310,8 @@ void set_mg(Ctx& cx, float* mg, int64_t stride)
     cx.mg_vec = mg && (reinterpret_cast<uintptr_t>(mg) % 16 == 0) && (stride % 4 == 0);
 }
 
-int g_variant = DDP_KERNEL_AUTO;
-int kernel_variant() { return g_variant; }
+std::atomic<int> g_variant{DDP_KERNEL_AUTO};
+int kernel_variant() { return g_variant.load(std::memory_order_relaxed); }
 
 // Under DDP_KERNEL_AUTO, a launch of one bucket with at most this many elements over
 // all replicas (numel x W) goes to the plain kernel: the streaming kernel's fixed
@@ -342,7 +334,7 @@ extern "C" ddp_status ddp_set_kernel_variant(int32_t variant)
 {
     if (variant != DDP_KERNEL_AUTO && variant != DDP_KERNEL_PLAIN && variant != DDP_KERNEL_STREAM)
         return ddp::fail(DDP_E_INVAL, "ddp_set_kernel_variant: unknown variant %d", variant);
-    ddpk::g_variant = variant;
+    ddpk::g_variant.store(variant, std::memory_order_relaxed);
     return ddp::ok();
 }
 

@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -658,17 +659,17 @@ PsgdArgs make_args(const ddp_powersgd& h, uint8_t* scratch, float* main_grad, in
 template <int RP>
 size_t out_blocks()
 {
-    static int per_sm[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (!per_sm[dev]) {
-        int sms = 0, v = 0;
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    static std::atomic<int> cached[ddp::kMaxDevices] = {};
+    const int dev = ddp::current_device();
+    int n = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
+    if (!n) {
+        int v = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, psgd_out_kernel<RP>, kThreads, 0) != cudaSuccess || v < 1)
             v = 1;
-        per_sm[dev] = std::max(1, sms) * v;
+        n = ddp::device_sm_count() * v;
+        if (dev >= 0) cached[dev].store(n, std::memory_order_relaxed);
     }
-    return static_cast<size_t>(per_sm[dev]);
+    return static_cast<size_t>(n);
 }
 
 template <int RP>
@@ -953,7 +954,10 @@ __device__ __align__(256) uint8_t g_psgd_static_scratch[kStaticScratchBytes];
 std::mutex g_static_mu;
 uint8_t* g_static_ptr[kMaxDevices] = {};
 
-// The array's address on the current device, looked up once per device.
+// The array's address on the current device, looked up once per device and
+// kept for the life of the process.  cudaDeviceReset on a device unloads the
+// library's module there, so the kept address is then stale: this entry point
+// must not be called again on that device in the same process.
 ddp_status static_scratch(uint8_t** out)
 {
     int dev = 0;
@@ -985,15 +989,15 @@ extern "C" ddp_status ddp_powersgd_reduce_static(ddp_powersgd* h, float* main_gr
     if (h->W > 1 && replica_stride < h->bucket_numel)
         return fail(DDP_E_INVAL, "%s: replica_stride %lld < bucket numel %lld", fn, static_cast<long long>(replica_stride),
                     static_cast<long long>(h->bucket_numel));
-    if (static_cast<int64_t>(h->scratch_bytes) > kStaticScratchBytes)
-        return fail(DDP_E_CAPACITY, "%s: this bucket needs %lld bytes of scratch, the static array holds %lld "
-                    "(use ddp_powersgd_reduce with a workspace)", fn, static_cast<long long>(h->scratch_bytes),
-                    static_cast<long long>(kStaticScratchBytes));
-    if (h->iter < h->start_iter) {
+    if (h->iter < h->start_iter) {  // warm-up: the plain all-reduce, which uses no scratch
         const ddp_status st = ddp::launch_allreduce(main_grad, replica_stride, h->bucket_numel, h->W, DDP_ALLREDUCE, stream);
         if (st == DDP_OK) ++h->iter;
         return st;
     }
+    if (static_cast<int64_t>(h->scratch_bytes) > kStaticScratchBytes)
+        return fail(DDP_E_CAPACITY, "%s: this bucket needs %lld bytes of scratch, the static array holds %lld "
+                    "(use ddp_powersgd_reduce with a workspace)", fn, static_cast<long long>(h->scratch_bytes),
+                    static_cast<long long>(kStaticScratchBytes));
     if (!h->ws) return fail(DDP_E_STATE, "%s: call ddp_powersgd_bind first", fn);
     uint8_t* scratch = nullptr;
     const ddp_status sst = static_scratch(&scratch);

@@ -1,4 +1,7 @@
 // Status strings and the per-thread last-error message.
+#include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -23,6 +26,28 @@ ddp_status ok()
 {
     g_message[0] = '\0';
     return DDP_OK;
+}
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+int device_sm_count()
+{
+    static std::atomic<int> cached[kMaxDevices] = {};
+    const int dev = current_device();
+    int v = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
+    if (!v) {
+        int d = 0;
+        if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+            v <= 0)
+            v = 132;
+        if (dev >= 0) cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 }  // namespace ddp

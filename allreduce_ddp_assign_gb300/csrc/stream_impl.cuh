@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "common.h"
@@ -650,19 +651,6 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
 constexpr uint32_t kSmemBudget2 = DDP_STREAM_BUDGET2_KB * 1024;  // two CTAs per SM
 constexpr uint32_t kSmemBudget1 = 220 * 1024;                    // one CTA per SM
 
-inline int sm_count_tma()
-{
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 132;
-    if (!cached[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = v > 0 ? v : 132;
-    }
-    return cached[dev];
-}
-
 // stages that fit the budget (0 if fewer than two)
 inline int stages_for(int W, int tile, int gb, bool acc, bool sbulk, uint32_t budget)
 {
@@ -699,24 +687,35 @@ ddp_status launch_instance(StreamArgs& a, void* stream)
     if (!plan_for(a.W, tile, gb, ACC, a.store_bulk, &p))
         return ddp::fail(DDP_E_INVAL, "stream kernel: no stage layout fits for W = %d", a.W);
     a.ns = p.ns;
-    static uint32_t configured = 0;
-    if (configured < p.budget) {
+    // Per device: the dynamic shared memory this instantiation may use (a function
+    // attribute, set once per device and raised when a launch needs more), and the
+    // resident CTAs per SM at the last shared-memory size asked for, packed as
+    // (bytes << 32 | CTAs) so that the pair is read and written as one value.
+    static std::atomic<uint32_t> configured[ddp::kMaxDevices] = {};
+    static std::atomic<uint64_t> occupancy[ddp::kMaxDevices] = {};
+    const int dev = ddp::current_device();
+    if (dev < 0 || configured[dev].load(std::memory_order_acquire) < p.budget) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.budget);
         if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        configured = p.budget;
+        if (dev >= 0) {
+            uint32_t cur = configured[dev].load(std::memory_order_relaxed);
+            while (cur < p.budget && !configured[dev].compare_exchange_weak(cur, p.budget, std::memory_order_release)) {
+            }
+        }
     }
-    static uint32_t occ_bytes = 0;
-    static int occ = 0;
-    if (occ_bytes != p.bytes) {
+    const uint64_t packed = dev >= 0 ? occupancy[dev].load(std::memory_order_relaxed) : 0;
+    int occ = static_cast<int>(packed & 0xffffffffu);
+    if (packed == 0 || (packed >> 32) != p.bytes) {
         int v = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kThreadsTma, p.bytes) != cudaSuccess || v < 1) v = 1;
         occ = v;
-        occ_bytes = p.bytes;
+        if (dev >= 0) occupancy[dev].store((static_cast<uint64_t>(p.bytes) << 32) | static_cast<uint32_t>(v),
+                                           std::memory_order_relaxed);
     }
     // small launches: spread down to 16-element slices so that the pieces (one per ring
     // chunk, at least) run in parallel CTAs rather than through one CTA's pipeline
     const int64_t want = (a.total + 15) / 16;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(sm_count_tma()) * occ)));
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(ddp::device_sm_count()) * occ)));
     kern<<<grid, kThreadsTma, p.bytes, static_cast<cudaStream_t>(stream)>>>(a);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "stream kernel launch failed: %s", cudaGetErrorString(err));

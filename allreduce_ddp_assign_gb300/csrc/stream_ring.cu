@@ -11,17 +11,19 @@ namespace {
 // bit 0: a streaming kernel gave up on an mbarrier wait
 __device__ int g_device_status = 0;
 
+// The status word's address on the current device, looked up once per device.
 int* status_word()
 {
-    static int* cached[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cached[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-        cached[dev] = static_cast<int*>(p);
+    static std::atomic<int*> cached[ddp::kMaxDevices] = {};
+    const int dev = ddp::current_device();
+    int* p = dev >= 0 ? cached[dev].load(std::memory_order_acquire) : nullptr;
+    if (!p) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_status) != cudaSuccess) return nullptr;
+        p = static_cast<int*>(a);
+        if (dev >= 0) cached[dev].store(p, std::memory_order_release);
     }
-    return cached[dev];
+    return p;
 }
 }  // namespace
 

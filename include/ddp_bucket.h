@@ -469,16 +469,19 @@ ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replic
  * all.  The workspace bound by ddp_powersgd_bind still supplies the tile
  * tables; its scratch part is not used.
  *
- * Set-up: the first call on each device, with that device current, looks up
- * the array's address (cudaGetSymbolAddress) and keeps it; make that first
- * call before any stream capture.  Nothing of the scratch is read before the
+ * Set-up: the first compressing call on each device, with that device
+ * current, looks up the array's address (cudaGetSymbolAddress) and keeps it
+ * for the life of the process; make that first call before any stream
+ * capture.  cudaDeviceReset on a device makes the kept address stale: do not
+ * call this entry point on that device again in the same process.  Nothing of the scratch is read before the
  * same call writes it (the first kernel zeroes the counters), so nothing needs
  * clearing beforehand.  Calls that overlap in time
  * (any state objects, any streams, on one device) share the array and race:
  * serialise them.  Results are identical to ddp_powersgd_reduce's.
- * Errors: as ddp_powersgd_reduce; DDP_E_CAPACITY when the bucket's scratch
- * (ddp_powersgd_sizes minus the tables) exceeds the array; DDP_E_CUDA if the
- * address lookup fails.
+ * Errors: as ddp_powersgd_reduce; DDP_E_CAPACITY when a compressing call's
+ * scratch (ddp_powersgd_sizes minus the tables) exceeds the array (the plain
+ * warm-up iterations use no scratch and are never refused for size), checked
+ * before anything is launched; DDP_E_CUDA if the address lookup fails.
  */
 #define DDP_POWERSGD_STATIC_SCRATCH_BYTES (8ll << 20)
 ddp_status ddp_powersgd_reduce_static(ddp_powersgd* h, float* main_grad, int64_t replica_stride, void* stream);

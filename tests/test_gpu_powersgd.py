@@ -1,12 +1,25 @@
 """The PowerSGD hook on the GPU against the oracle (``oracle/powersgd.py``).
 
 1-D tensors and the plain warm-up iterations are compared bit for bit (the ring's
-arithmetic).  Compressed tensors are compared within a tolerance derived from
-the arithmetic: the GPU accumulates the products P = M Q (length N) and
-Q = M^T P (length M) in fp32 and orthonormalises P; a first-order bound on the
-normwise error of the output relative to the fp64 evaluation is
-(M + N + R) u kappa(P) with u = 2^-24 and kappa(P) the condition number of the
-summed P (from the oracle); the test allows 8 times that per iteration run.
+arithmetic).  Compressed tensors are compared with the fp64 oracle in the max
+norm relative to max |output| (Q: max |Q|; error buffer: the larger of max
+|output| and max |error|), within
+
+    TOL_OUT_Q * k * u * kappa(P)   for the output and Q,
+    TOL_ERR   * k * u * kappa(P)   for the error-feedback buffer,
+
+u = 2^-24, k = compressed iterations so far (each one's error reaches the next
+through the warm-started Q and the error buffer), kappa(P) = the condition
+number of the summed P, from the oracle (the orthonormalisation amplifies the
+fp32 error of P by about that much).  The kernels accumulate P = M Q and
+Q = M^T P in fp32 per lane and combine the lanes' partial sums in a fixed tree,
+so the error stays at a few units in the last place of the output instead of
+growing with the product length: measured over every case below and the
+ResNet-50 buckets (shapes 1 x 16 to 2048 x 4608, kappa up to 1.2e3), the worst
+output error is 5.0 k u kappa, the worst Q error 3.7 and the worst error-buffer
+error 2.4.  The constants are those maxima rounded up to a power of two with at
+least a factor 3 to spare, so a slip of a few ulps more than the arithmetic
+makes fails the test.
 """
 import numpy as np
 import pytest
@@ -24,6 +37,8 @@ if not torch.cuda.is_available():  # pragma: no cover
 
 DEV = torch.device("cuda:0")
 U = 2.0 ** -24
+TOL_OUT_Q = 16.0   # output and Q: k * u * kappa(P) units (worst measured 5.0 and 3.7)
+TOL_ERR = 8.0      # error-feedback buffer (worst measured 2.4)
 
 SHAPES = [(64, 3, 7, 7), (8,), (256, 64), (3, 5), (1, 16), (10,), (40, 36), (2048,), (130, 2, 3)]
 
@@ -56,7 +71,7 @@ def q0_of(rng_seed, shapes, rank):
 
 
 def check_against(state, want, got, shapes, offs, it, what):
-    """Vectors bit for bit, matrices within the derived tolerance."""
+    """Vectors bit for bit, matrices within TOL_OUT_Q k u kappa(P) of max |output|."""
     W = want.shape[0]
     for t, s in enumerate(shapes):
         lo, k = offs[t], int(np.prod(s))
@@ -64,8 +79,7 @@ def check_against(state, want, got, shapes, offs, it, what):
         if mv is None:
             assert_bits_equal(got[:, lo:lo + k], want[:, lo:lo + k].astype(np.float32), f"{what}: 1-D tensor {t}")
             continue
-        m, n = mv
-        tol = 8 * it * (m + n + state.rank) * U * max(state.cond.get(t, 1.0), 1.0)
+        tol = TOL_OUT_Q * it * U * max(state.cond.get(t, 1.0), 1.0)
         ref = want[:, lo:lo + k]
         scale = max(np.abs(ref).max(), 1e-30)
         err = np.abs(got[:, lo:lo + k].astype(np.float64) - ref).max() / scale
@@ -111,14 +125,14 @@ def test_powersgd_bucket_vs_oracle(orc, W, rank, ef, aligned):
             if mv is None:
                 continue
             qg = hook.q(t).cpu().numpy().astype(np.float64)
-            tol = 8 * (it - start_iter) * (mv[0] + mv[1] + rank) * U * max(st.cond[t], 1.0)
-            assert np.abs(qg - st.q[t]).max() <= tol * max(np.abs(st.q[t]).max(), 1e-30), f"Q of tensor {t}"
+            unit = (it - start_iter) * U * max(st.cond[t], 1.0)
+            assert np.abs(qg - st.q[t]).max() <= TOL_OUT_Q * unit * max(np.abs(st.q[t]).max(), 1e-30), f"Q of tensor {t}"
             if ef:
                 for w in range(W):
                     eg = hook.error_of(w, offs[t], mv[0] * mv[1]).cpu().numpy().astype(np.float64)
                     er = st.error[w][t].reshape(-1)
                     scale = max(np.abs(want[w, offs[t]:offs[t] + mv[0] * mv[1]]).max(), np.abs(er).max(), 1e-30)
-                    assert np.abs(eg - er).max() <= tol * scale, f"error of tensor {t} replica {w}"
+                    assert np.abs(eg - er).max() <= TOL_ERR * unit * scale, f"error of tensor {t} replica {w}"
     assert hook.iteration == 3
     hook.close()
 

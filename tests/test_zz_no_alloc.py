@@ -52,9 +52,13 @@ def test_static_scratch_matches_workspace_two_calls_in_a_row():
 
 def test_static_scratch_rejects_oversized_bucket():
     """A 65536 x 4096 matrix needs far more than the 8 MiB array: refused on the host
-    before anything is launched."""
-    h = D.ddp_powersgd_create(8, 4, [0], [65536 * 4096], [65536], 65536 * 4096)
+    before anything is launched.  main_grad is a placeholder address that nothing may
+    touch, so the state is made to compress from its first call (start_iter = 0: no
+    plain warm-up all-reduce would run on it) and is never bound (the compressed path
+    has no tables to launch with); the size check comes first all the same."""
+    h = D.ddp_powersgd_create(8, 4, [0], [65536 * 4096], [65536], 65536 * 4096, error_feedback=1, start_iter=0)
     with pytest.raises(D.DdpError, match="static array holds 8388608") as e:
         D.ddp_powersgd_reduce_static(h, 0x1000, 65536 * 4096, stream=0)
     assert e.value.status == D.DDP_E_CAPACITY
+    assert D.ddp_powersgd_iter(h) == 0
     D.ddp_powersgd_destroy(h)
