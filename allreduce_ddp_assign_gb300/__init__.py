@@ -99,6 +99,15 @@ _SIGS = {
     "ddp_device_status": (C.c_int32, [_vp, _i32p, C.c_int32]),
     "ddp_wait_selftest": (C.c_int32, [C.c_int32, C.c_int64, _vp]),
     "ddp_copy_rows": (C.c_int32, [_vp, C.c_int64, _vp, C.c_int64, C.c_int64, C.c_int64, _vp]),
+    "ddp_plan_create": (C.c_int32, [_i64p, _i32p, C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int32,
+                                    C.c_int64, C.POINTER(_vp)]),
+    "ddp_plan_describe": (C.c_int32, [_vp, _vp, _i64p, _i64p, _i32p, _i32p, _i64p, _i32p, _i32p, _i32p, _i64p]),
+    "ddp_plan_tables": (C.c_int32, [_vp, _i64p, _i32p]),
+    "ddp_plan_bucket_descs": (C.c_int32, [_vp, _vp, _vp, C.POINTER(BucketDesc)]),
+    "ddp_plan_rebuilt": (C.c_int32, [_vp, _i32p, _i64p, _i64p, C.c_int32, _i32p]),
+    "ddp_reducer_create_from_plan": (C.c_int32, [_vp, C.POINTER(BucketDesc), C.c_int32, C.c_int32, C.c_int32, _vp, _vp,
+                                                 C.c_int32, _vp, _vp, _vp, _vp, C.POINTER(_vp)]),
+    "ddp_plan_destroy": (None, [_vp]),
     "ddp_status_str": (C.c_char_p, [C.c_int32]),
     "ddp_last_error_message": (C.c_char_p, []),
     "ddp_version": (C.c_int32, []),
@@ -198,6 +207,74 @@ def ddp_assign_buckets(numels, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=
     out["members"] = out["members"][:P].copy()
     out["nbuckets"] = B
     return out
+
+
+class PlanInfo(C.Structure):
+    """ddp_plan_info."""
+    _fields_ = [("nparams", C.c_int32), ("nbuckets", C.c_int32), ("order", C.c_int32), ("pad_multiple", C.c_int32),
+                ("grad_reduce_in_fp32", C.c_int32), ("reserved_", C.c_int32), ("cap_bytes", C.c_int64),
+                ("first_cap_bytes", C.c_int64), ("align_elems", C.c_int64), ("replica_stride", C.c_int64),
+                ("seg_offset_len", C.c_int64), ("seg_param_len", C.c_int64)]
+
+
+def ddp_plan_create(numels, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=1 << 20, order=DDP_ORDER_REVERSE,
+                    pad_multiple=1, grad_reduce_in_fp32=1, align_elems=64) -> int:
+    numels = _a(numels, np.int64)
+    dt = None if dtypes is None else _a(dtypes, np.int32)
+    h = _vp()
+    _check(lib().ddp_plan_create(_cp(numels, _i64p), None if dt is None else _cp(dt, _i32p), len(numels),
+                                 int(cap_bytes), int(first_cap_bytes), int(order), int(pad_multiple),
+                                 int(grad_reduce_in_fp32), int(align_elems), C.byref(h)))
+    return h.value
+
+
+def ddp_plan_describe(h) -> dict:
+    """Every table of the plan as numpy arrays, plus the ddp_plan_info fields."""
+    info = PlanInfo()
+    _check(lib().ddp_plan_describe(h, C.byref(info), None, None, None, None, None, None, None, None, None))
+    B, P = info.nbuckets, info.nparams
+    out = {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved_"}
+    arrs = dict(bucket_numel=np.zeros(max(B, 1), np.int64), bucket_bytes=np.zeros(max(B, 1), np.int64),
+                bucket_dtype=np.zeros(max(B, 1), np.int32), bucket_order=np.zeros(max(B, 1), np.int32),
+                bucket_start=np.zeros(max(B, 1), np.int64), member_start=np.zeros(B + 1, np.int32),
+                members=np.zeros(max(P, 1), np.int32), bucket_of=np.zeros(max(P, 1), np.int32),
+                offset_of=np.zeros(max(P, 1), np.int64))
+    _check(lib().ddp_plan_describe(h, None, *(_cp(arrs[k], _i64p if arrs[k].dtype == np.int64 else _i32p) for k in
+                                             ("bucket_numel", "bucket_bytes", "bucket_dtype", "bucket_order",
+                                              "bucket_start", "member_start", "members", "bucket_of", "offset_of"))))
+    for k in ("bucket_numel", "bucket_bytes", "bucket_dtype", "bucket_order", "bucket_start"):
+        arrs[k] = arrs[k][:B].copy()
+    for k in ("members", "bucket_of", "offset_of"):
+        arrs[k] = arrs[k][:P].copy()
+    out.update(arrs)
+    return out
+
+
+def ddp_plan_tables(h, seg_offset_len: int, seg_param_len: int):
+    so = np.zeros(max(seg_offset_len, 1), np.int64)
+    sp = np.zeros(max(seg_param_len, 1), np.int32)
+    _check(lib().ddp_plan_tables(h, _cp(so, _i64p), _cp(sp, _i32p)))
+    return so[:seg_offset_len].copy(), sp[:seg_param_len].copy()
+
+
+def ddp_plan_bucket_descs(h, nbuckets: int, seg_offset_dev, seg_param_dev) -> list:
+    arr = (BucketDesc * max(nbuckets, 1))()
+    _check(lib().ddp_plan_bucket_descs(h, _ptr(seg_offset_dev), _ptr(seg_param_dev), arr))
+    return [arr[b] for b in range(nbuckets)]
+
+
+def ddp_plan_rebuilt(h, sequence, nparams: int) -> dict:
+    seq = _a(sequence, np.int32)
+    cap = nparams + 2
+    by, nm = np.zeros(cap, np.int64), np.zeros(cap, np.int64)
+    nb = C.c_int32(0)
+    _check(lib().ddp_plan_rebuilt(h, _cp(seq, _i32p), _cp(by, _i64p), _cp(nm, _i64p), cap, C.byref(nb)))
+    return dict(nbuckets=nb.value, bucket_bytes=by[:nb.value].copy(), bucket_numel=nm[:nb.value].copy())
+
+
+def ddp_plan_destroy(h):
+    if h:
+        lib().ddp_plan_destroy(h)
 
 
 def ddp_assign_buckets_ordered(numels, sequence, dtypes=None, cap_bytes=25 << 20, first_cap_bytes=1 << 20,
@@ -319,6 +396,17 @@ def ddp_reducer_create(nparams, bucket_of, bucket_order, descs, bucket_start, W,
                                     _cp(bucket_start, _i64p), int(W), int(mode), int(flags), _ptr(grads), _ptr(used),
                                     int(ld), _ptr(main_grad), int(replica_stride), _ptr(grads_out), _ptr(global_used),
                                     side, C.byref(h)))
+    return h.value
+
+
+def ddp_reducer_create_from_plan(plan, descs, W, mode, flags, grads=None, used=None, ld=0, main_grad=None,
+                                 grads_out=None, global_used=None, side_stream=None):
+    arr = (BucketDesc * max(len(descs), 1))(*descs)
+    h = _vp()
+    side = None if flags & DDP_R_DRY_RUN else _stream(side_stream)
+    _check(lib().ddp_reducer_create_from_plan(plan, arr, int(W), int(mode), int(flags), _ptr(grads), _ptr(used),
+                                              int(ld), _ptr(main_grad), _ptr(grads_out), _ptr(global_used), side,
+                                              C.byref(h)))
     return h.value
 
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUTDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUTDIR, "libddpbucket.so")
 SOURCES = ["kernels.cu", "stream_ring.cu", "stream_fused.cu", "stream_fused_wire.cu", "stream_pack.cu", "bitmap.cu",
-           "powersgd.cu", "reducer.cpp", "assign.cpp", "timeline.cpp", "status.cpp"]
+           "powersgd.cu", "reducer.cpp", "assign.cpp", "plan.cpp", "timeline.cpp", "status.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

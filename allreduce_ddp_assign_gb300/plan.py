@@ -1,22 +1,20 @@
-"""Plumbing around ddp_assign_buckets: the caller-owned tables the kernels read.
+"""Plumbing around the library's plan object (ddp_plan_create): the caller-owned
+tables the kernels read.
 
-A Plan runs the library's bucket assignment once, lays the buckets out in one
-fp32 main_grad buffer per replica (each bucket starting on a 64-element,
-256-byte boundary so every replica's copy is vector-aligned), and uploads the
-per-bucket segment tables (ddp_bucket_desc.seg_offset / seg_param) to the
-device.  Nothing here computes any part of the path.
+A Plan asks the library for the bucket assignment and its layout (each bucket
+starting on a 64-element, 256-byte boundary of the per-replica fp32 main_grad
+buffer, so every replica's copy is vector-aligned), copies the plan's segment
+tables to the device and gets the bucket descriptors over those copies.
+Nothing here computes any part of the path.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import BucketDesc, ddp_assign_buckets, ddp_assign_buckets_ordered
+from . import (ddp_plan_bucket_descs, ddp_plan_create, ddp_plan_describe, ddp_plan_destroy, ddp_plan_rebuilt,
+               ddp_plan_tables)
 
 ALIGN_ELEMS = 64
-
-
-def _round_up(x: int, m: int) -> int:
-    return (x + m - 1) // m * m
 
 
 class Plan:
@@ -27,9 +25,9 @@ class Plan:
         self.numels = [int(v) for v in numels]
         P = self.nparams = len(self.numels)
         self.dtypes = [0] * P if dtypes is None else [int(v) for v in dtypes]
-        a = ddp_assign_buckets(self.numels, self.dtypes, cap_bytes, first_cap_bytes, order, pad_multiple,
-                               grad_reduce_in_fp32)
-        self.assignment = a
+        self.handle = ddp_plan_create(self.numels, self.dtypes, cap_bytes, first_cap_bytes, order, pad_multiple,
+                                      grad_reduce_in_fp32, ALIGN_ELEMS)
+        a = self.assignment = ddp_plan_describe(self.handle)
         self.caps = dict(cap_bytes=int(cap_bytes), first_cap_bytes=int(first_cap_bytes), order=int(order),
                          pad_multiple=int(pad_multiple), grad_reduce_in_fp32=int(grad_reduce_in_fp32))
         self.nbuckets = B = a["nbuckets"]
@@ -39,34 +37,17 @@ class Plan:
         self.bucket_bytes = a["bucket_bytes"]
         self.bucket_dtype = a["bucket_dtype"]
         self.bucket_order = a["bucket_order"]
-        self.members = [[] for _ in range(B)]
-        for p in a["members"]:
-            self.members[self.bucket_of[p]].append(int(p))
-        starts, pos = [], 0
-        for b in range(B):
-            starts.append(pos)
-            pos = _round_up(pos + int(self.bucket_numel[b]), ALIGN_ELEMS)
-        self.bucket_start = np.array(starts, dtype=np.int64)
-        self.replica_stride = max(pos, ALIGN_ELEMS)
+        self.bucket_start = a["bucket_start"]
+        self.replica_stride = int(a["replica_stride"])
+        ms = a["member_start"]
+        self.members = [[int(p) for p in a["members"][ms[b]:ms[b + 1]]] for b in range(B)]
         self.device = torch.device(device)
 
-        # segment tables, all buckets in one tensor each
-        seg_off, seg_par, self._seg_base = [], [], []
-        for b in range(B):
-            self._seg_base.append((len(seg_off), len(seg_par)))
-            for p in self.members[b]:
-                seg_off.append(int(self.offset_of[p]))
-                seg_par.append(p)
-            end = int(self.offset_of[self.members[b][-1]]) + self.numels[self.members[b][-1]] if self.members[b] else 0
-            seg_off.append(end)
-        self.seg_offset_dev = torch.tensor(seg_off or [0], dtype=torch.int64, device=self.device)
-        self.seg_param_dev = torch.tensor(seg_par or [0], dtype=torch.int32, device=self.device)
-        self.descs = []
-        for b in range(B):
-            o, q = self._seg_base[b]
-            self.descs.append(BucketDesc(int(self.bucket_numel[b]), len(self.members[b]), int(self.bucket_dtype[b]),
-                                         self.seg_offset_dev.data_ptr() + 8 * o,
-                                         self.seg_param_dev.data_ptr() + 4 * q))
+        # the kernels' segment tables, all buckets in one device tensor each
+        so, sp = ddp_plan_tables(self.handle, a["seg_offset_len"], a["seg_param_len"])
+        self.seg_offset_dev = torch.from_numpy(so if len(so) else np.zeros(1, np.int64)).to(self.device)
+        self.seg_param_dev = torch.from_numpy(sp if len(sp) else np.zeros(1, np.int32)).to(self.device)
+        self.descs = ddp_plan_bucket_descs(self.handle, B, self.seg_offset_dev, self.seg_param_dev)
 
     # -- description ----------------------------------------------------------
     def describe(self) -> dict:
@@ -82,11 +63,20 @@ class Plan:
 
     def rebuilt(self, sequence) -> dict:
         """The buckets a rebuild would form over the observed gradient-ready
-        sequence (ddp_assign_buckets_ordered), as plain lists."""
-        a = ddp_assign_buckets_ordered(self.numels, sequence, self.dtypes, self.caps["cap_bytes"],
-                                       self.caps["first_cap_bytes"], self.caps["pad_multiple"],
-                                       self.caps["grad_reduce_in_fp32"])
+        sequence (ddp_plan_rebuilt), as plain lists."""
+        a = ddp_plan_rebuilt(self.handle, sequence, self.nparams)
         return dict(num_buckets=int(a["nbuckets"]), bucket_sizes=[int(v) for v in a["bucket_bytes"]])
+
+    def close(self):
+        if getattr(self, "handle", None):
+            ddp_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
     # -- buffers and tables -------------------------------------------------
     def alloc_main_grad(self, W: int, fill: float = 0.0):

@@ -39,6 +39,13 @@
  *   - Alignment: no alignment is required.  16-byte-aligned buffers whose
  *     offsets keep that alignment take the vector path; the rest is done with
  *     scalar accesses on the GPU (there is no CPU fallback).
+ *   - Threads and devices: every entry point may be called from several host
+ *     threads at once and for several devices in one process (the launch
+ *     caches -- occupancy, function attributes, symbol addresses -- are kept
+ *     per device, in atomics), with these exceptions: a reducer, a plan
+ *     under construction and a PowerSGD state are used by one thread at a
+ *     time, and ddp_set_kernel_variant is process-wide.  Kernels launch on the
+ *     device that is current in the calling thread; pointers must belong to it.
  */
 #ifndef DDP_BUCKET_H
 #define DDP_BUCKET_H
@@ -678,6 +685,14 @@ ddp_status ddp_reducer_register_powersgd(ddp_reducer* r, int32_t bucket, ddp_pow
  * ddp_reducer_mark_ready -- the autograd hook of parameter `param` fired: its
  * gradient has been (or is being) produced on `producer_stream`
  * (mark_variable_ready, DDP chapter 17.12; lecture 2.3).
+ * The producer is given as a stream, not as an event the caller recorded:
+ * when the bucket's last parameter is marked, the reducer records one event of
+ * its own on each distinct producer stream of the bucket, at that moment, and
+ * the bucket's issue waits for those.  A caller-recorded event per parameter
+ * would cost an event record per gradient (161 for ResNet-50) where this costs
+ * one per bucket and stream, and would leave the caller to keep every event
+ * alive until the side stream has waited on it.  A caller that holds an event
+ * instead can make a stream of its own wait on it and pass that stream.
  * Errors: DDP_E_INVAL (param out of range); DDP_E_STATE if param was already
  * marked in this iteration (DDP chapter 17.16: "Expected to mark a variable
  * ready only once") or prepare was not called; DDP_E_CUDA (event/launch).
@@ -736,6 +751,109 @@ ddp_status ddp_reducer_ready_order(const ddp_reducer* r, int32_t* out, int32_t c
 ddp_status ddp_reducer_bucket_ms(ddp_reducer* r, float* out, int32_t cap);
 
 void ddp_reducer_destroy(ddp_reducer* r);
+
+/* ------------------------------------------------------------------------ */
+/* The bucket plan as an object (host)                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * A ddp_plan holds step 1's result and everything derived from it that a C
+ * caller needs to run the path without re-deriving it: the buckets' places in
+ * one fp32 main_grad buffer per replica, the segment tables the kernels read
+ * (to be copied to the device by the caller: the library allocates no device
+ * memory), the bucket descriptors over those device copies, and the
+ * description DDP's logging data reports -- every bucket's bytes, padded
+ * elements, dtype, parameters and issue position (bucket_sizes), and the sizes
+ * of the buckets a rebuild over an observed gradient-ready order would form
+ * (rebuilt_bucket_sizes) ("DDP: ring AllReduce and gradient buckets" 17.13;
+ * 17.12: a bucket is a flat buffer with its parameters at fixed offsets;
+ * Megatron page 1: the buckets are slices of one contiguous main_grad buffer).
+ * A plan is immutable after creation and may be read from several threads.
+ */
+typedef struct ddp_plan ddp_plan;
+
+typedef struct ddp_plan_info {
+    int32_t nparams, nbuckets;
+    int32_t order, pad_multiple, grad_reduce_in_fp32, reserved_;
+    int64_t cap_bytes, first_cap_bytes;
+    int64_t align_elems;     /* every bucket starts on a multiple of this in main_grad */
+    int64_t replica_stride;  /* fp32 elements of one main_grad replica (all buckets) */
+    int64_t seg_offset_len;  /* entries of the segment-offset table: nparams + nbuckets */
+    int64_t seg_param_len;   /* entries of the segment-parameter table: nparams */
+} ddp_plan_info;
+
+/*
+ * ddp_plan_create -- run ddp_assign_buckets (same arguments and rules; dtypes
+ * NULL = every parameter fp32) and lay the buckets out: bucket b occupies
+ * elements [bucket_start[b], bucket_start[b] + bucket_numel[b]) of each
+ * replica, bucket_start[0] = 0 and every later start the previous bucket's end
+ * rounded up to a multiple of align_elems (64 makes every replica of every
+ * bucket 256-byte aligned when main_grad is).  HOST in; *out owns host memory
+ * only, released by ddp_plan_destroy.
+ * Errors: those of ddp_assign_buckets; DDP_E_INVAL (out NULL, align_elems
+ * outside [1, 2^20]).
+ */
+ddp_status ddp_plan_create(const int64_t* numels, const int32_t* dtypes, int32_t nparams, int64_t cap_bytes,
+                           int64_t first_cap_bytes, int32_t order, int32_t pad_multiple,
+                           int32_t grad_reduce_in_fp32, int64_t align_elems, ddp_plan** out);
+
+/*
+ * ddp_plan_describe -- the plan's sizes into *info and, for every output that
+ * is not NULL, its tables (HOST, caller-allocated): per bucket (nbuckets
+ * entries) bucket_numel (padded), bucket_bytes (unpadded, the logging data's
+ * bucket_sizes), bucket_dtype, bucket_order (bucket_order[k] = bucket issued
+ * k-th), bucket_start; member_start[nbuckets + 1] with members[nparams]
+ * (bucket b's parameters, in layout order, are members[member_start[b]] ..
+ * members[member_start[b + 1] - 1]); per parameter bucket_of and offset_of
+ * (elements from its bucket's start).  Same values as ddp_assign_buckets.
+ * Errors: DDP_E_INVAL (plan NULL).
+ */
+ddp_status ddp_plan_describe(const ddp_plan* plan, ddp_plan_info* info, int64_t* bucket_numel, int64_t* bucket_bytes,
+                             int32_t* bucket_dtype, int32_t* bucket_order, int64_t* bucket_start,
+                             int32_t* member_start, int32_t* members, int32_t* bucket_of, int64_t* offset_of);
+
+/*
+ * ddp_plan_tables -- the kernels' segment tables, HOST out: seg_offset
+ * int64[info.seg_offset_len], seg_param int32[info.seg_param_len].  Bucket by
+ * bucket: its parameters' offsets in layout order followed by the end of its
+ * last gradient (nseg + 1 entries), and its parameters' indices (nseg).  Copy
+ * both to the device and pass the device copies to ddp_plan_bucket_descs.
+ * Errors: DDP_E_INVAL (NULL plan or output).
+ */
+ddp_status ddp_plan_tables(const ddp_plan* plan, int64_t* seg_offset, int32_t* seg_param);
+
+/*
+ * ddp_plan_bucket_descs -- the descriptors of every bucket (HOST out
+ * ddp_bucket_desc[nbuckets]) pointing into the DEVICE copies of the tables of
+ * ddp_plan_tables.  Errors: DDP_E_INVAL (NULL argument).
+ */
+ddp_status ddp_plan_bucket_descs(const ddp_plan* plan, const int64_t* seg_offset_dev, const int32_t* seg_param_dev,
+                                 ddp_bucket_desc* out);
+
+/*
+ * ddp_plan_rebuilt -- the buckets a rebuild over `sequence` (HOST
+ * int32[nparams], a permutation: the gradient-ready order, e.g. from
+ * ddp_reducer_ready_order) would form with the plan's caps and dtypes
+ * (ddp_assign_buckets_ordered; DDP chapter 17.13, rebuilt_bucket_sizes):
+ * HOST out bucket_bytes and bucket_numel (either may be NULL), max_buckets
+ * entries; *nbuckets = their count.
+ * Errors: as ddp_assign_buckets_ordered; DDP_E_CAPACITY if more than
+ * max_buckets (nparams + 2 always suffices).
+ */
+ddp_status ddp_plan_rebuilt(const ddp_plan* plan, const int32_t* sequence, int64_t* bucket_bytes,
+                            int64_t* bucket_numel, int32_t max_buckets, int32_t* nbuckets);
+
+/*
+ * ddp_reducer_create_from_plan -- ddp_reducer_create with the plan's
+ * bucket_of, bucket_order, bucket_start and replica_stride; buckets are the
+ * descriptors from ddp_plan_bucket_descs.  The plan may be destroyed after
+ * the call (the reducer copies what it needs); the device tables may not.
+ */
+ddp_status ddp_reducer_create_from_plan(const ddp_plan* plan, const ddp_bucket_desc* buckets, int32_t W, int32_t mode,
+                                        int32_t flags, const void* const* grads, const uint8_t* used, int32_t ld,
+                                        float* main_grad, void* const* grads_out, const uint8_t* global_used,
+                                        void* side_stream, ddp_reducer** out);
+
+void ddp_plan_destroy(ddp_plan* plan);
 
 /* ------------------------------------------------------------------------ */
 /* Kernel variants and device status                                         */
