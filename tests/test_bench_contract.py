@@ -30,15 +30,21 @@ def test_reference_arm_json_line():
     assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["higher_is_better"] is True and d["value"] > 0
     assert d["config"]["workload"] == "resnet50_w8_allreduce"
+    # the same workload as the GPU arm's step: all five buckets, every algorithmic byte
+    assert d["config"]["buckets"] == 5 and d["config"]["bytes_per_step"] == 1_635_650_048
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["sample"].startswith("the whole workload: all 5 buckets")
+    th = cb["threaded"]
+    assert th["threads"] >= 1 and th["value"] > 0
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
 
 
 def test_reference_arm_other_ranks_print_nothing():
-    lines = run_bench({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}, "--steps", "1", "--warmup", "3")
+    lines = run_bench({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}, "--steps", "1", "--warmup", "3",
+                      "--no-threaded")
     assert lines == []
 
 
