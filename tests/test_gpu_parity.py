@@ -324,21 +324,47 @@ def test_mlp_copy_back_partial_use(orc):
         sess.close()
 
 
-def _sample(rng, n, k=1500):
-    return np.unique(np.concatenate([rng.integers(0, n, k), [0, n - 1]]))
+def boundary_sample(rng, n, W, seg_offsets=(), k=1500):
+    """Sampled element indices of an n-element bucket: k random ones plus the
+    elements on both sides of every place where the kernels' work changes hands --
+    every ring chunk's first and last element, every parameter segment's first and
+    last, the first and last element of each CTA's slice for one and two CTAs per
+    SM (152 and 304 slices, cut on 16-element multiples) and of the streaming
+    tiles that follow each slice start (1024, 2048 and 4096 elements), and every
+    multiple of 1024 within the first and last 64 Ki elements of each chunk."""
+    pts = [0, n - 1]
+    L = max(1, -(-n // W))
+    for c in range(W + 1):
+        pts += [c * L - 1, c * L, c * L + 1]
+        for t in range(0, 65536, 1024):
+            pts += [c * L + t, c * L + t - 1, c * L - t, c * L - t - 1]
+    for o in seg_offsets:
+        pts += [o - 1, o, o + 1]
+    for G in (152, 304):
+        for b in range(G + 1):
+            lo = (b * n // G) & ~15
+            for tile in (0, 1024, 2048, 4096, 8192):
+                pts += [lo + tile - 1, lo + tile]
+    pts = np.array(pts, np.int64)
+    pts = pts[(pts >= 0) & (pts < n)]
+    return np.unique(np.concatenate([pts, rng.integers(0, n, k)]))
 
 
 @pytest.mark.slow
-def test_gpt2_reduce_scatter_full_size_sampled(orc):
-    """GPT-2 small, bf16 -> fp32, Megatron buckets, W = 8 reduce_scatter: sampled
-    elements of every shard against the oracle; nothing outside the shards written."""
+def test_gpt2_reduce_scatter_full_size(orc):
+    """GPT-2 small, bf16 -> fp32, Megatron buckets, W = 8 reduce_scatter: every
+    element of every shard of all nine buckets against the oracle (pack, then the
+    ring's reduce-scatter), and nothing outside the shards written.  The oracle's
+    inputs are the seeded generator's gradients (its torch form, checked bit for
+    bit against its numpy form by the workload tests), copied to the host."""
     wl = WL.c3_gpt2()
-    sess = make_session(wl, device_grads(wl))
+    grads = device_grads(wl)
+    sess = make_session(wl, grads)
     sess.main_grad.fill_(float(SENTINEL))
     sess.step()
     torch.cuda.synchronize()
-    rng = np.random.default_rng(33)
     plan = sess.plan
+    assert plan.nbuckets == 9
     for b in range(plan.nbuckets):
         n = int(plan.bucket_numel[b])
         got = plan.bucket_view(sess.main_grad, b).cpu().numpy()
@@ -346,23 +372,23 @@ def test_gpt2_reduce_scatter_full_size_sampled(orc):
         for w in range(wl.W):  # outside shard w, replica w keeps the sentinel
             assert np.all(bits(got[w, :w * k]) == bits(np.array([SENTINEL])))
             assert np.all(bits(got[w, (w + 1) * k:]) == bits(np.array([SENTINEL])))
-        e = _sample(rng, n)
-        owner = chunk_of(e, n, wl.W)
-        t = np.zeros((wl.W, len(e)), np.float32)
-        for p in plan.members[b]:
-            lo, hi = int(plan.offset_of[p]), int(plan.offset_of[p]) + wl.numels[p]
-            sel = np.nonzero((e >= lo) & (e < hi))[0]
-            if len(sel):
-                t[:, sel] = packed_at(orc, wl, p, e[sel] - lo, 1)
-        want = oracle_at(orc, t, owner)
-        assert_bits_equal(got[owner, e], want, f"bucket {b}")
+        mem = plan.members[b]
+        raw = [[grads[w][p].view(torch.int16).cpu().numpy().view(np.uint16) for p in mem] for w in range(wl.W)]
+        packed = orc.pack(raw, [int(plan.offset_of[p]) for p in mem], n, [wl.dtype] * len(mem))
+        del raw
+        want, _ = orc.ring(packed, D.DDP_REDUCE_SCATTER)
+        for w in range(wl.W):
+            assert_bits_equal(got[w, w * k:(w + 1) * k], want[w, w * k:(w + 1) * k], f"bucket {b} shard {w}")
+        del packed, want, got
     sess.close()
 
 
 @pytest.mark.slow
 def test_bert_nosync_full_size_sampled(orc):
     """BERT-large, W = 4: three no_sync micro-steps accumulated locally, the fourth
-    reduced with the accumulated sum; one encoder layer unused (zero)."""
+    reduced with the accumulated sum; one encoder layer unused (zero).  Sampled at
+    every place where the kernels' work changes hands (boundary_sample) plus 500
+    random elements per bucket."""
     wl = WL.c4_bert_large()
     sess = make_session(wl, device_grads(wl, 3))
     for m in range(3):
@@ -381,7 +407,8 @@ def test_bert_nosync_full_size_sampled(orc):
         got = plan.bucket_view(sess.main_grad, b).cpu().numpy()
         for w in range(1, wl.W):
             assert np.array_equal(bits(got[0]), bits(got[w]))
-        e = _sample(rng, n, 500)
+        segs = [int(plan.offset_of[p]) for p in plan.members[b]]
+        e = boundary_sample(rng, n, wl.W, segs + [segs[-1] + wl.numels[plan.members[b][-1]]], 500)
         t = np.zeros((wl.W, len(e)), np.float32)
         for p in plan.members[b]:
             lo, hi = int(plan.offset_of[p]), int(plan.offset_of[p]) + wl.numels[p]
@@ -405,7 +432,7 @@ def test_sweep_bucket_sampled(orc, nbytes, W):
     for w in range(1, W):
         assert torch.equal(x[0], x[w])
     rng = np.random.default_rng(55)
-    e = _sample(rng, n, 4000)
+    e = boundary_sample(rng, n, W, (), 4000)
     t = np.stack([WL.values_np(WL.bits_at_np(WL.stream_key(1005, WL.stream_id(0, w)), e), "uniform")
                   for w in range(W)])
     want = oracle_at(orc, t, chunk_of(e, n, W))
@@ -567,7 +594,8 @@ def test_coalesced_reducer_vs_oracle(orc, name):
             ref = O.run_workload(wl, orc, copy_back=False) if b == 0 else ref
             assert_bits_equal(got, ref["bucket"][b], f"{name} bucket {b}")
         else:
-            e = _sample(rng, n, 400)
+            segs = [int(sess.plan.offset_of[p]) for p in sess.plan.members[b]]
+            e = boundary_sample(rng, n, wl.W, segs, 400)
             owner = chunk_of(e, n, wl.W)
             t = np.zeros((wl.W, len(e)), np.float32)
             for p in sess.plan.members[b]:
@@ -645,7 +673,7 @@ def test_bert_nosync_coalesced_sampled(orc):
     for b in range(0, plan.nbuckets, 3):
         n = int(plan.bucket_numel[b])
         got = plan.bucket_view(sess.main_grad, b).cpu().numpy()
-        e = _sample(rng, n, 300)
+        e = boundary_sample(rng, n, wl.W, [int(plan.offset_of[p]) for p in plan.members[b]], 300)
         t = np.zeros((wl.W, len(e)), np.float32)
         for p in plan.members[b]:
             lo, hi = int(plan.offset_of[p]), int(plan.offset_of[p]) + wl.numels[p]
