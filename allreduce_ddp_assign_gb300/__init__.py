@@ -25,7 +25,7 @@ DDP_ORDER_REVERSE, DDP_ORDER_FWD_THEN_REVERSE, DDP_ORDER_MEGATRON = 0, 1, 2
 DDP_ALLREDUCE, DDP_REDUCE_SCATTER = 0, 1
 DDP_R_FUSED, DDP_R_COPY_BACK, DDP_R_TIMING, DDP_R_DRY_RUN, DDP_R_COALESCE = 1, 2, 4, 8, 16
 DDP_R_WIRE_BF16, DDP_R_WIRE_F16, DDP_R_BUCKET_DONE = 32, 64, 128
-DDP_KERNEL_AUTO, DDP_KERNEL_PLAIN, DDP_KERNEL_STREAM = 0, 1, 2
+DDP_KERNEL_AUTO, DDP_KERNEL_PLAIN, DDP_KERNEL_STREAM, DDP_KERNEL_STREAM_DYNAMIC = 0, 1, 2, 3
 
 
 class DdpError(RuntimeError):

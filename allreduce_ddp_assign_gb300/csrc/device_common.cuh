@@ -167,6 +167,8 @@ struct StreamSpan {
     const int32_t* seg_param;
     int32_t nseg;
     int32_t mg_vec;              // every replica of mg is 16-byte aligned
+    int32_t cache_base;          // first entry of this span's tables in the shared-memory copy (set by the launcher)
+    int32_t pad_;
 };
 
 struct StreamArgs {
@@ -182,6 +184,15 @@ struct StreamArgs {
     int32_t store_bulk;          // results leave through TMA bulk stores (set by the launcher)
     int* status;                 // device status word (set by the launcher)
     int32_t wire;                // ring arithmetic type: DDP_F32, DDP_BF16, DDP_F16
+    // Work split (set by the launcher).  Elements [0, head) of the launch are cut
+    // into equal static slices, one per CTA; elements [head, total) form a pool of
+    // `unit`-element units that CTAs claim one at a time from the counters at
+    // `dyn` (claimed, finished) once their slice is done.  dyn == nullptr: no
+    // pool (head == total).
+    uint32_t* dyn;
+    int64_t head;
+    int32_t unit;
+    int32_t seg_cached;          // segment-table entries copied into shared memory (0: read from global memory)
     StreamSpan span[kMaxBatch];
 };
 

@@ -137,10 +137,12 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
     }
 }
 
-// Stage the piece's pointers; returns nonzero (on every thread) when all of
-// them allow 16-byte vectors.  Contains two block-wide barriers.
+// Stage the piece's pointers (parameter p, or -1 for padding); returns nonzero
+// (on every thread) when all of them allow 16-byte vectors.  The flag and
+// pointer tables are read side by side, not one after the other: one round
+// trip to memory instead of two.  Contains two block-wide barriers.
 template <int OP, int DT>
-__device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int s, int64_t off)
+__device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int p, int64_t off)
 {
     __syncthreads();  // the previous piece is done reading sh
     int ok = 1;
@@ -148,15 +150,19 @@ __device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int s
     if (t < cx.W) {
         const void* src = nullptr;
         float* dst = nullptr;
-        const int p = (cx.seg_offset && s < cx.nseg) ? cx.seg_param[s] : -1;
         if (p >= 0 && p < cx.ld) {
             const int64_t slot = static_cast<int64_t>(t) * cx.ld + p;
             if constexpr (OP == OP_PACK || OP == OP_FUSED) {
-                if (!cx.used || cx.used[slot]) src = cx.grads[slot];
+                const uint8_t u = cx.used ? cx.used[slot] : uint8_t{1};
+                const void* g = cx.grads[slot];
+                src = u ? g : nullptr;
             }
             if constexpr (OP == OP_UNPACK || OP == OP_FUSED) {
-                if (cx.grads_out && (!cx.global_used || cx.global_used[p]))
-                    dst = static_cast<float*>(cx.grads_out[slot]);
+                if (cx.grads_out) {
+                    const uint8_t gu = cx.global_used ? cx.global_used[p] : uint8_t{1};
+                    void* d = cx.grads_out[slot];
+                    dst = gu ? static_cast<float*>(d) : nullptr;
+                }
             }
         }
         sh.src[t] = src;
@@ -170,11 +176,11 @@ __device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int s
 }
 
 template <int OP, int WT, int DT>
-__device__ __forceinline__ void process_piece(const Ctx& cx, PieceShared& sh, int c, int s, int64_t off, int64_t a,
+__device__ __forceinline__ void process_piece(const Ctx& cx, PieceShared& sh, int c, int p, int64_t off, int64_t a,
                                               int64_t b)
 {
     constexpr int U = unroll_for<WT>();
-    if (piece_setup<OP, DT>(cx, sh, s, off)) {
+    if (piece_setup<OP, DT>(cx, sh, p, off)) {
         const int64_t va = lmin(b, (a + 3) & ~int64_t(3));
         const int64_t vb = lmax(va, b & ~int64_t(3));
         run_range<OP, WT, DT, 1, 1>(cx, sh, c, a, va - a, off);
@@ -185,16 +191,38 @@ __device__ __forceinline__ void process_piece(const Ctx& cx, PieceShared& sh, in
     }
 }
 
+// A bucket's segment table, copied into shared memory by every CTA when it has at
+// most kSegCache segments: all entries are read at once (one round trip) instead
+// of a binary search of dependent loads followed by a load per piece.  Buckets
+// with more segments read the table in global memory as they go.
+constexpr int kSegCache = 256;
+struct SegCache {
+    int64_t off[kSegCache + 1];
+    int32_t par[kSegCache];
+};
+
 template <int OP, int WT, int DT>
 __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
 {
     __shared__ PieceShared sh;
+    __shared__ SegCache sc;
     const int64_t G = gridDim.x;
     const int64_t blk = blockIdx.x;
     // this CTA's slice of the bucket, boundaries on 16-element multiples
     const int64_t lo = (blk * cx.n / G) & ~int64_t(15);
     const int64_t hi = (blk + 1 == G) ? cx.n : (((blk + 1) * cx.n / G) & ~int64_t(15));
     if (lo >= hi) return;  // whole CTA: no barrier is skipped by part of it
+
+    const bool cached = cx.seg_offset && cx.nseg <= kSegCache;
+    if (cached) {
+        for (int i = threadIdx.x; i <= cx.nseg; i += kThreads) {
+            sc.off[i] = cx.seg_offset[i];
+            if (i < cx.nseg) sc.par[i] = cx.seg_param[i];
+        }
+        __syncthreads();
+    }
+    auto seg_off = [&](int i) -> int64_t { return cached ? sc.off[i] : cx.seg_offset[i]; };
+    auto seg_par = [&](int i) -> int { return cached ? sc.par[i] : cx.seg_param[i]; };
 
     int c = static_cast<int>(lo / cx.chunk);
     if (c >= cx.nchunks) c = cx.nchunks - 1;
@@ -203,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
         int lo_i = 0, hi_i = cx.nseg + 1;
         while (hi_i - lo_i > 1) {
             const int mid = (lo_i + hi_i) >> 1;
-            if (cx.seg_offset[mid] <= lo) lo_i = mid; else hi_i = mid;
+            if (seg_off(mid) <= lo) lo_i = mid; else hi_i = mid;
         }
         s = lo_i;
     }
@@ -211,16 +239,20 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
     while (a < hi) {
         const int64_t c_end = (c + 1 >= cx.nchunks) ? cx.n : lmin(static_cast<int64_t>(c + 1) * cx.chunk, cx.n);
         int64_t s_off = 0, s_end = cx.n;
+        int p = -1;
         if (cx.seg_offset) {
-            s_off = cx.seg_offset[s];
-            s_end = (s < cx.nseg) ? cx.seg_offset[s + 1] : cx.n;
+            s_off = seg_off(s);
+            if (s < cx.nseg) {
+                s_end = seg_off(s + 1);
+                p = seg_par(s);
+            }
         }
         const int64_t b = lmin(hi, lmin(c_end, s_end));
-        if (b > a) process_piece<OP, WT, DT>(cx, sh, c, s, s_off, a, b);
+        if (b > a) process_piece<OP, WT, DT>(cx, sh, c, p, s_off, a, b);
         a = lmax(a, b);
         while (c + 1 < cx.nchunks && static_cast<int64_t>(c + 1) * cx.chunk <= a) ++c;
         if (cx.seg_offset)
-            while (s < cx.nseg && cx.seg_offset[s + 1] <= a) ++s;
+            while (s < cx.nseg && seg_off(s + 1) <= a) ++s;
     }
 }
 
@@ -332,7 +364,8 @@ bool use_stream(int op, int32_t W, int32_t dtype, bool acc, int32_t mode, int64_
 
 extern "C" ddp_status ddp_set_kernel_variant(int32_t variant)
 {
-    if (variant != DDP_KERNEL_AUTO && variant != DDP_KERNEL_PLAIN && variant != DDP_KERNEL_STREAM)
+    if (variant != DDP_KERNEL_AUTO && variant != DDP_KERNEL_PLAIN && variant != DDP_KERNEL_STREAM &&
+        variant != DDP_KERNEL_STREAM_DYNAMIC)
         return ddp::fail(DDP_E_INVAL, "ddp_set_kernel_variant: unknown variant %d", variant);
     ddpk::g_variant.store(variant, std::memory_order_relaxed);
     return ddp::ok();

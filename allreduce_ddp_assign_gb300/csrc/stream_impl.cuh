@@ -188,10 +188,13 @@ __device__ __forceinline__ void record_error(int* status, int code) { atomicOr(s
 
 // -- shared-memory layout (dynamic) -------------------------------------------
 struct Layout {
-    uint32_t full, empty, desc, src, dst, res, data, mgd, total;
+    uint32_t full, empty, desc, src, dst, res, data, mgd, cache, total;
 };
 
-__host__ __device__ inline Layout layout_for(int ns, int W, int tile, int gb, bool acc, bool store_bulk)
+// seg_cached: segment-table entries copied into shared memory (8 bytes of offset
+// and 4 of parameter index each), placed after everything else
+__host__ __device__ inline Layout layout_for(int ns, int W, int tile, int gb, bool acc, bool store_bulk,
+                                             int seg_cached = 0)
 {
     Layout L{};
     uint32_t o = 0;
@@ -214,6 +217,8 @@ __host__ __device__ inline Layout layout_for(int ns, int W, int tile, int gb, bo
     o = (o + 127u) & ~127u;
     L.mgd = o;
     if (acc) o += static_cast<uint32_t>(ns) * W * tile * 4;
+    L.cache = o;
+    o += static_cast<uint32_t>(seg_cached) * 12u;
     L.total = o;
     return L;
 }
@@ -276,7 +281,7 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
     const int ns = a.ns;
     constexpr bool acc = ACC;
     const bool sbulk = a.store_bulk != 0;
-    const Layout L = layout_for(ns, W, kTile, gb, acc, sbulk);
+    const Layout L = layout_for(ns, W, kTile, gb, acc, sbulk, a.seg_cached);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full);
     uint64_t* empty = reinterpret_cast<uint64_t*>(smem + L.empty);
     TileDesc* desc = reinterpret_cast<TileDesc*>(smem + L.desc);
@@ -285,6 +290,8 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
     float* res = reinterpret_cast<float*>(smem + L.res);
     unsigned char* data = smem + L.data;
     unsigned char* mgd = smem + L.mgd;
+    int64_t* cache_off = reinterpret_cast<int64_t*>(smem + L.cache);
+    int32_t* cache_par = reinterpret_cast<int32_t*>(smem + L.cache + 8u * static_cast<uint32_t>(a.seg_cached));
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x;
@@ -297,12 +304,26 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
         abort_flag = 0;
         fence_mbar_init();
     }
+    // every thread copies a share of the launch's segment tables: one round of
+    // independent loads, after which finding a piece's segment, offset and
+    // parameter reads shared memory only
+    if (a.seg_cached) {
+        for (int b = 0; b < a.nb; ++b) {
+            const StreamSpan& S = a.span[b];
+            if (!S.seg_offset) continue;
+            for (int i = tid; i <= S.nseg; i += kThreadsTma) {
+                cache_off[S.cache_base + i] = S.seg_offset[i];
+                if (i < S.nseg) cache_par[S.cache_base + i] = S.seg_param[i];
+            }
+        }
+    }
     __syncthreads();
 
+    // this CTA's static slice of the head [0, a.head)
     const int64_t G = gridDim.x;
     const int64_t blk = blockIdx.x;
-    const int64_t lo = (blk * a.total / G) & ~int64_t(15);
-    const int64_t hi = (blk + 1 == G) ? a.total : (((blk + 1) * a.total / G) & ~int64_t(15));
+    const int64_t lo = (blk * a.head / G) & ~int64_t(15);
+    const int64_t hi = (blk + 1 == G) ? a.head : (((blk + 1) * a.head / G) & ~int64_t(15));
 
     if (tid < 32) {
         // ===================== producer warp =====================
@@ -366,70 +387,100 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
             ++k;
         };
 
-        int b = 0;
-        int64_t x = lo;  // position in the launch's element space
-        while (x < hi && ok) {
-            while (b + 1 < a.nb && a.span[b].base + a.span[b].numel <= x) ++b;
-            const StreamSpan& S = a.span[b];
-            const int64_t end = lmin(hi, S.base + S.numel) - S.base;  // bucket-local end of this CTA's part
-            const int64_t chunk = (OP == OP_PACK) ? lmax(1, S.numel) : lmax(1, (S.numel + W - 1) / W);
-            int64_t e = x - S.base;
-            int c = static_cast<int>(e / chunk);
-            if (c >= W) c = W - 1;
-            int s = S.seg_offset ? warp_find_segment(S.seg_offset, S.nseg, e, lane) : 0;
-            while (e < end && ok) {
-                const int64_t c_end = (c + 1 >= W) ? S.numel : lmin(static_cast<int64_t>(c + 1) * chunk, S.numel);
-                int64_t s_off = 0, s_end = S.numel;
-                int p = -1;
-                if (S.seg_offset) {
-                    s_off = S.seg_offset[s];
-                    if (s < S.nseg) {
-                        s_end = S.seg_offset[s + 1];
-                        p = S.seg_param[s];
-                    }
-                }
-                const int64_t y = lmin(end, lmin(c_end, s_end));
-                if (y > e) {
-                    my_src = nullptr;
-                    my_dst = nullptr;
-                    if (lane < W) {
-                        if constexpr (OP == OP_RING) {
-                            my_src = S.mg + lane * a.stride;
-                        } else if (p >= 0 && p < a.ld) {
-                            const int64_t slot = static_cast<int64_t>(lane) * a.ld + p;
-                            if (!a.used || a.used[slot]) my_src = a.grads[slot];
-                            if (a.grads_out && (!a.global_used || a.global_used[p]))
-                                my_dst = static_cast<float*>(a.grads_out[slot]);
+        // tiles of the element range [lo, hi), in order
+        auto walk = [&](const int64_t lo, const int64_t hi) {
+            int b = 0;
+            int64_t x = lo;  // position in the launch's element space
+            while (x < hi && ok) {
+                while (b + 1 < a.nb && a.span[b].base + a.span[b].numel <= x) ++b;
+                const StreamSpan& S = a.span[b];
+                // the span's segment tables: the shared-memory copy when there is one
+                const int64_t* const seg_off = (a.seg_cached && S.seg_offset) ? cache_off + S.cache_base : S.seg_offset;
+                const int32_t* const seg_par = (a.seg_cached && S.seg_offset) ? cache_par + S.cache_base : S.seg_param;
+                const int64_t end = lmin(hi, S.base + S.numel) - S.base;  // bucket-local end of this CTA's part
+                const int64_t chunk = (OP == OP_PACK) ? lmax(1, S.numel) : lmax(1, (S.numel + W - 1) / W);
+                int64_t e = x - S.base;
+                int c = static_cast<int>(e / chunk);
+                if (c >= W) c = W - 1;
+                int s = seg_off ? warp_find_segment(seg_off, S.nseg, e, lane) : 0;
+                while (e < end && ok) {
+                    const int64_t c_end = (c + 1 >= W) ? S.numel : lmin(static_cast<int64_t>(c + 1) * chunk, S.numel);
+                    int64_t s_off = 0, s_end = S.numel;
+                    int p = -1;
+                    if (seg_off) {
+                        s_off = seg_off[s];
+                        if (s < S.nseg) {
+                            s_end = seg_off[s + 1];
+                            p = seg_par[s];
                         }
                     }
-                    bool lane_ok = true;
-                    if (my_src && (reinterpret_cast<uintptr_t>(my_src) - static_cast<uintptr_t>(s_off * gb)) % 16 != 0)
-                        lane_ok = false;
-                    if (my_dst && (reinterpret_cast<uintptr_t>(my_dst) - static_cast<uintptr_t>(s_off * 4)) % 16 != 0)
-                        lane_ok = false;
-                    const bool aligned = __all_sync(kFull, lane_ok) && (S.mg == nullptr || S.mg_vec);
-                    const uint32_t mask = __ballot_sync(kFull, my_src != nullptr);
-                    // bulk tiles start and end on 16-byte multiples of every operand
-                    constexpr int64_t gran = 16 / gb;
-                    int64_t t = e;
-                    if (aligned) {
-                        const int64_t va = lmin(y, (e + gran - 1) / gran * gran);
-                        const int64_t vb = lmax(va, y / gran * gran);
-                        if (va > e) emit(S.mg, c, s_off, e, static_cast<int32_t>(va - e), false, mask);
-                        for (t = va; t < vb && ok; t += kTile)
-                            emit(S.mg, c, s_off, t, static_cast<int32_t>(lmin(kTile, vb - t)), true, mask);
-                        t = vb;
+                    const int64_t y = lmin(end, lmin(c_end, s_end));
+                    if (y > e) {
+                        my_src = nullptr;
+                        my_dst = nullptr;
+                        if (lane < W) {
+                            if constexpr (OP == OP_RING) {
+                                my_src = S.mg + lane * a.stride;
+                            } else if (p >= 0 && p < a.ld) {
+                                // flags and pointers read side by side: one round trip, not two
+                                const int64_t slot = static_cast<int64_t>(lane) * a.ld + p;
+                                const uint8_t u = a.used ? a.used[slot] : uint8_t{1};
+                                const void* g = a.grads[slot];
+                                const uint8_t gu = (a.grads_out && a.global_used) ? a.global_used[p] : uint8_t{1};
+                                void* d = a.grads_out ? a.grads_out[slot] : nullptr;
+                                my_src = u ? g : nullptr;
+                                my_dst = gu ? static_cast<float*>(d) : nullptr;
+                            }
+                        }
+                        bool lane_ok = true;
+                        if (my_src && (reinterpret_cast<uintptr_t>(my_src) - static_cast<uintptr_t>(s_off * gb)) % 16 != 0)
+                            lane_ok = false;
+                        if (my_dst && (reinterpret_cast<uintptr_t>(my_dst) - static_cast<uintptr_t>(s_off * 4)) % 16 != 0)
+                            lane_ok = false;
+                        const bool aligned = __all_sync(kFull, lane_ok) && (S.mg == nullptr || S.mg_vec);
+                        const uint32_t mask = __ballot_sync(kFull, my_src != nullptr);
+                        // bulk tiles start and end on 16-byte multiples of every operand
+                        constexpr int64_t gran = 16 / gb;
+                        int64_t t = e;
+                        if (aligned) {
+                            const int64_t va = lmin(y, (e + gran - 1) / gran * gran);
+                            const int64_t vb = lmax(va, y / gran * gran);
+                            if (va > e) emit(S.mg, c, s_off, e, static_cast<int32_t>(va - e), false, mask);
+                            for (t = va; t < vb && ok; t += kTile)
+                                emit(S.mg, c, s_off, t, static_cast<int32_t>(lmin(kTile, vb - t)), true, mask);
+                            t = vb;
+                        }
+                        for (; t < y && ok; t += kTile)
+                            emit(S.mg, c, s_off, t, static_cast<int32_t>(lmin(kTile, y - t)), false, mask);
                     }
-                    for (; t < y && ok; t += kTile)
-                        emit(S.mg, c, s_off, t, static_cast<int32_t>(lmin(kTile, y - t)), false, mask);
+                    e = lmax(e, y);
+                    while (c + 1 < W && static_cast<int64_t>(c + 1) * chunk <= e) ++c;
+                    if (seg_off)
+                        while (s < S.nseg && seg_off[s + 1] <= e) ++s;
                 }
-                e = lmax(e, y);
-                while (c + 1 < W && static_cast<int64_t>(c + 1) * chunk <= e) ++c;
-                if (S.seg_offset)
-                    while (s < S.nseg && S.seg_offset[s + 1] <= e) ++s;
+                x = S.base + e;
+                if (b + 1 >= a.nb && e >= S.numel) break;  // past the last bucket
             }
-            x = S.base + e;
-            if (b + 1 >= a.nb && e >= S.numel) break;  // past the last bucket
+        };
+        walk(lo, hi);
+        if (a.dyn) {
+            // the pool: claim a unit after the previous one's tiles are issued (the
+            // claim's round trip overlaps the stages still queued), until none is left
+            const int64_t nunits = (a.total - a.head + a.unit - 1) / a.unit;
+            while (ok) {
+                uint32_t u = 0;
+                if (lane == 0) u = atomicAdd(&a.dyn[0], 1u);
+                u = __shfl_sync(kFull, u, 0);
+                if (static_cast<int64_t>(u) >= nunits) break;
+                const int64_t x0 = a.head + static_cast<int64_t>(u) * a.unit;
+                walk(x0, lmin(a.total, x0 + a.unit));
+            }
+            // the last CTA to stop claiming clears both counters for the slot's next
+            // launch (which the launcher orders after this one)
+            if (lane == 0 && atomicAdd(&a.dyn[1], 1u) == gridDim.x - 1) {
+                atomicExch(&a.dyn[0], 0u);
+                atomicExch(&a.dyn[1], 0u);
+            }
         }
         // sentinel
         const int st = claim();
@@ -649,7 +700,11 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
 
 // -- host side ------------------------------------------------------------------
 constexpr uint32_t kSmemBudget2 = DDP_STREAM_BUDGET2_KB * 1024;  // two CTAs per SM
-constexpr uint32_t kSmemBudget1 = 220 * 1024;                    // one CTA per SM
+constexpr uint32_t kSmemBudget1 = 220 * 1024;                    // one CTA per SM: the stage ring
+// Fraction of a launch with a pool that is split statically (in 1/16ths), and the
+// operand bytes staged per pool unit (whole tiles, at least one).
+constexpr int64_t kHeadSixteenths = 10;
+constexpr int64_t kUnitBytes = 64 * 1024;
 
 // stages that fit the budget (0 if fewer than two)
 inline int stages_for(int W, int tile, int gb, bool acc, bool sbulk, uint32_t budget)
@@ -677,6 +732,23 @@ inline bool plan_for(int W, int tile, int gb, bool acc, bool sbulk, StagePlan* p
     return true;
 }
 
+// The most dynamic shared memory a CTA of the current device may use (per device).
+inline uint32_t smem_optin_limit()
+{
+    static std::atomic<uint32_t> cached[ddp::kMaxDevices] = {};
+    const int dev = ddp::current_device();
+    uint32_t v = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
+    if (!v) {
+        int x = 0, d = 0;
+        if (cudaGetDevice(&d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&x, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) != cudaSuccess || x <= 0)
+            x = static_cast<int>(kSmemBudget1);
+        v = static_cast<uint32_t>(x);
+        if (dev >= 0) cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
 template <int OP, int WT, int DT, bool ACC, bool WR>
 ddp_status launch_instance(StreamArgs& a, void* stream)
 {
@@ -687,19 +759,40 @@ ddp_status launch_instance(StreamArgs& a, void* stream)
     if (!plan_for(a.W, tile, gb, ACC, a.store_bulk, &p))
         return ddp::fail(DDP_E_INVAL, "stream kernel: no stage layout fits for W = %d", a.W);
     a.ns = p.ns;
+    // the segment tables go into shared memory when they fit beside the stages
+    // without costing a CTA per SM: up to the device's limit for one CTA per SM, up
+    // to the two-CTA budget otherwise
+    int64_t entries = 0;
+    for (int b = 0; b < a.nb; ++b) {
+        a.span[b].cache_base = static_cast<int32_t>(entries);
+        if (a.span[b].seg_offset) entries += a.span[b].nseg + 1;
+    }
+    const uint32_t room = (p.budget == kSmemBudget1) ? smem_optin_limit() : kSmemBudget2;
+    a.seg_cached = (entries > 0 && p.bytes + 12 * entries <= room) ? static_cast<int32_t>(entries) : 0;
+    const uint32_t bytes = layout_for(p.ns, a.W, tile, gb, ACC, a.store_bulk, a.seg_cached).total;
+    // the pool: whole tiles of about kUnitBytes of staged operands
+    if (a.dyn) {
+        const int64_t stage = static_cast<int64_t>(a.W) * tile * (gb + (ACC ? 4 : 0));
+        a.unit = static_cast<int32_t>(tile * lmax(1, kUnitBytes / stage));
+        a.head = (a.total * kHeadSixteenths / 16) & ~int64_t(15);
+    } else {
+        a.unit = 0;
+        a.head = a.total;
+    }
     // Per device: the dynamic shared memory this instantiation may use (a function
     // attribute, set once per device and raised when a launch needs more), and the
-    // resident CTAs per SM at the last shared-memory size asked for, packed as
+    // resident CTAs per SM at the last stage-ring size asked for, packed as
     // (bytes << 32 | CTAs) so that the pair is read and written as one value.
     static std::atomic<uint32_t> configured[ddp::kMaxDevices] = {};
     static std::atomic<uint64_t> occupancy[ddp::kMaxDevices] = {};
     const int dev = ddp::current_device();
-    if (dev < 0 || configured[dev].load(std::memory_order_acquire) < p.budget) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.budget);
+    const uint32_t want_attr = bytes > p.budget ? bytes : p.budget;
+    if (dev < 0 || configured[dev].load(std::memory_order_acquire) < want_attr) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, want_attr);
         if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         if (dev >= 0) {
             uint32_t cur = configured[dev].load(std::memory_order_relaxed);
-            while (cur < p.budget && !configured[dev].compare_exchange_weak(cur, p.budget, std::memory_order_release)) {
+            while (cur < want_attr && !configured[dev].compare_exchange_weak(cur, want_attr, std::memory_order_release)) {
             }
         }
     }
@@ -716,7 +809,7 @@ ddp_status launch_instance(StreamArgs& a, void* stream)
     // chunk, at least) run in parallel CTAs rather than through one CTA's pipeline
     const int64_t want = (a.total + 15) / 16;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(ddp::device_sm_count()) * occ)));
-    kern<<<grid, kThreadsTma, p.bytes, static_cast<cudaStream_t>(stream)>>>(a);
+    kern<<<grid, kThreadsTma, bytes, static_cast<cudaStream_t>(stream)>>>(a);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "stream kernel launch failed: %s", cudaGetErrorString(err));
     return ddp::ok();

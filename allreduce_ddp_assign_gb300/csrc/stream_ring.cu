@@ -1,5 +1,7 @@
 // The streaming kernel's ring instantiation, the per-operation dispatch, and
 // the device status word the streaming kernels report wait timeouts in.
+#include <mutex>
+
 #include "stream_impl.cuh"
 
 namespace ddpk {
@@ -39,15 +41,92 @@ bool stream_supported(int op, int W, int dtype, bool acc, int mode)
     return plan_for(W, tile, gb, acc, sbulk, &p);
 }
 
+namespace {
+
+// Counters of the streaming kernels' work pools.  A launch with a pool owns one
+// slot (claimed, finished; 128 bytes apart) for its lifetime: the last of its CTAs
+// to stop claiming clears the slot.  Slots are handed out round robin per device,
+// and a launch waits, on its stream, for the event recorded after the slot's
+// previous launch, so two launches never share a slot at the same time whatever
+// streams they run on.
+constexpr int kPoolSlots = 64;
+constexpr int kSlotWords = 32;
+__device__ uint32_t g_pool_counters[kPoolSlots * kSlotWords];
+
+// A launch moving at least this many operand elements (numel x W) gets a pool
+// under DDP_KERNEL_AUTO: below it the static split's tail is short.
+constexpr int64_t kPoolMinElems = int64_t{1} << 23;
+
+struct PoolSlots {
+    std::mutex mu;
+    uint32_t next = 0;
+    uint32_t* base = nullptr;
+    cudaEvent_t done[kPoolSlots] = {};
+    bool pending[kPoolSlots] = {};
+};
+PoolSlots g_pools[ddp::kMaxDevices];
+
+bool wants_pool(const StreamArgs& a, void* stream)
+{
+    const int v = kernel_variant();
+    if (v == DDP_KERNEL_STREAM) return false;
+    if (v != DDP_KERNEL_STREAM_DYNAMIC && a.total * a.W < kPoolMinElems) return false;
+    // a captured launch would replay with the slot it was captured with, outside the
+    // event chain: captured launches keep the static split
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cs == cudaStreamCaptureStatusNone;
+}
+
+}  // namespace
+
 ddp_status launch_stream(int op, StreamArgs& a, int dtype, void* stream)
 {
     a.status = status_word();
     if (!a.status) return ddp::fail(DDP_E_CUDA, "stream kernel: device status word unavailable");
     a.store_bulk = op != OP_PACK && a.mode == DDP_ALLREDUCE;
-    if (op == OP_RING)
-        return a.wire == DDP_F32 ? launch_op<OP_RING, false>(a, dtype, stream) : launch_op<OP_RING, true>(a, dtype, stream);
-    if (op == OP_PACK) return launch_stream_pack(a, dtype, stream);
-    return launch_stream_fused(a, dtype, stream);
+    a.dyn = nullptr;
+    auto launch = [&]() -> ddp_status {
+        if (op == OP_RING)
+            return a.wire == DDP_F32 ? launch_op<OP_RING, false>(a, dtype, stream)
+                                     : launch_op<OP_RING, true>(a, dtype, stream);
+        if (op == OP_PACK) return launch_stream_pack(a, dtype, stream);
+        return launch_stream_fused(a, dtype, stream);
+    };
+    const int dev = ddp::current_device();
+    if (dev < 0 || !wants_pool(a, stream)) return launch();
+
+    PoolSlots& P = g_pools[dev];
+    std::lock_guard<std::mutex> lock(P.mu);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!P.base) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_pool_counters) != cudaSuccess) {
+            cudaGetLastError();
+            return launch();   // no pool: the static split
+        }
+        P.base = static_cast<uint32_t*>(addr);
+    }
+    const uint32_t k = P.next % kPoolSlots;
+    if (!P.done[k] && cudaEventCreateWithFlags(&P.done[k], cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        P.done[k] = nullptr;
+        return launch();
+    }
+    if (P.pending[k]) {
+        const cudaError_t e = cudaStreamWaitEvent(s, P.done[k], 0);
+        if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "cudaStreamWaitEvent: %s", cudaGetErrorString(e));
+    }
+    ++P.next;
+    a.dyn = P.base + k * kSlotWords;
+    const ddp_status st = launch();
+    const cudaError_t e = cudaEventRecord(P.done[k], s);
+    if (e != cudaSuccess) return ddp::fail(DDP_E_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+    P.pending[k] = true;
+    return st;
 }
 
 ddp_status read_device_status(void* stream, int32_t* out, int reset)

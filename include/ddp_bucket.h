@@ -25,8 +25,12 @@
  *     why, naming the parameter or bucket involved.  Arguments are validated on
  *     the host before anything is launched; a failed call launches nothing.
  *   - Memory: the caller owns all host and device memory.  The library
- *     allocates no device memory.  A reducer owns host bookkeeping and the
- *     CUDA events it creates, released by ddp_reducer_destroy.
+ *     allocates no device memory; its own device data are three small static
+ *     arrays of the module (the status word of ddp_device_status, the
+ *     streaming kernels' pool counters, and the scratch of
+ *     ddp_powersgd_reduce_static).  A reducer owns host bookkeeping and the
+ *     CUDA events it creates, released by ddp_reducer_destroy; the library
+ *     keeps up to 64 events per device for the pool counters until exit.
  *   - Streams: `stream` arguments are cudaStream_t handles passed as void*
  *     (NULL = the legacy default stream).  Data-path calls are asynchronous on
  *     that stream; only ddp_reducer_finalize with a timeout waits on the host.
@@ -860,19 +864,30 @@ void ddp_plan_destroy(ddp_plan* plan);
 /* ------------------------------------------------------------------------ */
 /*
  * Two implementations compute every data-path call with identical results:
- *   DDP_KERNEL_STREAM every launch the TMA-pipelined streaming kernel can take
- *                     (its shared-memory stage ring fits: 2 <= W <= 16, and a
- *                     vector-aligned main_grad for the allreduce) uses it; the
- *                     rest use the plain kernel.
- *   DDP_KERNEL_AUTO   (default) as DDP_KERNEL_STREAM, except that a launch of a
- *                     single bucket with numel x W <= 2^21 elements uses the
- *                     plain kernel, which finishes such small launches first.
- *   DDP_KERNEL_PLAIN  every call uses the plain kernel (16-byte loads straight
- *                     into registers).
+ * the TMA-pipelined streaming kernel (it takes a launch when its shared-memory
+ * stage ring fits: 2 <= W <= 16, and a vector-aligned main_grad for the
+ * allreduce) and the plain kernel (16-byte loads straight into registers).
+ * The streaming kernel splits a launch between its CTAs in one of two ways with
+ * identical results: a static split (equal slices), or a static head of about
+ * 5/8 of the elements followed by a pool of units of about 64 KB of operands
+ * that CTAs claim one at a time when their slice is done, so that CTAs on
+ * faster SMs take more of the tail.  A launch with a pool uses one of 64
+ * counter slots in the library's own device memory and waits, on its stream,
+ * for the previous launch that used the same slot (an event the library
+ * records); launches made during stream capture keep the static split.
+ *   DDP_KERNEL_AUTO   (default) a launch of a single bucket with numel x W <=
+ *                     2^21 elements takes the plain kernel, which finishes such
+ *                     small launches first; the rest take the streaming kernel,
+ *                     with a pool when numel x W >= 2^23.
+ *   DDP_KERNEL_STREAM every launch the streaming kernel can take uses it, with
+ *                     the static split; the rest use the plain kernel.
+ *   DDP_KERNEL_STREAM_DYNAMIC  as DDP_KERNEL_STREAM, with a pool on every
+ *                     streaming launch outside stream capture.
+ *   DDP_KERNEL_PLAIN  every call uses the plain kernel.
  * The choice is process-wide and applies to calls made after it.
  * Errors: DDP_E_INVAL for an unknown variant.
  */
-enum { DDP_KERNEL_AUTO = 0, DDP_KERNEL_PLAIN = 1, DDP_KERNEL_STREAM = 2 };
+enum { DDP_KERNEL_AUTO = 0, DDP_KERNEL_PLAIN = 1, DDP_KERNEL_STREAM = 2, DDP_KERNEL_STREAM_DYNAMIC = 3 };
 ddp_status ddp_set_kernel_variant(int32_t variant);
 
 /*

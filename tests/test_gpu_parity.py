@@ -21,12 +21,13 @@ if not torch.cuda.is_available():  # pragma: no cover
 DEV = torch.device("cuda:0")
 
 
-@pytest.fixture(params=[D.DDP_KERNEL_AUTO, D.DDP_KERNEL_PLAIN, D.DDP_KERNEL_STREAM],
-                ids=["auto", "plain", "stream"])
+@pytest.fixture(params=[D.DDP_KERNEL_AUTO, D.DDP_KERNEL_PLAIN, D.DDP_KERNEL_STREAM, D.DDP_KERNEL_STREAM_DYNAMIC],
+                ids=["auto", "plain", "stream", "stream_pool"])
 def variant(request):
     """Both implementations (the TMA-pipelined streaming kernel wherever it applies,
-    and the plain 16-byte-load kernel) and the default mix of the two (small
-    single-bucket launches plain) must match the oracle."""
+    with its static split and with the claimed pool of units, and the plain
+    16-byte-load kernel) and the default mix (small single-bucket launches plain,
+    a pool on large launches) must match the oracle."""
     D.ddp_set_kernel_variant(request.param)
     yield request.param
     D.ddp_set_kernel_variant(D.DDP_KERNEL_AUTO)
