@@ -702,9 +702,32 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
 constexpr uint32_t kSmemBudget2 = DDP_STREAM_BUDGET2_KB * 1024;  // two CTAs per SM
 constexpr uint32_t kSmemBudget1 = 220 * 1024;                    // one CTA per SM: the stage ring
 // Fraction of a launch with a pool that is split statically (in 1/16ths), and the
-// operand bytes staged per pool unit (whole tiles, at least one).
-constexpr int64_t kHeadSixteenths = 10;
-constexpr int64_t kUnitBytes = 64 * 1024;
+// operand bytes staged per pool unit (whole tiles, at least one).  Measured on
+// GB300: the ring reduction of packed replicas does best with the larger pool of
+// smaller units (its units cost the producer no table reads), the launches that
+// read gradients through the segment tables with the smaller pool of larger units
+// (ResNet-50 W = 8, coalesced: 6.01 TB/s at 10/16 and 64 KB, 6.22 at 12/16 and
+// 128 KB, 6.12 at 12/16 and 256 KB; the 64 MiB x 2 ring: 5.62 against 5.39).
+#ifndef DDP_STREAM_HEAD_16THS
+#define DDP_STREAM_HEAD_16THS 12
+#endif
+#ifndef DDP_STREAM_UNIT_KB
+#define DDP_STREAM_UNIT_KB 128
+#endif
+#ifndef DDP_STREAM_RING_HEAD_16THS
+#define DDP_STREAM_RING_HEAD_16THS 10
+#endif
+#ifndef DDP_STREAM_RING_UNIT_KB
+#define DDP_STREAM_RING_UNIT_KB 64
+#endif
+template <int OP> constexpr int64_t head_sixteenths()
+{
+    return OP == OP_RING ? DDP_STREAM_RING_HEAD_16THS : DDP_STREAM_HEAD_16THS;
+}
+template <int OP> constexpr int64_t unit_bytes()
+{
+    return (OP == OP_RING ? DDP_STREAM_RING_UNIT_KB : DDP_STREAM_UNIT_KB) * 1024;
+}
 
 // stages that fit the budget (0 if fewer than two)
 inline int stages_for(int W, int tile, int gb, bool acc, bool sbulk, uint32_t budget)
@@ -773,8 +796,8 @@ ddp_status launch_instance(StreamArgs& a, void* stream)
     // the pool: whole tiles of about kUnitBytes of staged operands
     if (a.dyn) {
         const int64_t stage = static_cast<int64_t>(a.W) * tile * (gb + (ACC ? 4 : 0));
-        a.unit = static_cast<int32_t>(tile * lmax(1, kUnitBytes / stage));
-        a.head = (a.total * kHeadSixteenths / 16) & ~int64_t(15);
+        a.unit = static_cast<int32_t>(tile * lmax(1, unit_bytes<OP>() / stage));
+        a.head = (a.total * head_sixteenths<OP>() / 16) & ~int64_t(15);
     } else {
         a.unit = 0;
         a.head = a.total;
