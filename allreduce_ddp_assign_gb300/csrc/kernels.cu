@@ -37,15 +37,58 @@
 namespace ddpk {
 
 // ---------------------------------------------------------------------------
+// main_grad access of VEC consecutive elements whose address is aligned to MGA
+// floats: a 16-byte vector (MGA 4), two 8-byte halves (2) or four words (1).
+// A segment whose bucket offset is not a multiple of 4 (a 10-element bias ahead
+// of it, say) keeps 16-byte gradient and output accesses this way, with only
+// its main_grad accesses split.
+// ---------------------------------------------------------------------------
+template <int VEC, int MGA> struct MgLane {
+    __device__ __forceinline__ static float ld(const float* p) { return __ldcs(p); }
+    __device__ __forceinline__ static void st(float* p, float v) { __stcs(p, v); }
+};
+template <int MGA> struct MgLane<4, MGA> {
+    __device__ __forceinline__ static float4 ld(const float* p)
+    {
+        if constexpr (MGA == 4) {
+            return __ldcs(reinterpret_cast<const float4*>(p));
+        } else if constexpr (MGA == 2) {
+            const float2 x = __ldcs(reinterpret_cast<const float2*>(p));
+            const float2 y = __ldcs(reinterpret_cast<const float2*>(p + 2));
+            return make_float4(x.x, x.y, y.x, y.y);
+        } else {
+            return make_float4(__ldcs(p), __ldcs(p + 1), __ldcs(p + 2), __ldcs(p + 3));
+        }
+    }
+    __device__ __forceinline__ static void st(float* p, float4 v)
+    {
+        if constexpr (MGA == 4) {
+            __stcs(reinterpret_cast<float4*>(p), v);
+        } else if constexpr (MGA == 2) {
+            __stcs(reinterpret_cast<float2*>(p), make_float2(v.x, v.y));
+            __stcs(reinterpret_cast<float2*>(p + 2), make_float2(v.z, v.w));
+        } else {
+            __stcs(p, v.x);
+            __stcs(p + 1, v.y);
+            __stcs(p + 2, v.z);
+            __stcs(p + 3, v.w);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
 // one piece: elements [a, b) of chunk c, inside one segment (or the padding)
 // ---------------------------------------------------------------------------
 // Processes elements e0 + VEC*v, v in [0, count).  `off` is the segment's
-// first bucket element (gradient index i = e - off).
-template <int OP, int WT, int DT, int VEC, int U>
+// first bucket element (gradient index i = e - off).  With VEC = 4 the
+// gradient and output vectors are 16-byte aligned and main_grad's are aligned
+// to MGA floats.
+template <int OP, int WT, int DT, int VEC, int U, int MGA = 4>
 __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, int c, int64_t e0, int64_t count,
                                           int64_t off)
 {
     using L = Lane<VEC>;
+    using M = MgLane<VEC, MGA>;
     using T = typename L::T;
     const int W = WT ? WT : cx.W;
     const int64_t step = static_cast<int64_t>(kThreads) * U;
@@ -64,11 +107,11 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
             // value of replica r at element x (before scaling)
             auto value = [&](int r, int64_t x) -> T {
                 if constexpr (OP == OP_RING) {
-                    return L::ld(cx.mg + r * cx.stride + x);
+                    return M::ld(cx.mg + r * cx.stride + x);
                 } else {
                     const void* src = sh.src[r];
                     if (cx.accumulate) {
-                        const T m = L::ld(cx.mg + r * cx.stride + x);
+                        const T m = M::ld(cx.mg + r * cx.stride + x);
                         return src ? L::add(m, L::template ldg<DT>(src, x - off)) : m;
                     }
                     return src ? L::template ldg<DT>(src, x - off) : L::zero();
@@ -96,9 +139,9 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
                 if (!live[u]) continue;
                 if (cx.mg) {
                     if (cx.mode == DDP_ALLREDUCE) {
-                        for (int w = 0; w < W; ++w) L::st(cx.mg + w * cx.stride + e[u], acc[u]);
+                        for (int w = 0; w < W; ++w) M::st(cx.mg + w * cx.stride + e[u], acc[u]);
                     } else {
-                        L::st(cx.mg + c * cx.stride + e[u], acc[u]);
+                        M::st(cx.mg + c * cx.stride + e[u], acc[u]);
                     }
                 }
                 if constexpr (OP == OP_FUSED) {
@@ -119,8 +162,8 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
                 for (int u = 0; u < U; ++u) {
                     if (!live[u]) continue;
                     T t = src ? L::template ldg<DT>(src, e[u] - off) : L::zero();
-                    if (cx.accumulate) t = L::add(L::ld(row + e[u]), t);
-                    L::st(row + e[u], t);
+                    if (cx.accumulate) t = L::add(M::ld(row + e[u]), t);
+                    M::st(row + e[u], t);
                 }
             }
         } else {  // OP_UNPACK
@@ -131,21 +174,24 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
                 const float* row = cx.mg + w * cx.stride;
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (live[u]) L::st(dst + (e[u] - off), L::ld(row + e[u]));
+                    if (live[u]) L::st(dst + (e[u] - off), M::ld(row + e[u]));
             }
         }
     }
 }
 
-// Stage the piece's pointers (parameter p, or -1 for padding); returns nonzero
-// (on every thread) when all of them allow 16-byte vectors.  The flag and
-// pointer tables are read side by side, not one after the other: one round
-// trip to memory instead of two.  Contains two block-wide barriers.
+// Stage the piece's pointers (parameter p, or -1 for padding).  Returns, on
+// every thread: 2 when every operand allows 16-byte vectors at bucket elements
+// e = 0 mod 4; 1 when the gradients and outputs allow them at gradient index
+// 0 mod 4 (bucket elements e = off mod 4) and main_grad is vector-aligned, so
+// that only main_grad's accesses there are narrower; 0 otherwise (scalars).  The
+// flag and pointer tables are read side by side, not one after the other: one
+// round trip to memory instead of two.  Contains three block-wide barriers.
 template <int OP, int DT>
 __device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int p, int64_t off)
 {
     __syncthreads();  // the previous piece is done reading sh
-    int ok = 1;
+    int ok = 1, okg = 1;
     const int t = threadIdx.x;
     if (t < cx.W) {
         const void* src = nullptr;
@@ -171,8 +217,13 @@ __device__ __forceinline__ int piece_setup(const Ctx& cx, PieceShared& sh, int p
         constexpr int64_t gb = elem_bytes<DT>();
         if (src && ((reinterpret_cast<uintptr_t>(src) - static_cast<uintptr_t>(off * gb)) % (4 * gb)) != 0) ok = 0;
         if (dst && ((reinterpret_cast<uintptr_t>(dst) - static_cast<uintptr_t>(off * 4)) % 16) != 0) ok = 0;
+        if (src && (reinterpret_cast<uintptr_t>(src) % (4 * gb)) != 0) okg = 0;
+        if (dst && (reinterpret_cast<uintptr_t>(dst) % 16) != 0) okg = 0;
     }
-    return __syncthreads_and(ok) && (cx.mg == nullptr || cx.mg_vec);
+    const bool all = __syncthreads_and(ok) != 0;
+    const bool shifted = __syncthreads_and(okg) != 0;
+    if (!(cx.mg == nullptr || cx.mg_vec)) return 0;
+    return all ? 2 : (shifted ? 1 : 0);
 }
 
 template <int OP, int WT, int DT>
@@ -180,11 +231,23 @@ __device__ __forceinline__ void process_piece(const Ctx& cx, PieceShared& sh, in
                                               int64_t b)
 {
     constexpr int U = unroll_for<WT>();
-    if (piece_setup<OP, DT>(cx, sh, p, off)) {
+    const int al = piece_setup<OP, DT>(cx, sh, p, off);
+    if (al == 2 || (al == 1 && off % 4 == 0)) {
         const int64_t va = lmin(b, (a + 3) & ~int64_t(3));
         const int64_t vb = lmax(va, b & ~int64_t(3));
         run_range<OP, WT, DT, 1, 1>(cx, sh, c, a, va - a, off);
         run_range<OP, WT, DT, 4, U>(cx, sh, c, va, (vb - va) >> 2, off);
+        run_range<OP, WT, DT, 1, 1>(cx, sh, c, vb, b - vb, off);
+    } else if (al == 1) {
+        // vectors on the gradient's grid: bucket elements e = off mod 4
+        const int64_t va = lmin(b, a + (((off - a) % 4) + 4) % 4);
+        const int64_t nv = (b - va) >> 2;
+        const int64_t vb = va + 4 * nv;
+        run_range<OP, WT, DT, 1, 1>(cx, sh, c, a, va - a, off);
+        if (off % 2 == 0)
+            run_range<OP, WT, DT, 4, U, 2>(cx, sh, c, va, nv, off);
+        else
+            run_range<OP, WT, DT, 4, U, 1>(cx, sh, c, va, nv, off);
         run_range<OP, WT, DT, 1, 1>(cx, sh, c, vb, b - vb, off);
     } else {
         run_range<OP, WT, DT, 1, 4>(cx, sh, c, a, b - a, off);

@@ -43,13 +43,22 @@
 
 namespace {
 
+#ifndef DDP_PSGD_P_BLOCKS
+#define DDP_PSGD_P_BLOCKS 1   // resident blocks per SM the P pass is compiled for
+#endif
+#ifndef DDP_PSGD_Q_BLOCKS
+#define DDP_PSGD_Q_BLOCKS 1   // resident blocks per SM the Q pass is compiled for
+#endif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsOut = kWarps;       // rows per output tile: one per warp
 constexpr int kRowsPerSplit = 256;     // rows of one partial M^T P
 constexpr int kMaxPairs = 256;         // (row, replica) pairs per P tile
 constexpr int kMaxRowsP = 16;          // rows per P tile
-constexpr int kGW = 4;                 // replicas a warp carries at once in the P pass
+#ifndef DDP_PSGD_GW
+#define DDP_PSGD_GW 4
+#endif
+constexpr int kGW = DDP_PSGD_GW;       // replicas a warp carries at once in the P pass
 constexpr int kOutBatch = 8;           // replicas whose error loads the output pass issues together
 constexpr int kOutQuads = 2048;        // 16-byte quads per flat output tile
 constexpr int64_t kVecPiece = 16384;   // elements of a 1-D tensor per block
@@ -148,7 +157,7 @@ __device__ void vec_piece(const PsgdArgs& a, const PsgdVec v)
 // group of up to kGW replicas, which share the loads of Q)
 // ---------------------------------------------------------------------------
 template <int RP>
-__global__ void __launch_bounds__(kThreads) psgd_p_kernel(const PsgdArgs a)
+__global__ void __launch_bounds__(kThreads, DDP_PSGD_P_BLOCKS) psgd_p_kernel(const PsgdArgs a)
 {
     constexpr int NG = RP * (RP + 1) / 2;
     __shared__ float part[kMaxPairs][RP];
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
 // partials in the order (replica, split) and writes Q = sum / W.
 // ---------------------------------------------------------------------------
 template <int RP>
-__global__ void __launch_bounds__(kThreads) psgd_qpart_kernel(const PsgdArgs a)
+__global__ void __launch_bounds__(kThreads, DDP_PSGD_Q_BLOCKS) psgd_qpart_kernel(const PsgdArgs a)
 {
     __shared__ float red[kWarps][128 * RP];
     __shared__ int last;

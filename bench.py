@@ -497,18 +497,43 @@ def run_ours(args, wl):
         descs = [plan.descs[b] for b in order]
         starts = [int(plan.bucket_start[b]) for b in order]
         ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(sess.side):
-            for r in range(Kp + 3):
-                if r == 3:
-                    ka.record(sess.side)
-                s_ = sessions[r % R]
-                D2.ddp_fused_bucket_group(descs, starts, s_.grads_tab, s_.used_tab, wl.nparams, wl.W, wl.mode, 0,
-                                          s_.main_grad, plan.replica_stride, None, None, sess.side)
+
+        def launch(r, stream):
+            s_ = sessions[r % R]
+            D2.ddp_fused_bucket_group(descs, starts, s_.grads_tab, s_.used_tab, wl.nparams, wl.W, wl.mode, 0,
+                                      s_.main_grad, plan.replica_stride, None, None, stream)
+        if R > 1:
+            # small launches: replayed from a CUDA graph of one launch per input copy, so
+            # the figure is the GPU's time per launch (from HBM), not the host's rate of
+            # issuing them
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=sess.side):
+                for r in range(R):
+                    launch(r, torch.cuda.current_stream())
+            reps = max(3, -(-Kp // R))
+            g.replay()
+            torch.cuda.synchronize()
+            ka.record(sess.side)
+            with torch.cuda.stream(sess.side):
+                for _ in range(reps):
+                    g.replay()
             kb.record(sess.side)
-        torch.cuda.synchronize()
-        kms = ka.elapsed_time(kb) / Kp
+            torch.cuda.synchronize()
+            kms = ka.elapsed_time(kb) / (reps * R)
+            del g
+        else:
+            with torch.cuda.stream(sess.side):
+                for r in range(Kp + 3):
+                    if r == 3:
+                        ka.record(sess.side)
+                    launch(r, sess.side)
+                kb.record(sess.side)
+            torch.cuda.synchronize()
+            kms = ka.elapsed_time(kb) / Kp
         kernel_only = {"value": round(fused_bytes / (kms * 1e-3) / 1e9, 1), "unit": "GB/s", "us_per_step": round(kms * 1e3, 1),
-                       "frac_of_measured_peak": round(fused_bytes / (kms * 1e-3) / 1e9 / peak, 4)}
+                       "frac_of_measured_peak": round(fused_bytes / (kms * 1e-3) / 1e9 / peak, 4),
+                       "timing": (f"CUDA graph of {R} launches (one per input copy) replayed, GPU time per launch"
+                                  if R > 1 else "launches back to back on the side stream")}
 
     # end to end: pinned host buffers in, reduced main_grad out, through the public API
     e2e = None
