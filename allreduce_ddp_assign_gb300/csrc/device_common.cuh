@@ -39,6 +39,7 @@ struct Ctx {
     int64_t stride;     // elements between replicas of mg
     int32_t mg_vec;     // every replica of mg is 16-byte aligned
     int32_t wire;       // ring arithmetic type: DDP_F32, or DDP_BF16 / DDP_F16 (compression hook)
+    int64_t per_cta;    // > 0: every CTA takes at most this many elements of one piece (set by the launcher)
 };
 
 struct PieceShared {

@@ -264,6 +264,31 @@ struct SegCache {
     int32_t par[kSegCache];
 };
 
+// Exclusive prefix sum over the block's threads (one value each); *total gets the sum.
+// Contains two block-wide barriers.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total)
+{
+    __shared__ int warp_sum[kThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    int base = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        base += (w < warp) ? warp_sum[w] : 0;
+        all += warp_sum[w];
+    }
+    __syncthreads();
+    *total = all;
+    return base + x - v;
+}
+
 template <int OP, int WT, int DT>
 __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
 {
@@ -271,10 +296,10 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
     __shared__ SegCache sc;
     const int64_t G = gridDim.x;
     const int64_t blk = blockIdx.x;
-    // this CTA's slice of the bucket, boundaries on 16-element multiples
+    // uniform split: this CTA's slice of the bucket, boundaries on 16-element multiples
     const int64_t lo = (blk * cx.n / G) & ~int64_t(15);
     const int64_t hi = (blk + 1 == G) ? cx.n : (((blk + 1) * cx.n / G) & ~int64_t(15));
-    if (lo >= hi) return;  // whole CTA: no barrier is skipped by part of it
+    if (cx.per_cta == 0 && lo >= hi) return;  // whole CTA: no barrier is skipped by part of it
 
     const bool cached = cx.seg_offset && cx.nseg <= kSegCache;
     if (cached) {
@@ -286,6 +311,58 @@ __global__ void __launch_bounds__(kThreads) bucket_kernel(const Ctx cx)
     }
     auto seg_off = [&](int i) -> int64_t { return cached ? sc.off[i] : cx.seg_offset[i]; };
     auto seg_par = [&](int i) -> int { return cached ? sc.par[i] : cx.seg_param[i]; };
+
+    if (cx.per_cta > 0 && cached) {
+        // One piece part per CTA: interval s (segment s, or s == nseg: the padding
+        // after the last gradient) is cut at ring-chunk ends into pieces, and piece
+        // i gets ceil(len_i / per_cta) CTAs.  A CTA then waits on one round of pointer
+        // loads and one of data, never on a second piece's.
+        __shared__ int first_cta[kSegCache + 2];
+        const int nint = cx.nseg + 1;
+        // visit(s, f): the pieces of interval s in order, f(chunk, start, end, ctas)
+        // returning true to stop
+        auto visit = [&](int s, auto&& f) {
+            const int64_t lo_s = seg_off(s), hi_s = (s < cx.nseg) ? seg_off(s + 1) : cx.n;
+            for (int64_t x = lo_s; x < hi_s;) {
+                int c = static_cast<int>(x / cx.chunk);
+                if (c >= cx.nchunks) c = cx.nchunks - 1;
+                const int64_t y = (c + 1 < cx.nchunks) ? lmin(hi_s, static_cast<int64_t>(c + 1) * cx.chunk) : hi_s;
+                if (f(c, x, y, static_cast<int>((y - x + cx.per_cta - 1) / cx.per_cta))) return;
+                x = y;
+            }
+        };
+        int count = 0;
+        if (static_cast<int>(threadIdx.x) < nint)
+            visit(threadIdx.x, [&](int, int64_t, int64_t, int k) { count += k; return false; });
+        int total = 0;
+        const int first = block_exclusive_scan(count, &total);
+        if (static_cast<int>(threadIdx.x) < nint) first_cta[threadIdx.x] = first;
+        __syncthreads();
+        const int b = blockIdx.x;
+        if (b >= total) return;  // whole CTA: a spare one
+        int lo_i = 0, hi_i = nint;  // last interval whose first CTA is <= b
+        while (hi_i - lo_i > 1) {
+            const int mid = (lo_i + hi_i) >> 1;
+            if (first_cta[mid] <= b) lo_i = mid; else hi_i = mid;
+        }
+        const int s = lo_i;
+        int j = b - first_cta[s];
+        int pc = 0;
+        int64_t pa = 0, pb = 0;
+        visit(s, [&](int c, int64_t x, int64_t y, int k) {
+            if (j >= k) {
+                j -= k;
+                return false;
+            }
+            pc = c;
+            pa = x + static_cast<int64_t>(j) * cx.per_cta;
+            pb = lmin(y, pa + cx.per_cta);
+            return true;
+        });
+        if (pb > pa)
+            process_piece<OP, WT, DT>(cx, sh, pc, (s < cx.nseg) ? seg_par(s) : -1, seg_off(s), pa, pb);
+        return;
+    }
 
     int c = static_cast<int>(lo / cx.chunk);
     if (c >= cx.nchunks) c = cx.nchunks - 1;
@@ -341,8 +418,21 @@ ddp_status launch_instance(const Ctx& cx, void* stream)
     int64_t want = (cx.n + kMinElemsPerCta - 1) / kMinElemsPerCta;
     if (cx.nchunks > 1) want = std::max<int64_t>(want, std::min<int64_t>(cx.nchunks, (cx.n + 15) / 16));
     const int64_t room = static_cast<int64_t>(ddp::device_sm_count()) * blocks_per_sm;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min(want, room)));
-    kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(cx);
+    int grid = static_cast<int>(std::max<int64_t>(1, std::min(want, room)));
+    Ctx c = cx;
+    c.per_cta = 0;
+    // a bucket whose segment table the CTAs copy into shared memory gets one piece
+    // part per CTA, when a wave has room for a CTA per piece besides the elements:
+    // the pieces number at most nseg + 1 (the padding) + nchunks - 1, and each adds
+    // at most one partly filled CTA to ceil(n / per_cta)
+    const int64_t extra = static_cast<int64_t>(cx.nseg) + cx.nchunks;
+    if (cx.seg_offset && cx.nseg < kSegCache && cx.n > 0 && room > 2 * extra) {
+        int64_t per = std::max<int64_t>(kMinElemsPerCta, (cx.n + room - extra - 1) / (room - extra));
+        per = (per + 15) & ~int64_t(15);
+        c.per_cta = per;
+        grid = static_cast<int>(std::min<int64_t>(room, (cx.n + per - 1) / per + extra));
+    }
+    kern<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(c);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return ddp::fail(DDP_E_CUDA, "kernel launch failed: %s", cudaGetErrorString(err));
     return ddp::ok();
