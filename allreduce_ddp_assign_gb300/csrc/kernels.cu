@@ -29,6 +29,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <type_traits>
 #include <vector>
 
 #include "common.h"
@@ -127,7 +128,43 @@ __device__ __forceinline__ void run_range(const Ctx& cx, const PieceShared& sh, 
                     acc[u] = (k == 0) ? t : ring_add(acc[u], t, cx.wire);
                 }
             };
-            if constexpr (WT > 0) {
+            if constexpr (WT > 0 && OP == OP_FUSED) {
+                // every replica's values first, then the ring's arithmetic: the W x U
+                // loads are all in flight together instead of one replica's at a time
+                T val[WT][U];
+                auto load_all = [&](auto accumulate) {
+#pragma unroll
+                    for (int k = 0; k < WT; ++k) {
+                        int r = c + 1 + k;
+                        if (r >= WT) r -= WT;
+                        const void* src = sh.src[r];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            if (!live[u]) {
+                                val[k][u] = L::zero();
+                                continue;
+                            }
+                            if constexpr (decltype(accumulate)::value) {
+                                const T m = M::ld(cx.mg + r * cx.stride + e[u]);
+                                val[k][u] = src ? L::add(m, L::template ldg<DT>(src, e[u] - off)) : m;
+                            } else {
+                                val[k][u] = src ? L::template ldg<DT>(src, e[u] - off) : L::zero();
+                            }
+                        }
+                    }
+                };
+                if (cx.accumulate)
+                    load_all(std::true_type{});
+                else
+                    load_all(std::false_type{});
+#pragma unroll
+                for (int k = 0; k < WT; ++k)
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const T t = ring_term(val[k][u], cx.inv_w, static_cast<float>(WT), cx.wire);
+                        acc[u] = (k == 0) ? t : ring_add(acc[u], t, cx.wire);
+                    }
+            } else if constexpr (WT > 0) {
 #pragma unroll
                 for (int k = 0; k < WT; ++k) term(k);
             } else {
