@@ -77,6 +77,7 @@ class State:
     iter: int = 0
     error: list = field(default_factory=list)   # error[w][t]: M x N float64 (None for 1-D)
     cond: dict = field(default_factory=dict)    # per tensor: 2-norm condition number of the last P (for tolerances)
+    amp: dict = field(default_factory=dict)     # per tensor: product condition of the last step (for tolerances)
 
     def __post_init__(self):
         if not self.error:
@@ -100,6 +101,20 @@ def _orthonormal(p: np.ndarray) -> np.ndarray:
     qm = qm * np.where(d < 0, -1.0, 1.0)
     qm[:, d == 0] = 0.0
     return qm
+
+
+def product_condition(a_list, b) -> float:
+    """max |sum_w |A_w| |B|| / max |sum_w A_w B|, at least 1: how far the entries of
+    the summed product sit below the sums of their terms' magnitudes.  A float
+    product obeys |fl(A B) - A B| <= gamma_n |A| |B| entrywise (Higham, Accuracy and
+    Stability of Numerical Algorithms, 2nd ed., section 3.5), so its error relative
+    to max |A B| is this ratio times the summation's growth factor.  Diagnostic for
+    tolerances only: it changes nothing the step computes."""
+    num = np.abs(sum(np.abs(a) @ np.abs(b) for a in a_list)).max(initial=0.0)
+    den = np.abs(sum(a @ b for a in a_list)).max(initial=0.0)
+    if den == 0.0:
+        return 1.0
+    return max(1.0, float(num / den))
 
 
 def step(state: State, bucket: np.ndarray, seg_offset, orc) -> np.ndarray:
@@ -140,8 +155,10 @@ def step(state: State, bucket: np.ndarray, seg_offset, orc) -> np.ndarray:
         p = sum(mw[w] @ q for w in range(W))
         sv = np.linalg.svd(p, compute_uv=False)
         state.cond[t] = float(sv[0] / sv[-1]) if sv[-1] > 0 else float("inf")
+        amp_p = product_condition(mw, q)
         p = _orthonormal(p)
         qn = sum(mw[w].T @ p for w in range(W)) / W
+        state.amp[t] = max(amp_p, product_condition([x.T for x in mw], p))
         approx = p @ qn.T
         for w in range(W):
             out[w, lo:lo + m * n] = approx.reshape(-1)

@@ -176,4 +176,30 @@ def pin_psgd_zero_gradient(orc, psgd):
     assert np.all(out == 0) and not np.any(st.error[0][0]) and not np.any(np.isnan(st.q[0]))
 
 
+def pin_psgd_product_condition(orc, psgd):
+    """The tolerance diagnostic: exactly 1 without cancellation (nonnegative
+    factors), the hand-computed ratio on a 1 x 2 times 2 x 1 product with one
+    cancelling pair, and the max over the P and Q products after a step."""
+    rng = np.random.default_rng(57)
+    a = [np.abs(rng.standard_normal((4, 6))) for _ in range(3)]
+    b = np.abs(rng.standard_normal((6, 2)))
+    assert psgd.product_condition(a, b) == 1.0
+    # [1, -0.75] . [1, 1]: terms 1 and -0.75, sum 0.25 -> ratio 1.75 / 0.25 = 7
+    assert psgd.product_condition([np.array([[1.0, -0.75]])], np.array([[1.0], [1.0]])) == 7.0
+    assert psgd.product_condition([np.zeros((2, 2))], np.ones((2, 1))) == 1.0
+    W, m, n, r = 2, 3, 5, 2
+    g = [[_dyadic(rng, (m, n))] for _ in range(W)]
+    bk, offs, shapes = _bucket(g, W)
+    q0 = rng.standard_normal((n, r))
+    st = psgd.make_state(shapes, W, r, [q0], error_feedback=False)
+    psgd.step(st, bk, offs, orc)
+    mw = [x[0].astype(np.float64) for x in g]
+    p = sum(x @ q0 for x in mw)
+    basis = _chol_basis(p)
+    want = max(np.abs(sum(np.abs(x) @ np.abs(q0) for x in mw)).max() / np.abs(p).max(),
+               np.abs(sum(np.abs(x.T) @ np.abs(basis) for x in mw)).max() / np.abs(sum(x.T @ basis for x in mw)).max(),
+               1.0)
+    assert abs(st.amp[0] - want) <= 1e-9 * want
+
+
 POWERSGD_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_psgd_")]
