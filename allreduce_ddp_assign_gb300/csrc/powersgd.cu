@@ -10,12 +10,14 @@
 //
 // Kernels per compressed iteration (one launch each, over every tensor of the
 // bucket through tile tables built on the host):
-//   psgd_p_kernel       per (row, group of replicas): M = G + E (stored back into
-//                       E), P_w[row] = M[row, :] Q; the sum over replicas; the
-//                       tile's share of P^T P in fp64.  Extra blocks take the
-//                       1-D tensors: ring-ordered mean over their concatenation
-//   psgd_orth_kernel    per tensor: P^T P from the tiles' shares, its Cholesky
-//                       factor R, and P <- P R^-1
+//   psgd_p_kernel       per (row, group of replicas, column split): M = G + E
+//                       (stored back into E), P_w[row] = M[row, split] Q[split];
+//                       the sum over replicas, one partial P per split.  Extra
+//                       blocks take the 1-D tensors: ring-ordered mean over
+//                       their concatenation
+//   psgd_orth_kernel    per tensor: P = the splits' partials added in order,
+//                       P^T P in float pairs (compensated), its Cholesky factor
+//                       R in fp64, and P <- P R^-1
 //   psgd_qpart_kernel   per (column block, row split, replica): partial M^T P,
 //                       the split's rows shared by the block's warps; the last
 //                       block of a column block sums the partials in a fixed
@@ -47,20 +49,38 @@ namespace {
 #define DDP_PSGD_P_BLOCKS 1   // resident blocks per SM the P pass is compiled for
 #endif
 #ifndef DDP_PSGD_Q_BLOCKS
-#define DDP_PSGD_Q_BLOCKS 1   // resident blocks per SM the Q pass is compiled for
+#define DDP_PSGD_Q_BLOCKS 3   // resident blocks per SM the Q pass is compiled for
 #endif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsOut = kWarps;       // rows per output tile: one per warp
-constexpr int kRowsPerSplit = 256;     // rows of one partial M^T P
+#ifndef DDP_PSGD_Q_WAVE
+#define DDP_PSGD_Q_WAVE 0   // 1: the Q launch is one wave of blocks looping over the tiles (0: a block per tile)
+#endif
+#ifndef DDP_PSGD_QROWS
+#define DDP_PSGD_QROWS 256
+#endif
+constexpr int kRowsPerSplit = DDP_PSGD_QROWS;   // rows of one partial M^T P
 constexpr int kMaxPairs = 256;         // (row, replica) pairs per P tile
 constexpr int kMaxRowsP = 16;          // rows per P tile
+#ifndef DDP_PSGD_PCOLS
+#define DDP_PSGD_PCOLS 1024
+#endif
+constexpr int kPCols = DDP_PSGD_PCOLS;  // longest column split of a P tile (a multiple of 128)
+// Rank 8 holds 148 registers a thread in the P pass (one block per SM): twice the split
+// there, so that a matrix's tiles still fit the fewer resident blocks.
+constexpr int p_cols(int rp) { return rp >= 8 ? 2 * kPCols : kPCols; }
+// The Q pass at rank 8 needs more than the 80 registers three blocks per SM allow.
+constexpr int q_min_blocks(int rp) { return rp >= 8 ? 2 : DDP_PSGD_Q_BLOCKS; }
 #ifndef DDP_PSGD_GW
 #define DDP_PSGD_GW 4
 #endif
 constexpr int kGW = DDP_PSGD_GW;       // replicas a warp carries at once in the P pass
 constexpr int kOutBatch = 8;           // replicas whose error loads the output pass issues together
-constexpr int kOutQuads = 2048;        // 16-byte quads per flat output tile
+#ifndef DDP_PSGD_OUTQ
+#define DDP_PSGD_OUTQ 2048
+#endif
+constexpr int kOutQuads = DDP_PSGD_OUTQ;   // 16-byte quads per flat output tile
 constexpr int64_t kVecPiece = 16384;   // elements of a 1-D tensor per block
 
 struct PsgdMat {
@@ -73,8 +93,9 @@ struct PsgdMat {
     int32_t vec;     // offset and N are multiples of 4 (16-byte rows when the buffers are aligned)
     int32_t S;       // row splits of M^T P
     int32_t cbw;     // column block width of M^T P (128 on the 16-byte path, 32 otherwise)
-    int32_t pt0;     // first P tile of the tensor (its shares of P^T P follow in tile order)
-    int32_t ntp;     // P tiles of the tensor
+    int32_t psp;     // column splits of the P pass (their partial sums of P follow in split order)
+    int32_t pcw;     // columns of one split (a multiple of 128 unless the split is the whole row)
+    int64_t ps_off;  // into the partial sums of P: psp x M x RP
     int32_t cnt0;    // first completion counter (one per column block)
     int32_t pad;
 };
@@ -93,13 +114,14 @@ struct PsgdArgs {
     float* P;
     float* Q;
     float* QP;
-    double* GR;       // per P tile: its share of P^T P (upper triangle, row-major)
+    float* PS;        // per tensor and column split: the replica-summed partial P
     int* CNT;         // per column block: blocks of the Q pass finished
     const PsgdMat* mats;
     const int4* tiles;
     const PsgdVec* vecs;
     int32_t n_ptiles; // blocks of the P launch past this take the 1-D tensors
     int32_t n_otiles; // output tiles (the output launch's blocks loop over them)
+    int32_t n_qtiles; // Q-pass tiles (the Q launch's blocks loop over them)
     int32_t ncnt;
     int32_t W;
     int32_t ef;
@@ -153,15 +175,15 @@ __device__ void vec_piece(const PsgdArgs& a, const PsgdVec v)
 }
 
 // ---------------------------------------------------------------------------
-// P = sum_w (G_w + E_w) Q  (tile: {mat, row0, nrows}; one warp per row and
-// group of up to kGW replicas, which share the loads of Q)
+// P = sum_w (G_w + E_w) Q  (tile: {mat, row0, nrows, column split}; one warp per
+// row and group of up to kGW replicas, which share the loads of Q).  A tile sums
+// its columns [split * pcw, +pcw) into the split's partial P; the
+// orthonormalisation adds the splits.
 // ---------------------------------------------------------------------------
 template <int RP>
 __global__ void __launch_bounds__(kThreads, DDP_PSGD_P_BLOCKS) psgd_p_kernel(const PsgdArgs a)
 {
-    constexpr int NG = RP * (RP + 1) / 2;
     __shared__ float part[kMaxPairs][RP];
-    __shared__ float prow[kMaxRowsP][RP];
     if (static_cast<int>(blockIdx.x) >= a.n_ptiles) {
         vec_piece(a, a.vecs[blockIdx.x - a.n_ptiles]);
         return;
@@ -175,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, DDP_PSGD_P_BLOCKS) psgd_p_kernel(con
     const int units = t.z * ngroups;
     const bool vec = m.vec && a.vec_ok;
     const float* q = a.Q + m.q_off;
+    const int c0 = t.w * m.pcw, c1 = min(m.N, c0 + m.pcw);
     for (int u = warp; u < units; u += kWarps) {
         const int rl = u / ngroups, w0 = (u % ngroups) * kGW;
         const int gw = min(kGW, a.W - w0);
@@ -193,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, DDP_PSGD_P_BLOCKS) psgd_p_kernel(con
 #pragma unroll
             for (int r = 0; r < RP; ++r) acc[k][r] = 0.f;
         if (vec) {
-            for (int j = 4 * lane; j < m.N; j += 128) {
+            for (int j = c0 + 4 * lane; j < c1; j += 128) {
                 // every load of the step first (stores to E would otherwise keep the
                 // next replica's loads from being issued early), then the sums
                 float4 x[kGW], y[kGW];
@@ -226,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, DDP_PSGD_P_BLOCKS) psgd_p_kernel(con
                 }
             }
         } else {
-            for (int j = lane; j < m.N; j += 32) {
+            for (int j = c0 + lane; j < c1; j += 32) {
                 float qv[RP];
                 load_row<RP>(q + static_cast<int64_t>(j) * RP, qv);
 #pragma unroll
@@ -257,31 +280,53 @@ __global__ void __launch_bounds__(kThreads, DDP_PSGD_P_BLOCKS) psgd_p_kernel(con
     }
     __syncthreads();
     // the all-reduce of P: replicas summed in order 0 .. W-1
+    float* ps = a.PS + m.ps_off + (static_cast<int64_t>(t.w) * m.M + t.y) * RP;
     for (int k = threadIdx.x; k < t.z * RP; k += kThreads) {
         const int rl = k / RP, r = k % RP;
         float s = 0.f;
         for (int w = 0; w < a.W; ++w) s = __fadd_rn(s, part[rl * a.W + w][r]);
-        a.P[m.p_off + static_cast<int64_t>(t.y + rl) * RP + r] = s;
-        prow[rl][r] = s;
-    }
-    __syncthreads();
-    // this tile's share of P^T P (fp32 products are exact in fp64)
-    if (threadIdx.x < NG) {
-        int c = 0, k = threadIdx.x;
-        while (k >= RP - c) {
-            k -= RP - c;
-            ++c;
-        }
-        const int d = c + k;
-        double s = 0.0;
-        for (int rl = 0; rl < t.z; ++rl) s += static_cast<double>(prow[rl][c]) * prow[rl][d];
-        a.GR[static_cast<int64_t>(blockIdx.x) * NG + threadIdx.x] = s;
+        ps[k] = s;
     }
 }
 
 // ---------------------------------------------------------------------------
-// orthonormal columns of P (one block per tensor): P^T P summed from the P
-// tiles' shares in a fixed order, its Cholesky factor R (upper triangular,
+// P^T P in pairs of floats (this GPU's fp64 rate is a small fraction of its fp32
+// rate): each sum is carried as hi + lo with the error-free transformations
+// TwoSum (Knuth) and TwoProduct (one fused multiply-add), the compensated dot
+// product Dot2 of Ogita, Rump and Oishi ("Accurate sum and dot product", SIAM
+// J. Sci. Comput. 26(6), 2005), which is as accurate as a sum in twice the
+// working precision; partial pairs are merged the same way.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e)
+{
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// (hi, lo) += x * y
+__device__ __forceinline__ void dot2_add(float& hi, float& lo, float x, float y)
+{
+    const float h = __fmul_rn(x, y);
+    const float r = __fmaf_rn(x, y, -h);   // x * y = h + r exactly
+    float s, q;
+    two_sum(hi, h, s, q);
+    hi = s;
+    lo = __fadd_rn(lo, __fadd_rn(q, r));
+}
+
+// (hi, lo) += (hi2, lo2)
+__device__ __forceinline__ void dot2_merge(float& hi, float& lo, float hi2, float lo2)
+{
+    float s, q;
+    two_sum(hi, hi2, s, q);
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, lo2), q);
+}
+
+// ---------------------------------------------------------------------------
+// orthonormal columns of P (one block per tensor): P from the column splits'
+// partial sums, P^T P summed over its rows in a fixed order, its Cholesky factor R (upper triangular,
 // positive diagonal) and R^-1 on one thread, then P <- P R^-1 -- the
 // orthonormal basis whose triangle has a positive diagonal.  A column whose
 // pivot is not positive (zero, or in the span of the earlier columns) becomes 0.
@@ -290,32 +335,47 @@ template <int RP>
 __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
 {
     constexpr int NG = RP * (RP + 1) / 2;
-    __shared__ double red[kWarps][NG];
+    __shared__ float2 red[kWarps][NG];
     __shared__ double gsum[NG];
     __shared__ float rinv[RP][RP];
     const PsgdMat m = a.mats[blockIdx.x];
     float* p = a.P + m.p_off;
-    {   // the tiles' shares: thread i adds tiles i, i + 256, ...; then a fixed tree over the block
+    {   // P = the column splits' partial sums added in split order; P^T P from the rows
+        // as float pairs: thread i takes rows i, i + 256, ..., then a fixed tree over
+        // the block (lanes, then warps in order)
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        double g[NG];
+        const float* ps = a.PS + m.ps_off;
+        const int64_t plane = static_cast<int64_t>(m.M) * RP;
+        float ghi[NG], glo[NG];
 #pragma unroll
-        for (int k = 0; k < NG; ++k) g[k] = 0.0;
-        for (int t = threadIdx.x; t < m.ntp; t += kThreads) {
-            const double* src = a.GR + static_cast<int64_t>(m.pt0 + t) * NG;
+        for (int k = 0; k < NG; ++k) ghi[k] = glo[k] = 0.f;
+        for (int i = threadIdx.x; i < m.M; i += kThreads) {
+            float x[RP];
 #pragma unroll
-            for (int k = 0; k < NG; ++k) g[k] += src[k];
+            for (int r = 0; r < RP; ++r) x[r] = ps[static_cast<int64_t>(i) * RP + r];
+            for (int c = 1; c < m.psp; ++c)
+#pragma unroll
+                for (int r = 0; r < RP; ++r) x[r] = __fadd_rn(x[r], ps[c * plane + static_cast<int64_t>(i) * RP + r]);
+#pragma unroll
+            for (int r = 0; r < RP; ++r) p[static_cast<int64_t>(i) * RP + r] = x[r];
+            int k = 0;
+#pragma unroll
+            for (int c = 0; c < RP; ++c)
+#pragma unroll
+                for (int d = c; d < RP; ++d, ++k) dot2_add(ghi[k], glo[k], x[c], x[d]);
         }
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
 #pragma unroll
-            for (int o = 16; o; o >>= 1) g[k] += __shfl_xor_sync(0xffffffffu, g[k], o);
-            if (lane == 0) red[warp][k] = g[k];
+            for (int o = 16; o; o >>= 1)
+                dot2_merge(ghi[k], glo[k], __shfl_xor_sync(0xffffffffu, ghi[k], o), __shfl_xor_sync(0xffffffffu, glo[k], o));
+            if (lane == 0) red[warp][k] = make_float2(ghi[k], glo[k]);
         }
         __syncthreads();
         if (threadIdx.x < NG) {
-            double s = 0.0;
-            for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
-            gsum[threadIdx.x] = s;
+            float hi = red[0][threadIdx.x].x, lo = red[0][threadIdx.x].y;
+            for (int w = 1; w < kWarps; ++w) dot2_merge(hi, lo, red[w][threadIdx.x].x, red[w][threadIdx.x].y);
+            gsum[threadIdx.x] = static_cast<double>(hi) + static_cast<double>(lo);
         }
     }
     __syncthreads();
@@ -343,8 +403,8 @@ __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
             for (int q = 0; q < c; ++q)
                 if (ok[q]) d -= R[q][c] * R[q][c];
             ok[c] = c < m.r && d > 0.0;
-            const double rc = ok[c] ? sqrt(d) : 1.0;
-            const double inv = 1.0 / rc;
+            const double inv = ok[c] ? rsqrt(d) : 1.0;
+            const double rc = ok[c] ? d * inv : 1.0;
             R[c][c] = ok[c] ? rc : 0.0;
 #pragma unroll
             for (int e = c + 1; e < RP; ++e) {
@@ -397,11 +457,8 @@ __global__ void __launch_bounds__(kThreads) psgd_orth_kernel(const PsgdArgs a)
 // partials in the order (replica, split) and writes Q = sum / W.
 // ---------------------------------------------------------------------------
 template <int RP>
-__global__ void __launch_bounds__(kThreads, DDP_PSGD_Q_BLOCKS) psgd_qpart_kernel(const PsgdArgs a)
+__device__ __forceinline__ void qpart_tile(const PsgdArgs& a, const int4 t, float (&red)[kWarps][128 * RP], int& last)
 {
-    __shared__ float red[kWarps][128 * RP];
-    __shared__ int last;
-    const int4 t = a.tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const PsgdMat m = a.mats[t.x];
     const int u = t.z;
@@ -470,28 +527,50 @@ __global__ void __launch_bounds__(kThreads, DDP_PSGD_Q_BLOCKS) psgd_qpart_kernel
     __syncthreads();
     if (threadIdx.x == 0) last = atomicAdd(a.CNT + m.cnt0 + t.y, 1) == m.S * a.W - 1;
     __syncthreads();
-    if (!last) return;
+    if (!last) return;   // uniform over the block
     __threadfence();
     const int64_t plane = static_cast<int64_t>(m.N) * RP;
     const float wf = static_cast<float>(a.W);
     for (int k = threadIdx.x; k < ncol * RP; k += kThreads) {
         const int64_t el = static_cast<int64_t>(c0) * RP + k;
-        float tot = 0.f;
-        for (int ww = 0; ww < a.W; ++ww) {
-            float qw = 0.f;
-            for (int s0 = 0; s0 < m.S; s0 += 8) {   // eight loads in flight, added in split order
-                float v[8];
+        // partial (replica ww, split s) is term ww * S + s: sixteen loads in flight,
+        // each replica's splits added in order, then the replicas in order
+        float tot = 0.f, qw = 0.f;
+        const int nterm = a.W * m.S;
+        for (int j0 = 0; j0 < nterm; j0 += 16) {
+            float v[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    v[j] = s0 + j < m.S ? __ldcg(a.QP + m.qp_off + (static_cast<int64_t>(s0 + j) * a.W + ww) * plane + el) : 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (s0 + j < m.S) qw = __fadd_rn(qw, v[j]);
+            for (int j = 0; j < 16; ++j) {
+                const int tj = j0 + j;
+                v[j] = tj < nterm
+                           ? __ldcg(a.QP + m.qp_off + (static_cast<int64_t>(tj % m.S) * a.W + tj / m.S) * plane + el)
+                           : 0.f;
             }
-            tot = __fadd_rn(tot, qw);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int tj = j0 + j;
+                if (tj < nterm) {
+                    qw = __fadd_rn(qw, v[j]);
+                    if (tj % m.S == m.S - 1) {
+                        tot = __fadd_rn(tot, qw);
+                        qw = 0.f;
+                    }
+                }
+            }
         }
         a.Q[m.q_off + el] = __fdiv_rn(tot, wf);
     }
+}
+
+// One wave of blocks looping over the tiles (in table order: a block's next tile
+// is gridDim.x further on).  The block-wide barriers inside a tile order the
+// reuse of red and last across tiles.
+template <int RP>
+__global__ void __launch_bounds__(kThreads, q_min_blocks(RP)) psgd_qpart_kernel(const PsgdArgs a)
+{
+    __shared__ float red[kWarps][128 * RP];
+    __shared__ int last;
+    for (int i = blockIdx.x; i < a.n_qtiles; i += gridDim.x) qpart_tile<RP>(a, a.tiles[i], red, last);
 }
 
 // ---------------------------------------------------------------------------
@@ -624,10 +703,10 @@ struct ddp_powersgd {
     int64_t nvec = 0;
     std::vector<int4> t_p, t_q, t_o;
     int32_t rows_p = 1, ncnt = 0;
-    int64_t q_elems = 0, p_elems = 0, qp_elems = 0;
+    int64_t q_elems = 0, p_elems = 0, qp_elems = 0, ps_elems = 0;
     // workspace: the tables, then the scratch (offsets from the scratch's start)
     size_t off_mats = 0, off_tp = 0, off_tq = 0, off_to = 0, off_vecs = 0, off_scratch = 0;
-    size_t s_P = 0, s_QP = 0, s_GR = 0, s_CNT = 0, scratch_bytes = 0;
+    size_t s_P = 0, s_QP = 0, s_PS = 0, s_CNT = 0, scratch_bytes = 0;
     size_t ws_bytes = 0;
     // bound buffers
     uint8_t* ws = nullptr;
@@ -648,7 +727,7 @@ PsgdArgs make_args(const ddp_powersgd& h, uint8_t* scratch, float* main_grad, in
     a.estride = h.estride;
     a.P = reinterpret_cast<float*>(scratch + h.s_P);
     a.QP = reinterpret_cast<float*>(scratch + h.s_QP);
-    a.GR = reinterpret_cast<double*>(scratch + h.s_GR);
+    a.PS = reinterpret_cast<float*>(scratch + h.s_PS);
     a.CNT = reinterpret_cast<int*>(scratch + h.s_CNT);
     a.Q = h.q;
     a.mats = reinterpret_cast<const PsgdMat*>(h.ws + h.off_mats);
@@ -664,21 +743,34 @@ PsgdArgs make_args(const ddp_powersgd& h, uint8_t* scratch, float* main_grad, in
     return a;
 }
 
-// Blocks of the output launch: one wave (SMs x resident blocks of the kernel).
-template <int RP>
-size_t out_blocks()
+// Blocks of one wave of a kernel (SMs x its resident blocks), cached per device
+// and kernel (`cached` is the kernel's own array).
+template <typename Kernel>
+size_t wave_blocks(Kernel kernel, std::atomic<int> (&cached)[ddp::kMaxDevices])
 {
-    static std::atomic<int> cached[ddp::kMaxDevices] = {};
     const int dev = ddp::current_device();
     int n = dev >= 0 ? cached[dev].load(std::memory_order_relaxed) : 0;
     if (!n) {
         int v = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, psgd_out_kernel<RP>, kThreads, 0) != cudaSuccess || v < 1)
-            v = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, kThreads, 0) != cudaSuccess || v < 1) v = 1;
         n = ddp::device_sm_count() * v;
         if (dev >= 0) cached[dev].store(n, std::memory_order_relaxed);
     }
     return static_cast<size_t>(n);
+}
+
+template <int RP>
+size_t out_blocks()
+{
+    static std::atomic<int> cached[ddp::kMaxDevices] = {};
+    return wave_blocks(psgd_out_kernel<RP>, cached);
+}
+
+template <int RP>
+size_t q_blocks()
+{
+    static std::atomic<int> cached[ddp::kMaxDevices] = {};
+    return wave_blocks(psgd_qpart_kernel<RP>, cached);
 }
 
 template <int RP>
@@ -693,7 +785,9 @@ ddp_status launch_all(const ddp_powersgd& h, const PsgdArgs& base, cudaStream_t 
     if (!h.mats.empty()) {
         psgd_orth_kernel<RP><<<static_cast<unsigned>(h.mats.size()), kThreads, 0, s>>>(a);
         a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_tq);
-        psgd_qpart_kernel<RP><<<static_cast<unsigned>(h.t_q.size()), kThreads, 0, s>>>(a);
+        a.n_qtiles = static_cast<int32_t>(h.t_q.size());
+        const size_t qgrid = DDP_PSGD_Q_WAVE ? std::min<size_t>(h.t_q.size(), q_blocks<RP>()) : h.t_q.size();
+        psgd_qpart_kernel<RP><<<static_cast<unsigned>(qgrid), kThreads, 0, s>>>(a);
         a.tiles = reinterpret_cast<const int4*>(h.ws + h.off_to);
         a.n_otiles = static_cast<int32_t>(h.t_o.size());
         psgd_out_kernel<RP><<<static_cast<unsigned>(std::min<size_t>(h.t_o.size(), out_blocks<RP>())), kThreads, 0, s>>>(a);
@@ -780,10 +874,21 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
         m.qp_off = h->qp_elems;
         h->qp_elems += align4(static_cast<int64_t>(m.S) * W * cols * RP);
         const int32_t mi = static_cast<int32_t>(h->mats.size());
-        m.pt0 = static_cast<int32_t>(h->t_p.size());
-        for (int32_t r0 = 0; r0 < m.M; r0 += h->rows_p)
-            h->t_p.push_back(make_int4(mi, r0, std::min(h->rows_p, m.M - r0), 0));
-        m.ntp = static_cast<int32_t>(h->t_p.size()) - m.pt0;
+        // P tiles: rows_p rows by one column split; rows longer than p_cols(RP)
+        // columns are cut into equal splits of whole 128-column blocks
+        m.psp = 1;
+        m.pcw = m.N;
+        const int pcols = p_cols(RP);
+        if (cols > pcols) {
+            const int64_t parts = (cols + pcols - 1) / pcols;
+            m.pcw = static_cast<int32_t>(((cols + parts - 1) / parts + 127) / 128 * 128);
+            m.psp = static_cast<int32_t>((cols + m.pcw - 1) / m.pcw);
+        }
+        m.ps_off = h->ps_elems;
+        h->ps_elems += align4(static_cast<int64_t>(m.psp) * rows * RP);
+        for (int32_t cs = 0; cs < m.psp; ++cs)
+            for (int32_t r0 = 0; r0 < m.M; r0 += h->rows_p)
+                h->t_p.push_back(make_int4(mi, r0, std::min(h->rows_p, m.M - r0), cs));
         const int64_t quads = rows * cols / 4;
         if (m.vec && quads < (int64_t{1} << 31) - kOutQuads) {
             for (int64_t q0 = 0; q0 < quads; q0 += kOutQuads)
@@ -801,7 +906,6 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
         h->seg_mat[t] = mi;
         h->mats.push_back(m);
     }
-    const size_t ng = static_cast<size_t>(RP * (RP + 1) / 2);
     size_t o = 0;
     h->off_mats = o;
     o = align256(o + h->mats.size() * sizeof(PsgdMat));
@@ -819,8 +923,8 @@ extern "C" ddp_status ddp_powersgd_create(int32_t W, int32_t rank, int32_t nseg,
     sc = align256(sc + static_cast<size_t>(h->p_elems) * sizeof(float));
     h->s_QP = sc;
     sc = align256(sc + static_cast<size_t>(h->qp_elems) * sizeof(float));
-    h->s_GR = sc;
-    sc = align256(sc + h->t_p.size() * ng * sizeof(double));
+    h->s_PS = sc;
+    sc = align256(sc + static_cast<size_t>(h->ps_elems) * sizeof(float));
     h->s_CNT = sc;
     sc = align256(sc + static_cast<size_t>(h->ncnt) * sizeof(int));
     h->scratch_bytes = sc;

@@ -399,14 +399,15 @@ ddp_status ddp_used_allreduce(const uint8_t* local_used, int32_t ld, int32_t W, 
  *       every replica's tensor = P Q^T;  E_w = M_w - P Q^T
  * The bucket's padding is left alone once compression starts.  Sums over
  * replicas are taken in replica order; P and Q products accumulate in fp32
- * with fused multiply-adds (P^T P in fp64), so
+ * with fused multiply-adds (P^T P as compensated float pairs, its Cholesky
+ * factor in fp64), so
  * results match an exact evaluation to within rounding, not bit for bit.
  *
  * Memory (all the caller's; the library allocates none):
  *   workspace  DEVICE, ddp_powersgd_sizes bytes, 256-byte aligned: tile
  *              tables (written by ddp_powersgd_bind) and the scratch: P, the
- *              partial sums of Q, the shares of P^T P and completion counters
- *              (all rewritten by every reduce).
+ *              column splits' partial sums of P, the partial sums of Q and
+ *              completion counters (all rewritten by every reduce).
  *   q_state    DEVICE fp32, q_elems: every matrix's Q as N rows of rank_pad
  *              floats (ddp_powersgd_matrix gives the offset); columns past
  *              the effective rank must be 0.  ddp_powersgd_set_q writes one
@@ -473,8 +474,7 @@ ddp_status ddp_powersgd_reduce(ddp_powersgd* h, float* main_grad, int64_t replic
 /*
  * ddp_powersgd_reduce_static -- ddp_powersgd_reduce, allocating nothing and
  * using no caller scratch: the kernels' scratch (the summed P, the partial
- * sums of Q, the blocks' shares of P^T P and the Q pass's completion
- * counters) lives in a fixed device array of DDP_POWERSGD_STATIC_SCRATCH_BYTES
+ * sums of P and of Q and the Q pass's completion counters) lives in a fixed device array of DDP_POWERSGD_STATIC_SCRATCH_BYTES
  * (8 MiB) inside the library.  The pages have no counterpart: this is an
  * entry point of this library for callers that want no scratch allocation at
  * all.  The workspace bound by ddp_powersgd_bind still supplies the tile
