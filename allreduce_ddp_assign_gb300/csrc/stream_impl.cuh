@@ -51,6 +51,9 @@
 #ifndef DDP_STREAM_L2_HINT
 #define DDP_STREAM_L2_HINT 0       // 1: stream operands in with an L2 evict-first policy
 #endif
+#ifndef DDP_STREAM_TAPER
+#define DDP_STREAM_TAPER 2         // > 1: the pool's last stretch in units of unit / DDP_STREAM_TAPER
+#endif
 #ifndef DDP_STREAM_BUDGET2_KB
 #define DDP_STREAM_BUDGET2_KB 110  // shared memory per CTA when two CTAs share an SM
 #endif
@@ -465,15 +468,27 @@ __global__ void __launch_bounds__(kThreadsTma) stream_kernel(const StreamArgs a)
         walk(lo, hi);
         if (a.dyn) {
             // the pool: claim a unit after the previous one's tiles are issued (the
-            // claim's round trip overlaps the stages still queued), until none is left
-            const int64_t nunits = (a.total - a.head + a.unit - 1) / a.unit;
+            // claim's round trip overlaps the stages still queued), until none is left.
+            // The last stretch, one unit per CTA, goes out in units of unit / d
+            // (d = DDP_STREAM_TAPER) where those are still whole tiles, so that the
+            // last claimers finish closer together.
+            const bool taper = DDP_STREAM_TAPER > 1 && a.unit / DDP_STREAM_TAPER >= kTile;
+            const int64_t small = taper ? (a.unit / DDP_STREAM_TAPER) & ~int64_t(15) : a.unit;
+            const int64_t z2 = taper ? lmax(a.head, (a.total - G * a.unit) & ~int64_t(15)) : a.total;
+            const int64_t n1 = (z2 - a.head + a.unit - 1) / a.unit;
+            const int64_t nunits = n1 + (a.total - z2 + small - 1) / small;
             while (ok) {
                 uint32_t u = 0;
                 if (lane == 0) u = atomicAdd(&a.dyn[0], 1u);
                 u = __shfl_sync(kFull, u, 0);
                 if (static_cast<int64_t>(u) >= nunits) break;
-                const int64_t x0 = a.head + static_cast<int64_t>(u) * a.unit;
-                walk(x0, lmin(a.total, x0 + a.unit));
+                if (static_cast<int64_t>(u) < n1) {
+                    const int64_t x0 = a.head + static_cast<int64_t>(u) * a.unit;
+                    walk(x0, lmin(z2, x0 + a.unit));
+                } else {
+                    const int64_t x0 = z2 + (static_cast<int64_t>(u) - n1) * small;
+                    walk(x0, lmin(a.total, x0 + small));
+                }
             }
             // the last CTA to stop claiming clears both counters for the slot's next
             // launch (which the launcher orders after this one)

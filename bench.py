@@ -459,7 +459,13 @@ def run_ours(args, wl):
         pb_ev.record(compute)
         torch.cuda.synchronize()
         pb_value = job_value(1, step_bytes, Kp, pa.elapsed_time(pb_ev))
-        per_bucket_ms = [float(x) for x in pb_sess.bucket_ms()]
+        # each bucket's launch time (events around it on the side stream): the median
+        # over Kp more steps, read back after each step
+        samples = []
+        for _ in range(Kp):
+            pb_step()
+            samples.append([float(x) for x in pb_sess.bucket_ms()])
+        per_bucket_ms = [float(np.median([smp[b] for smp in samples])) for b in range(len(samples[0]))]
         if pb_sess is not sess:
             pb_sess.close()
 
@@ -587,6 +593,7 @@ def run_ours(args, wl):
                        "issue": "coalesced (ready buckets in one launch)" if coalesce else "one launch per bucket",
                        "per_bucket_issue": None if pb_value is None else {
                            "value": round(pb_value, 1), "unit": "GB/s", "steps": Kp,
+                           "per_bucket_timing": f"events around each launch, median of {Kp} steps",
                            "per_bucket_gbs": [round(x[2] / (per_bucket_ms[x[1]] * 1e-3) / 1e9, 1)
                                               if per_bucket_ms[x[1]] > 0 else None for x in fused],
                            "bucket_bytes": [int(x[2]) for x in fused]}},
