@@ -185,6 +185,52 @@ def test_powersgd_long_rows_vs_oracle(orc, W, rank, ef, aligned):
     assert D.ddp_device_status(reset=True) == 0
 
 
+SPLIT_SHAPES = [(7, 1030), (3,), (2, 3001), (9, 2052), (4, 1025), (6, 4104)]
+SPLIT_CASES = [(W, rank, ef, aligned) for W in (2, 5) for rank in (1, 3, 8) for ef in (0, 1)
+               for aligned in (True, False)]
+
+
+@pytest.mark.parametrize("W,rank,ef,aligned", SPLIT_CASES)
+def test_powersgd_column_splits_vs_oracle(orc, W, rank, ef, aligned):
+    """Rows longer than one P tile's column split: lengths that are not multiples of 4
+    (the scalar path), of 128, or of the split count, so the splits end mid-block and
+    the last one is short (2052 and 4104 columns take the 16-byte path when aligned);
+    rank 8 doubles the split width.  Three iterations against the oracle with the same
+    checks and tolerance as the other bucket cases."""
+    rng = np.random.default_rng(9100 + 100 * W + 10 * rank + ef)
+    shapes = SPLIT_SHAPES
+    offs, numel = layout(shapes, pad_to=4 if aligned else 1)
+    stride = numel + (4 - numel % 4) % 4 + (0 if aligned else 1)
+    q0 = q0_of(93, shapes, rank)
+    st = OP.make_state(shapes, W, rank, q0, error_feedback=bool(ef), start_iter=0)
+    from allreduce_ddp_assign_gb300.powersgd import PowerSGDBucket
+
+    hook = PowerSGDBucket(W, rank, offs, [int(np.prod(s)) for s in shapes], shapes, numel,
+                          lambda k, n, r: q0[k], error_feedback=bool(ef), start_iter=0)
+    for it in range(1, 4):
+        host = make_bucket(rng, shapes, W, offs, numel, stride)
+        dev = torch.from_numpy(host).to(DEV)
+        want = OP.step(st, host[:, :numel], offs, orc)
+        hook.reduce(dev, stride)
+        torch.cuda.synchronize()
+        got = dev.cpu().numpy()
+        check_against(st, want, got[:, :numel], shapes, offs, it, f"iteration {it}")
+        for t, s in enumerate(shapes):
+            mv = OP.matrix_view(s)
+            if mv is None:
+                continue
+            qg = hook.q(t).cpu().numpy().astype(np.float64)
+            unit = it * U * max(st.cond[t], 1.0) * st.amp[t]
+            assert np.abs(qg - st.q[t]).max() <= TOL_OUT_Q * unit * max(np.abs(st.q[t]).max(), 1e-30), f"Q of tensor {t}"
+            if ef:
+                for w in range(W):
+                    eg = hook.error_of(w, offs[t], mv[0] * mv[1]).cpu().numpy().astype(np.float64)
+                    er = st.error[w][t].reshape(-1)
+                    scale = max(np.abs(want[w, offs[t]:offs[t] + mv[0] * mv[1]]).max(), np.abs(er).max(), 1e-30)
+                    assert np.abs(eg - er).max() <= TOL_ERR * unit * scale, f"error of tensor {t} replica {w}"
+    hook.close()
+
+
 def test_powersgd_zero_gradients_stay_finite(orc):
     W, rank = 4, 2
     shapes = [(32, 32), (5,)]
