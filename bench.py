@@ -490,6 +490,8 @@ def run_ours(args, wl):
                       + (" (minus the packs it waits for)" if packs else ""))
     achieved = dom_bytes / (kern_ms * 1e-3) / 1e9
     tag = f"{dominant}_{wl.name}"
+    if not coalesce and sess.plan.nbuckets > 1:
+        tag += "_per_bucket"   # other launches than the recorded coalesced one: no traffic record
     traffic = profile_traffic(tag)
 
     # context: the same fused launches back to back on the side stream, without
