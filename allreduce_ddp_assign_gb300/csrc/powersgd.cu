@@ -326,8 +326,8 @@ __device__ __forceinline__ void dot2_merge(float& hi, float& lo, float hi2, floa
 
 // ---------------------------------------------------------------------------
 // orthonormal columns of P (one block per tensor): P from the column splits'
-// partial sums, P^T P summed over its rows in a fixed order, its Cholesky factor R (upper triangular,
-// positive diagonal) and R^-1 on one thread, then P <- P R^-1 -- the
+// partial sums, P^T P summed over its rows in a fixed order, its Cholesky factor
+// R (upper triangular, positive diagonal) and R^-1 on one thread, then P <- P R^-1 -- the
 // orthonormal basis whose triangle has a positive diagonal.  A column whose
 // pivot is not positive (zero, or in the span of the earlier columns) becomes 0.
 // ---------------------------------------------------------------------------
