@@ -871,8 +871,9 @@ void ddp_plan_destroy(ddp_plan* plan);
  * identical results: a static split (equal slices), or a static head (5/8 of
  * the elements for the ring reduction, 3/4 for the launches that read
  * gradients) followed by a pool of units (about 64 KB and 128 KB of staged
- * operands) that CTAs claim one at a time when their slice is done, so that
- * CTAs on faster SMs take more of the tail.  A launch with a pool uses one of 64
+ * operands; the pool's last stretch, one unit per CTA, in half units where
+ * those are whole tiles) that CTAs claim one at a time when their slice is
+ * done, so that CTAs on faster SMs take more of the tail.  A launch with a pool uses one of 64
  * counter slots in the library's own device memory and waits, on its stream,
  * for the previous launch that used the same slot (an event the library
  * records); launches made during stream capture keep the static split.
