@@ -99,6 +99,9 @@ _SIGS = {
     "ddp_device_status": (C.c_int32, [_vp, _i32p, C.c_int32]),
     "ddp_wait_selftest": (C.c_int32, [C.c_int32, C.c_int64, _vp]),
     "ddp_copy_rows": (C.c_int32, [_vp, C.c_int64, _vp, C.c_int64, C.c_int64, C.c_int64, _vp]),
+    "ddp_host_front_create": (C.c_int32, [_vp, _vp, C.c_int64, _i64p, C.c_int32, C.POINTER(_vp)]),
+    "ddp_host_front_step": (C.c_int32, [_vp, _vp, C.c_int64, _vp, _vp]),
+    "ddp_host_front_destroy": (None, [_vp]),
     "ddp_plan_create": (C.c_int32, [_i64p, _i32p, C.c_int32, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int32,
                                     C.c_int64, C.POINTER(_vp)]),
     "ddp_plan_describe": (C.c_int32, [_vp, _vp, _i64p, _i64p, _i32p, _i32p, _i64p, _i32p, _i32p, _i32p, _i64p]),
@@ -550,6 +553,22 @@ def ddp_copy_rows(dst, dst_pitch, src, src_pitch, row_bytes, rows, stream=None) 
     """Pointers (tensors or integer addresses) and pitches in bytes."""
     _check(lib().ddp_copy_rows(_ptr(dst), int(dst_pitch), _ptr(src), int(src_pitch), int(row_bytes), int(rows),
                                _stream(stream)))
+
+
+def ddp_host_front_create(r, dev_in, dev_pitch, param_offset, elem_bytes):
+    """The host-buffer front end of reducer r; dev_in a pointer (or tensor), pitch in bytes."""
+    off = np.ascontiguousarray(param_offset, np.int64)
+    h = _vp()
+    _check(lib().ddp_host_front_create(r, _ptr(dev_in), int(dev_pitch), _cp(off, _i64p), int(elem_bytes), C.byref(h)))
+    return h
+
+
+def ddp_host_front_step(h, host_in, host_pitch, host_out, stream=None) -> None:
+    _check(lib().ddp_host_front_step(h, _ptr(host_in), int(host_pitch), _ptr(host_out), _stream(stream)))
+
+
+def ddp_host_front_destroy(h) -> None:
+    lib().ddp_host_front_destroy(h)
 
 
 def ddp_status_str(s: int) -> str:

@@ -94,6 +94,9 @@ struct ddp_reducer {
 
     std::vector<ddp_powersgd*> hooks;  // per bucket: the PowerSGD hook, or null
     std::vector<cudaEvent_t> bdone;    // per bucket: recorded after its reduction (DDP_R_BUCKET_DONE)
+    // per bucket: one more event its issue waits for, or null (the host front end's
+    // copy of the bucket's previous result to the host; owned by the front end)
+    std::vector<cudaEvent_t> extra_gate;
 
     bool dry() const { return flags & DDP_R_DRY_RUN; }
     uint8_t* host_bitmap() { return dry() ? fu_host_dry.data() : fu_host; }
@@ -172,6 +175,10 @@ struct ddp_reducer {
                 waited.push_back(e);
                 if (!cuda_ok(cudaStreamWaitEvent(side, e, 0), "cudaStreamWaitEvent", &st)) return st;
             }
+        }
+        for (int32_t i = 0; i < count; ++i) {
+            const cudaEvent_t e = extra_gate[order[pos + i]];
+            if (e && !cuda_ok(cudaStreamWaitEvent(side, e, 0), "cudaStreamWaitEvent", &st)) return st;
         }
         const bool timing = flags & DDP_R_TIMING;
         bool hooked = false;
@@ -389,6 +396,7 @@ extern "C" ddp_status ddp_reducer_create(int32_t nparams, int32_t nbuckets, cons
     r->grads_out = grads_out;
     r->global_used = global_used;
     r->side = static_cast<cudaStream_t>(side_stream);
+    r->extra_gate.assign(nbuckets, nullptr);
     r->pending.assign(nbuckets, 0);
     r->marked.assign(nparams, 0);
     r->producers.resize(nbuckets);
@@ -734,4 +742,202 @@ extern "C" ddp_status ddp_copy_rows(void* dst, int64_t dst_pitch, const void* sr
                  "cudaMemcpy2DAsync", &st))
         return st;
     return ddp::ok();
+}
+
+// ---------------------------------------------------------------------------
+// The host-buffer front end: every replica's gradients from pinned host memory
+// to the device, the reducer's iteration, each reduced bucket back to pinned
+// host memory -- as a pipeline over the buckets in issue order ("Megatron DDP:
+// contiguous buffer and overlap" section 3: a consumer starts on a bucket as
+// soon as its reduction is done).  Bucket b's copies to the device go out on
+// one stream and mark its parameters ready; its copy back waits for that
+// bucket alone on a second stream.  Consecutive steps overlap bucket by
+// bucket: step k + 1's copies into bucket b's gradients wait for step k's
+// reduction of bucket b, and its reduction of bucket b for step k's copy of
+// bucket b to the host (a gate the reducer waits for when it issues b).
+// ---------------------------------------------------------------------------
+struct ddp_host_front {
+    ddp_reducer* r = nullptr;
+    uint8_t* dev_in = nullptr;
+    int64_t dev_pitch = 0;
+    int32_t elem = 4;
+    int64_t row_elems = 0;
+    struct Bucket {
+        int32_t b = 0;
+        std::vector<std::pair<int64_t, int64_t>> runs;   // element ranges of a row, contiguous in the host layout
+        std::vector<int32_t> params;                     // in backward order (last parameter first)
+    };
+    std::vector<Bucket> issue;   // in issue order
+    cudaStream_t h2d = nullptr, d2h = nullptr, gate = nullptr;
+    std::vector<cudaEvent_t> reduced, downloaded;   // per issue position
+    cudaEvent_t join = nullptr;
+    bool first = true;
+    std::vector<int32_t> ready;   // scratch: a bucket's parameters still to mark
+
+    void release()
+    {
+        if (r)
+            for (cudaEvent_t& e : r->extra_gate) e = nullptr;
+        for (cudaEvent_t e : reduced)
+            if (e) cudaEventDestroy(e);
+        for (cudaEvent_t e : downloaded)
+            if (e) cudaEventDestroy(e);
+        if (join) cudaEventDestroy(join);
+        if (h2d) cudaStreamDestroy(h2d);
+        if (d2h) cudaStreamDestroy(d2h);
+        if (gate) cudaStreamDestroy(gate);
+    }
+};
+
+namespace {
+
+// `waiter` waits for everything queued on `waited` so far
+bool join_streams(cudaStream_t waiter, cudaStream_t waited, cudaEvent_t ev, ddp_status* st)
+{
+    return cuda_ok(cudaEventRecord(ev, waited), "cudaEventRecord", st) &&
+           cuda_ok(cudaStreamWaitEvent(waiter, ev, 0), "cudaStreamWaitEvent", st);
+}
+
+}  // namespace
+
+extern "C" ddp_status ddp_host_front_create(ddp_reducer* r, void* dev_in, int64_t dev_pitch, const int64_t* param_offset,
+                                            int32_t elem_bytes, ddp_host_front** out)
+{
+    using ddp::fail;
+    const char* fn = "ddp_host_front_create";
+    if (!out) return fail(DDP_E_INVAL, "%s: out is NULL", fn);
+    *out = nullptr;
+    if (!r || !param_offset) return fail(DDP_E_INVAL, "%s: NULL argument", fn);
+    if (r->dry()) return fail(DDP_E_INVAL, "%s: the reducer is a dry run", fn);
+    if (!(r->flags & DDP_R_BUCKET_DONE)) return fail(DDP_E_INVAL, "%s: the reducer needs DDP_R_BUCKET_DONE", fn);
+    if (!r->mg) return fail(DDP_E_INVAL, "%s: the reducer has no main_grad", fn);
+    if (elem_bytes != 2 && elem_bytes != 4) return fail(DDP_E_INVAL, "%s: elem_bytes = %d, not 2 or 4", fn, elem_bytes);
+    if (param_offset[0] != 0) return fail(DDP_E_INVAL, "%s: param_offset[0] = %lld, not 0", fn,
+                                          static_cast<long long>(param_offset[0]));
+    for (int32_t p = 0; p < r->nparams; ++p)
+        if (param_offset[p + 1] < param_offset[p])
+            return fail(DDP_E_INVAL, "%s: param_offset decreases at parameter %d", fn, p);
+    const int64_t row = param_offset[r->nparams];
+    if (row > 0 && !dev_in) return fail(DDP_E_INVAL, "%s: dev_in is NULL", fn);
+    if (r->W > 1 && dev_pitch < row * elem_bytes)
+        return fail(DDP_E_INVAL, "%s: dev_pitch %lld bytes below a row of %lld", fn, static_cast<long long>(dev_pitch),
+                    static_cast<long long>(row * elem_bytes));
+    auto* h = new ddp_host_front();
+    auto reject = [&](ddp_status st) {
+        h->release();
+        delete h;
+        return st;
+    };
+    h->r = r;
+    h->dev_in = static_cast<uint8_t*>(dev_in);
+    h->dev_pitch = dev_pitch;
+    h->elem = elem_bytes;
+    h->row_elems = row;
+    std::vector<std::vector<int32_t>> members(r->nbuckets);
+    for (int32_t p = 0; p < r->nparams; ++p) members[r->bucket_of[p]].push_back(p);
+    for (int32_t k = 0; k < r->nbuckets; ++k) {
+        ddp_host_front::Bucket B;
+        B.b = r->order[k];
+        const std::vector<int32_t>& mem = members[B.b];   // ascending
+        for (size_t i = 0; i < mem.size();) {
+            size_t j = i + 1;
+            while (j < mem.size() && mem[j] == mem[j - 1] + 1) ++j;
+            const int64_t lo = param_offset[mem[i]], hi = param_offset[mem[j - 1] + 1];
+            if (hi > lo) B.runs.emplace_back(lo, hi);
+            i = j;
+        }
+        B.params.assign(mem.rbegin(), mem.rend());
+        h->issue.push_back(std::move(B));
+    }
+    ddp_status st = DDP_OK;
+    if (!cuda_ok(cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking), "cudaStreamCreateWithFlags", &st) ||
+        !cuda_ok(cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking), "cudaStreamCreateWithFlags", &st) ||
+        !cuda_ok(cudaStreamCreateWithFlags(&h->gate, cudaStreamNonBlocking), "cudaStreamCreateWithFlags", &st) ||
+        !cuda_ok(cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming), "cudaEventCreateWithFlags", &st))
+        return reject(st);
+    h->reduced.assign(r->nbuckets, nullptr);
+    h->downloaded.assign(r->nbuckets, nullptr);
+    for (int32_t k = 0; k < r->nbuckets; ++k)
+        if (!cuda_ok(cudaEventCreateWithFlags(&h->reduced[k], cudaEventDisableTiming), "cudaEventCreateWithFlags", &st) ||
+            !cuda_ok(cudaEventCreateWithFlags(&h->downloaded[k], cudaEventDisableTiming), "cudaEventCreateWithFlags", &st))
+            return reject(st);
+    *out = h;
+    return ddp::ok();
+}
+
+extern "C" ddp_status ddp_host_front_step(ddp_host_front* h, const void* host_in, int64_t host_pitch, float* host_out,
+                                          void* stream)
+{
+    using ddp::fail;
+    const char* fn = "ddp_host_front_step";
+    if (!h) return fail(DDP_E_INVAL, "%s: handle is NULL", fn);
+    ddp_reducer* r = h->r;
+    if (h->row_elems > 0 && !host_in) return fail(DDP_E_INVAL, "%s: host_in is NULL", fn);
+    if (!host_out) return fail(DDP_E_INVAL, "%s: host_out is NULL", fn);
+    if (r->W > 1 && host_pitch < h->row_elems * h->elem)
+        return fail(DDP_E_INVAL, "%s: host_pitch %lld bytes below a row of %lld", fn, static_cast<long long>(host_pitch),
+                    static_cast<long long>(h->row_elems * h->elem));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ddp_status st = DDP_OK;
+    const int32_t nb = r->nbuckets;
+    if (h->first) {
+        if (!join_streams(h->h2d, s, h->join, &st) || !join_streams(r->side, s, h->join, &st)) return st;
+    } else {
+        // the previous step's reduction of each bucket, taken before prepare can
+        // issue this step's (its gradients may be overwritten after it)
+        for (int32_t k = 0; k < nb; ++k)
+            if (!cuda_ok(cudaStreamWaitEvent(h->gate, r->bdone[h->issue[k].b], 0), "cudaStreamWaitEvent", &st) ||
+                !cuda_ok(cudaEventRecord(h->reduced[k], h->gate), "cudaEventRecord", &st))
+                return st;
+        // and each bucket's reduction waits for the previous step's copy of it to the host
+        for (int32_t k = 0; k < nb; ++k) r->extra_gate[h->issue[k].b] = h->downloaded[k];
+    }
+    if (!join_streams(h->d2h, s, h->join, &st)) return st;
+    st = ddp_reducer_prepare(r, 0);
+    if (st != DDP_OK) return st;
+    for (int32_t k = 0; k < nb; ++k) {
+        const ddp_host_front::Bucket& B = h->issue[k];
+        if (!h->first && !cuda_ok(cudaStreamWaitEvent(h->h2d, h->reduced[k], 0), "cudaStreamWaitEvent", &st)) return st;
+        for (const auto& run : B.runs) {   // the W replicas' slices of a run, one pitch apart: one copy
+            const int64_t bytes = (run.second - run.first) * h->elem;
+            st = ddp_copy_rows(h->dev_in + run.first * h->elem, h->dev_pitch,
+                               static_cast<const uint8_t*>(host_in) + run.first * h->elem, host_pitch, bytes, r->W, h->h2d);
+            if (st != DDP_OK) return st;
+        }
+        h->ready.clear();
+        for (int32_t p : B.params)   // parameters prepare marked (unused everywhere) are not marked again
+            if (!r->marked[p]) h->ready.push_back(p);
+        if (!h->ready.empty()) {
+            st = ddp_reducer_mark_ready_many(r, h->ready.data(), static_cast<int32_t>(h->ready.size()), h->h2d);
+            if (st != DDP_OK) return st;
+        }
+    }
+    const int64_t stride = r->stride;
+    for (int32_t k = 0; k < nb; ++k) {
+        const int32_t b = h->issue[k].b;
+        st = ddp_reducer_wait_bucket(r, b, h->d2h);
+        if (st != DDP_OK) return st;
+        const int64_t lo = r->start[b], n = r->buckets[b].numel;
+        int64_t pitch = stride * 4, row = n * 4;
+        if (r->mode == DDP_REDUCE_SCATTER) {   // replica w's shard w: elements [w n / W, (w + 1) n / W) of the bucket
+            const int64_t kk = n / r->W;
+            pitch = (stride + kk) * 4;
+            row = kk * 4;
+        }
+        st = ddp_copy_rows(host_out + lo, pitch, r->mg + lo, pitch, row, r->W, h->d2h);
+        if (st != DDP_OK) return st;
+        if (!cuda_ok(cudaEventRecord(h->downloaded[k], h->d2h), "cudaEventRecord", &st)) return st;
+    }
+    st = ddp_reducer_finalize(r, stream, 0);
+    if (st != DDP_OK) return st;
+    if (!join_streams(s, h->d2h, h->join, &st)) return st;
+    h->first = false;
+    return ddp::ok();
+}
+
+extern "C" void ddp_host_front_destroy(ddp_host_front* h)
+{
+    if (!h) return;
+    h->release();
+    delete h;
 }

@@ -10,10 +10,10 @@ from __future__ import annotations
 import numpy as np
 
 from . import (DDP_BF16, DDP_F16, DDP_R_COALESCE, DDP_R_COPY_BACK, DDP_R_FUSED, DDP_R_TIMING, DDP_R_WIRE_BF16,
-               DDP_R_WIRE_F16, DDP_R_BUCKET_DONE, Plan, ddp_copy_rows, ddp_pack, ddp_pack_group,
-               ddp_reducer_wait_bucket,
+               DDP_R_WIRE_F16, DDP_R_BUCKET_DONE, Plan, ddp_pack, ddp_pack_group,
                ddp_reducer_bucket_ms, ddp_reducer_create,
                ddp_reducer_destroy, ddp_reducer_finalize, ddp_reducer_issue_log, ddp_reducer_mark_ready,
+               ddp_host_front_create, ddp_host_front_destroy, ddp_host_front_step,
                ddp_reducer_find_unused, ddp_reducer_mark_ready_many, ddp_reducer_prepare,
                ddp_reducer_ready_order, ddp_reducer_register_powersgd, ddp_reducer_set_local_used, DdpError)
 
@@ -162,18 +162,12 @@ class BucketReducer:
 
 
 class HostBucketReducer:
-    """Host-buffer front end of BucketReducer.  Each step copies every replica's
-    gradients from pinned host memory to the device, runs the synchronised
-    backward's bucket reduction, and copies the reduced buckets back.
-
-    The three run as a pipeline over the buckets in issue order: bucket b's
-    host-to-device copies go out on one copy stream and mark its parameters
-    ready (the reducer gates the bucket's reduction on them), and bucket b's
-    device-to-host copy waits for that bucket alone (ddp_reducer_wait_bucket)
-    on a second copy stream, so the two directions and the reductions overlap.
-    Consecutive steps overlap too, bucket by bucket: step k + 1's copies into
-    bucket b's gradients wait only for step k's reduction of bucket b, and its
-    reduction of bucket b only for step k's copy of bucket b to the host.
+    """Host-buffer front end of BucketReducer over ddp_host_front_*: each step
+    copies every replica's gradients from pinned host memory to the device, runs
+    the synchronised backward's bucket reduction, and copies the reduced buckets
+    back, as a pipeline over the buckets in issue order that also overlaps
+    consecutive steps bucket by bucket (the library's two copy streams and the
+    reducer's side stream; see ddp_host_front_step in the header).
 
     host_in   pinned [W, total] tensor (gradient dtype): replica w's gradients of
               all parameters back to back in parameter order.
@@ -195,29 +189,11 @@ class HostBucketReducer:
         grads = [[self.dev_in[w, self.offs[p]:self.offs[p + 1]] for p in range(len(numels))] for w in range(W)]
         self.reducer = BucketReducer(numels, dtypes, W, mode, order, cap_bytes, first_cap_bytes, pad_multiple, grads,
                                      used=used, fused=fused, timing=timing, coalesce=coalesce, bucket_done=True)
+        es = self.dev_in.element_size()
+        self.handle = ddp_host_front_create(self.reducer.handle, self.dev_in, self.dev_in.stride(0) * es, self.offs, es)
         plan = self.reducer.plan
-        # per bucket in issue order: its parameters as contiguous runs of the host layout
-        self.issue = []
-        for b in plan.bucket_order:
-            b = int(b)
-            mem = sorted(int(p) for p in plan.members[b])
-            runs, lo = [], mem[0] if mem else 0
-            for k in range(1, len(mem) + 1):
-                if k == len(mem) or mem[k] != mem[k - 1] + 1:
-                    runs.append((int(self.offs[lo]), int(self.offs[mem[k - 1] + 1])))
-                    if k < len(mem):
-                        lo = mem[k]
-            ready = [p for p in self.reducer.ready_order if plan.bucket_of[p] == b]
-            self.issue.append((b, runs, np.asarray(ready, np.int32)))
-        self.h2d = torch.cuda.Stream()
-        self.d2h = torch.cuda.Stream()
-        self.gate = torch.cuda.Stream()   # carries only waits and event records
-        # per bucket in issue order: the previous step's copy of it to the host is done
-        # (its main_grad may be overwritten); None before the first step
-        self.downloaded = None
-        self.h2d_bytes = int(self.offs[-1]) * W * self.dev_in.element_size()
-        self.reduce_scatter = int(mode) == 1
-        if self.reduce_scatter:
+        self.h2d_bytes = int(self.offs[-1]) * W * es
+        if int(mode) == 1:
             self.d2h_bytes = sum(int(plan.bucket_numel[b]) for b in range(plan.nbuckets)) * 4
         else:
             self.d2h_bytes = sum(int(plan.bucket_numel[b]) for b in range(plan.nbuckets)) * W * 4
@@ -229,68 +205,16 @@ class HostBucketReducer:
     def step(self, host_in, host_out, stream=None):
         import torch
 
-        r = self.reducer
-        plan = r.plan
         stream = torch.cuda.current_stream() if stream is None else stream
-        es = self.dev_in.element_size()
         if host_in.shape != self.dev_in.shape or host_in.dtype != self.dev_in.dtype or host_in.stride(1) != 1:
             raise ValueError(f"host_in must be a [W, total] {self.dev_in.dtype} tensor with contiguous rows")
         if host_out.dtype != torch.float32 or not host_out.is_contiguous() or \
                 host_out.numel() < self.W * self.reducer.plan.replica_stride:
             raise ValueError("host_out must be a contiguous fp32 tensor of W * replica_stride elements")
-        first = self.downloaded is None
-        if first:
-            self.h2d.wait_stream(stream)
-            r.side.wait_stream(stream)
-        else:
-            # a bucket with no parameter to mark (all of them unused everywhere) goes
-            # out at prepare: its main_grad must be on the host first
-            for i, (_, _, ready) in enumerate(self.issue):
-                if not len(ready):
-                    r.side.wait_event(self.downloaded[i])
-            # the previous step's completion of each bucket, taken before prepare starts
-            # this step (the gradients of bucket b are free once it is reduced)
-            reduced = []
-            for b, _, _ in self.issue:
-                ddp_reducer_wait_bucket(r.handle, b, self.gate)
-                ev = torch.cuda.Event()
-                ev.record(self.gate)
-                reduced.append(ev)
-        self.d2h.wait_stream(stream)
-        ddp_reducer_prepare(r.handle, 0)
-        with torch.cuda.stream(self.h2d):
-            for i, (b, runs, ready) in enumerate(self.issue):
-                if not first:
-                    self.h2d.wait_event(reduced[i])
-                for lo, hi in runs:   # the W replicas' slices of a run, one pitch apart: one copy
-                    ddp_copy_rows(self.dev_in.data_ptr() + lo * es, self.dev_in.stride(0) * es,
-                                  host_in.data_ptr() + lo * es, host_in.stride(0) * es, (hi - lo) * es, self.W,
-                                  self.h2d)
-                if not first:
-                    # and its main_grad once the previous step copied it to the host: the
-                    # side stream takes this wait just before the bucket's reduction
-                    r.side.wait_event(self.downloaded[i])
-                if len(ready):
-                    ddp_reducer_mark_ready_many(r.handle, ready, self.h2d)
-        stride = plan.replica_stride
-        downloaded = []
-        with torch.cuda.stream(self.d2h):
-            for b, _, _ in self.issue:
-                ddp_reducer_wait_bucket(r.handle, b, self.d2h)
-                lo, n = int(plan.bucket_start[b]), int(plan.bucket_numel[b])
-                if self.reduce_scatter:   # replica w's shard w: elements [w n / W, (w + 1) n / W) of the bucket
-                    k = n // self.W
-                    pitch, row = (stride + k) * 4, k * 4
-                else:
-                    pitch, row = stride * 4, n * 4
-                ddp_copy_rows(host_out.data_ptr() + lo * 4, pitch, r.main_grad.data_ptr() + lo * 4, pitch, row,
-                              self.W, self.d2h)
-                ev = torch.cuda.Event()
-                ev.record(self.d2h)
-                downloaded.append(ev)
-        self.downloaded = downloaded
-        ddp_reducer_finalize(r.handle, stream, 0)
-        stream.wait_stream(self.d2h)
+        ddp_host_front_step(self.handle, host_in, host_in.stride(0) * host_in.element_size(), host_out, stream)
 
     def close(self):
+        if self.handle is not None:
+            ddp_host_front_destroy(self.handle)   # before the reducer it gates
+            self.handle = None
         self.reducer.close()

@@ -927,6 +927,50 @@ ddp_status ddp_wait_selftest(int32_t arrive, int64_t limit_ns, void* stream);
 ddp_status ddp_copy_rows(void* dst, int64_t dst_pitch, const void* src, int64_t src_pitch, int64_t row_bytes,
                          int64_t rows, void* stream);
 
+/*
+ * The host-buffer front end of a reducer: per step, every replica's gradients
+ * from pinned host memory to the device, the reducer's iteration (all
+ * parameters marked ready as their bucket's copies land), and each reduced
+ * bucket back to pinned host memory as soon as that bucket is done ("Megatron
+ * DDP: contiguous buffer and overlap" section 3: a consumer may start on a
+ * bucket once its reduction finishes).  The three run as a pipeline over the
+ * buckets in issue order on two copy streams of the front end's own, and
+ * consecutive steps overlap bucket by bucket: step k + 1's copies into bucket
+ * b's gradients wait for step k's reduction of b, and its reduction of b waits
+ * for step k's copy of b to the host.  The pages have no counterpart (their
+ * gradients are on the device already); this is the library's entry for
+ * callers whose data lives in host memory.
+ *
+ * ddp_host_front_create
+ *   r            a reducer built with DDP_R_BUCKET_DONE and a main_grad, not a
+ *                dry run.  The front end must be destroyed before it.
+ *   dev_in       DEVICE: the gradient buffer the reducer's pointer table points
+ *                into, W rows `dev_pitch` bytes apart; parameter p occupies
+ *                elements [param_offset[p], param_offset[p + 1]) of each row.
+ *   param_offset HOST int64[nparams + 1], non-decreasing, param_offset[0] = 0.
+ *   elem_bytes   the gradients' element size (4: fp32; 2: bf16 or fp16).
+ *   Errors: DDP_E_INVAL (a NULL or inconsistent argument, a dry-run reducer,
+ *   no DDP_R_BUCKET_DONE, no main_grad); DDP_E_CUDA (streams or events).
+ *
+ * ddp_host_front_step -- one step, enqueued (nothing waits on the host).
+ *   host_in      HOST, pinned: W rows `host_pitch` bytes apart in dev_in's layout.
+ *   host_out     HOST, pinned fp32, W x replica_stride elements in main_grad's
+ *                layout.  Allreduce: every bucket's elements are written (the
+ *                alignment gaps between buckets are not); reduce_scatter: row w
+ *                receives only shard w of each bucket.
+ *   stream       waits for the whole step (the last copy to the host); the
+ *                host buffers must stay untouched until then.  The first step
+ *                also waits for what `stream` holds when it is called.
+ *   Errors: DDP_E_INVAL (a NULL buffer, a pitch below a row); the reducer's
+ *   errors (a parameter marked twice, DDP_E_STATE); DDP_E_CUDA.
+ */
+typedef struct ddp_host_front ddp_host_front;
+ddp_status ddp_host_front_create(ddp_reducer* r, void* dev_in, int64_t dev_pitch, const int64_t* param_offset,
+                                 int32_t elem_bytes, ddp_host_front** out);
+ddp_status ddp_host_front_step(ddp_host_front* h, const void* host_in, int64_t host_pitch, float* host_out,
+                               void* stream);
+void ddp_host_front_destroy(ddp_host_front* h);
+
 /* ------------------------------------------------------------------------ */
 /* Errors and version                                                        */
 /* ------------------------------------------------------------------------ */

@@ -129,3 +129,28 @@ def test_reducer_from_plan_dry_run():
         assert D.ddp_reducer_issue_log(r) == [int(b) for b in d["bucket_order"]]
     finally:
         D.ddp_reducer_destroy(r)
+
+
+def test_host_front_rejects_bad_arguments():
+    """ddp_host_front_create checks its arguments before touching CUDA: a dry-run
+    reducer, NULL arguments."""
+    wl = WL.c1_mlp()
+    h = D.ddp_plan_create(wl.numels, None, wl.cap_bytes, wl.first_cap_bytes, wl.order, wl.pad_multiple)
+    d = D.ddp_plan_describe(h)
+    descs = D.ddp_plan_bucket_descs(h, d["nbuckets"], 0x10000, 0x20000)
+    r = D.ddp_reducer_create_from_plan(h, descs, wl.W, wl.mode, D.DDP_R_DRY_RUN | D.DDP_R_FUSED | D.DDP_R_BUCKET_DONE)
+    D.ddp_plan_destroy(h)
+    offs = np.concatenate([[0], np.cumsum(wl.numels)]).astype(np.int64)
+    try:
+        with pytest.raises(D.DdpError) as e:
+            D.ddp_host_front_create(r, 0x1000, int(offs[-1]) * 4, offs, 4)   # dry run
+        assert e.value.status == D.DDP_E_INVAL
+        out = D._vp()
+        st = D.lib().ddp_host_front_create(r, D._vp(0x1000), int(offs[-1]) * 4, None, 4, C.byref(out))
+        assert st == D.DDP_E_INVAL and not out.value
+        st = D.lib().ddp_host_front_create(None, D._vp(0x1000), 4, D._cp(offs, D._i64p), 4, C.byref(out))
+        assert st == D.DDP_E_INVAL
+        assert D.lib().ddp_host_front_create(r, None, 0, D._cp(offs, D._i64p), 4, None) == D.DDP_E_INVAL
+    finally:
+        D.ddp_reducer_destroy(r)
+    D.ddp_host_front_destroy(None)   # a NULL handle is ignored
