@@ -29,8 +29,10 @@
  *     arrays of the module (the status word of ddp_device_status, the
  *     streaming kernels' pool counters, and the scratch of
  *     ddp_powersgd_reduce_static).  A reducer owns host bookkeeping and the
- *     CUDA events it creates, released by ddp_reducer_destroy; the library
- *     keeps up to 64 events per device for the pool counters until exit.
+ *     CUDA events it creates, released by ddp_reducer_destroy; a host front end
+ *     owns two copy streams, one gate stream and its events, released by
+ *     ddp_host_front_destroy; the library keeps up to 64 events per device for
+ *     the pool counters until exit.
  *   - Streams: `stream` arguments are cudaStream_t handles passed as void*
  *     (NULL = the legacy default stream).  Data-path calls are asynchronous on
  *     that stream; only ddp_reducer_finalize with a timeout waits on the host.
@@ -47,8 +49,9 @@
  *     threads at once and for several devices in one process (the launch
  *     caches -- occupancy, function attributes, symbol addresses -- are kept
  *     per device, in atomics), with these exceptions: a reducer, a plan
- *     under construction and a PowerSGD state are used by one thread at a
- *     time, and ddp_set_kernel_variant is process-wide.  Kernels launch on the
+ *     under construction, a PowerSGD state and a host front end (with its
+ *     reducer) are used by one thread at a time, and ddp_set_kernel_variant is
+ *     process-wide.  Kernels launch on the
  *     device that is current in the calling thread; pointers must belong to it.
  */
 #ifndef DDP_BUCKET_H
